@@ -1,0 +1,280 @@
+"""Pins of the fp64 oracle to facts fixed outside itself (CPU only).
+
+Each test targets a plausible mistake: a dropped softmax term or normalisation (one token,
+identical keys), a wrong sign / base / missing scale in the exponent (two-key logistic), a
+transposed or mis-indexed gather (permutation, library comparison, one-hot keys), a wrong GQA
+head map, a wrong bf16 decode, a wrong INT8 scale index, a wrong merge weight.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+F64_TOL = 1e-12
+
+
+def _pool_from_contiguous(K, V, perm_seed=None):
+    """Lay contiguous per-sequence K/V [B, n, Hkv, D] (all n equal) into a 16-token block pool
+    with either identity or shuffled block tables. Built here, independently of workloads."""
+    B, n, Hkv, D = K.shape
+    BS = 16
+    nb = -(-n // BS)
+    NB = B * nb
+    ids = np.arange(NB, dtype=np.int32)
+    if perm_seed is not None:
+        ids = np.random.default_rng(perm_seed).permutation(NB).astype(np.int32)
+    bt = ids.reshape(B, nb)
+    kp = np.zeros((NB, Hkv, BS, D), K.dtype)
+    vp = np.zeros((NB, Hkv, BS, D), V.dtype)
+    for b in range(B):
+        for t in range(n):
+            kp[bt[b, t // BS], :, t % BS, :] = K[b, t]
+            vp[bt[b, t // BS], :, t % BS, :] = V[b, t]
+    return kp, vp, bt, np.full(B, n, np.int32)
+
+
+def test_bf16_bit_patterns(orc):
+    cases = {0x3F80: 1.0, 0xC000: -2.0, 0x3E80: 0.25, 0x0000: 0.0, 0x3F81: 1.0 + 2.0 ** -7,
+             0x4049: 3.140625, 0x0001: 2.0 ** -133, 0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127}
+    for bits, val in cases.items():
+        assert orc.bf16_to_double(bits) == val, hex(bits)
+    assert math.isinf(orc.bf16_to_double(0x7F80))
+    assert math.copysign(1.0, orc.bf16_to_double(0x8000)) == -1.0
+
+
+@pytest.mark.parametrize("kv", ["f32", "bf16", "i8"])
+def test_single_token_returns_v(orc, kv):
+    """context_len 1: softmax over one score is exactly 1, so out = v_0."""
+    w = W.make_decode(name="t", B=3, Hq=4, Hkv=2, D=64, context_lens=[1, 1, 1], kv_dtype=kv,
+                      q_dtype="f32" if kv == "f32" else "bf16", seed=7)
+    out = orc.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                     w.scale, w.k_scales, w.v_scales)
+    for b in range(w.B):
+        blk = w.block_tables[b, 0]
+        for h in range(w.Hq):
+            v = w.v_pool[blk, h // 2, 0]
+            if kv == "bf16":
+                v = W.bf16_bits_to_f32(v).astype(np.float64)
+            elif kv == "i8":
+                v = v.astype(np.float64) * np.float64(w.v_scales[blk, h // 2, 0])
+            np.testing.assert_array_equal(out[b, h], np.asarray(v, np.float64))
+
+
+def test_identical_keys_give_mean_of_v(orc):
+    """All keys equal -> uniform weights -> out = mean_t v_t."""
+    rng = np.random.default_rng(3)
+    B, n, Hkv, D = 2, 37, 2, 64
+    K = np.broadcast_to(rng.standard_normal((1, 1, Hkv, D)), (B, n, Hkv, D)).astype(np.float32)
+    V = rng.standard_normal((B, n, Hkv, D)).astype(np.float32)
+    kp, vp, bt, cl = _pool_from_contiguous(K, V, perm_seed=1)
+    q = rng.standard_normal((B, 4, D)).astype(np.float32)
+    out = orc.paged_decode_attention(q, kp, vp, bt, cl, 0.125)
+    for b in range(B):
+        for h in range(4):
+            np.testing.assert_allclose(out[b, h], V[b, :, h // 2].astype(np.float64).mean(0),
+                                       rtol=0, atol=F64_TOL)
+
+
+def test_two_key_logistic_weights(orc):
+    """Keys e_0 and 0, query a*e_0: scores scale*a and 0, so the weight of key 0 is the
+    logistic 1 / (1 + exp(-scale*a)) (natural base, scale applied once)."""
+    D = 64
+    K = np.zeros((1, 2, 1, D), np.float32)
+    K[0, 0, 0, 0] = 1.0
+    V = np.zeros((1, 2, 1, D), np.float32)
+    V[0, 0, 0, :] = np.arange(D)
+    V[0, 1, 0, :] = -1.0
+    kp, vp, bt, cl = _pool_from_contiguous(K, V)
+    for a, scale in [(2.0, 0.5), (3.0, 1.0 / 8.0), (-4.0, 0.25)]:
+        q = np.zeros((1, 1, D), np.float32)
+        q[0, 0, 0] = a
+        out = orc.paged_decode_attention(q, kp, vp, bt, cl, scale)
+        w0 = 1.0 / (1.0 + math.exp(-scale * a))
+        expect = w0 * np.arange(D) + (1.0 - w0) * -1.0
+        np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=F64_TOL)
+
+
+def test_one_hot_keys_select_value(orc):
+    """Orthogonal keys and a query aligned with key j at a large scale: out -> v_j."""
+    D, n = 64, 40
+    K = np.zeros((1, n, 1, D), np.float32)
+    for t in range(n):
+        K[0, t, 0, t] = 1.0
+    V = np.random.default_rng(5).standard_normal((1, n, 1, D)).astype(np.float32)
+    kp, vp, bt, cl = _pool_from_contiguous(K, V, perm_seed=4)
+    for j in (0, 15, 16, 39):
+        q = np.zeros((1, 1, D), np.float32)
+        q[0, 0, j] = 1.0
+        out = orc.paged_decode_attention(q, kp, vp, bt, cl, 60.0)
+        # every other weight is exp(-60) relative: far below the tolerance
+        np.testing.assert_allclose(out[0, 0], V[0, j, 0], rtol=0, atol=1e-20)
+
+
+def test_gqa_head_map_is_contiguous_groups(orc):
+    """Hq=8, Hkv=2: query heads 0-3 read kv head 0 and 4-7 read kv head 1."""
+    D, n = 64, 20
+    rng = np.random.default_rng(9)
+    K = rng.standard_normal((1, n, 2, D)).astype(np.float32)
+    V = np.empty((1, n, 2, D), np.float32)
+    V[:, :, 0, :] = 1.0
+    V[:, :, 1, :] = 2.0
+    kp, vp, bt, cl = _pool_from_contiguous(K, V)
+    q = rng.standard_normal((1, 8, D)).astype(np.float32)
+    out = orc.paged_decode_attention(q, kp, vp, bt, cl, 0.125)
+    for h in range(8):
+        np.testing.assert_allclose(out[0, h], np.full(D, 1.0 + h // 4), rtol=0, atol=F64_TOL)
+
+
+@pytest.mark.parametrize("g,D,n", [(1, 64, 1), (4, 128, 33), (2, 64, 100), (8, 128, 47)])
+def test_matches_library_attention_on_contiguous_kv(orc, g, D, n):
+    """Against torch's scaled_dot_product_attention in float64 on CPU (a library routine the
+    oracle does not use), with the K/V laid out through shuffled block tables."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(g * 1000 + n)
+    B, Hkv = 3, 2
+    Hq = Hkv * g
+    K = rng.standard_normal((B, n, Hkv, D)).astype(np.float32)
+    V = rng.standard_normal((B, n, Hkv, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    kp, vp, bt, cl = _pool_from_contiguous(K, V, perm_seed=n)
+    scale = 1.0 / math.sqrt(D)
+    out = orc.paged_decode_attention(q, kp, vp, bt, cl, scale)
+    tq = torch.from_numpy(q.astype(np.float64)).unsqueeze(2)             # [B, Hq, 1, D]
+    tk = torch.from_numpy(K.astype(np.float64)).permute(0, 2, 1, 3)      # [B, Hkv, n, D]
+    tv = torch.from_numpy(V.astype(np.float64)).permute(0, 2, 1, 3)
+    tk = tk.repeat_interleave(g, dim=1)
+    tv = tv.repeat_interleave(g, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+    np.testing.assert_allclose(out, ref[:, :, 0].numpy(), rtol=0, atol=1e-12)
+
+
+def test_block_permutation_is_bit_identical(orc):
+    w = W.make_config(2, B=4, ctx_lo=40, ctx_hi=300)
+    p = W.permute_blocks(w, seed=77)
+    assert not np.array_equal(w.block_tables, p.block_tables)
+    a = orc.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    b = orc.paged_decode_attention(p.q, p.k_pool, p.v_pool, p.block_tables, p.context_lens, p.scale)
+    assert np.array_equal(a, b)
+
+
+def test_shared_prefix_equals_copy_on_write(orc):
+    w = W.make_config(5, B=5, ctx_lo=16, ctx_hi=70, prefix_tokens=64)
+    assert (w.ref_count[w.block_tables[0, :4]] == 5).all()
+    c = W.unshare_prefix(w)
+    assert c.ref_count.max() == 1
+    a = orc.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    b = orc.paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.context_lens, c.scale)
+    assert np.array_equal(a, b)
+
+
+def test_int8_dequant_uses_per_token_scales(orc):
+    """Two tokens; K zero so weights are 1/2 each; out = (v0*s0 + v1*s1) / 2 with each token's
+    own V scale (a wrong scale index -- K's, or the other token's -- fails)."""
+    D = 64
+    kp = np.zeros((2, 1, 16, D), np.int8)
+    vp = np.zeros((2, 1, 16, D), np.int8)
+    vp[1, 0, 0, :] = np.arange(D) - 32
+    vp[0, 0, 0, :] = 7
+    ks = np.full((2, 1, 16), 3.0, np.float32)
+    vs = np.zeros((2, 1, 16), np.float32)
+    vs[1, 0, 0] = 0.5
+    vs[0, 0, 0] = 0.25
+    bt = np.array([[1, 0]], np.int32)  # token 0 -> block 1, token 16 -> block 0
+    cl = np.array([17], np.int32)
+    q = W.f32_to_bf16_bits(np.ones((1, 1, D), np.float32))
+    # tokens 1..15 of block 1 are zero K and zero V with scale 0: they carry weight too
+    out = orc.paged_decode_attention(q, kp, vp, bt, cl, 1.0, ks, vs)
+    expect = ((np.arange(D) - 32) * 0.5 + 7 * 0.25) / 17.0
+    np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=F64_TOL)
+
+
+def test_context_len_zero_gives_zeros(orc):
+    w = W.make_decode(name="z", B=3, Hq=2, Hkv=1, D=64, context_lens=[0, 5, 0], kv_dtype="f32",
+                      q_dtype="f32", seed=1)
+    out = orc.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0) and np.all(np.isfinite(out))
+    assert np.any(out[1] != 0)
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 64, 256, 512])
+def test_split_merge_equals_unsplit(orc, chunk):
+    w = W.make_config(2, B=5, ctx_lo=1, ctx_hi=700, seed=11)
+    w.context_lens[0] = 0
+    maxn = w.max_context_len
+    S = max(1, maxn // chunk)
+    m, l, acc, ns = orc.paged_decode_partials(w.q, w.k_pool, w.v_pool, w.block_tables,
+                                              w.context_lens, w.scale, chunk, S)
+    merged = orc.merge_partials(m, l, acc, ns)
+    full = orc.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    np.testing.assert_allclose(merged, full, rtol=1e-12, atol=1e-13)
+    for b, n in enumerate(w.context_lens):
+        assert ns[b] == orc.split_count(n, chunk, S)[0]
+
+
+def test_split_rule_closed_forms(orc):
+    """split_num = max(1, n // chunk) from the FlashDecoding notes, whole blocks per split,
+    no empty split, capped by the grid extent."""
+    assert orc.split_count(0, 512, 8) == (1, 0)
+    assert orc.split_count(100, 512, 8) == (1, 112)
+    assert orc.split_count(511, 512, 8) == (1, 512)
+    assert orc.split_count(512, 512, 8) == (1, 512)
+    assert orc.split_count(2560, 512, 8) == (5, 512)
+    assert orc.split_count(2561, 512, 8) == (5, 528)
+    assert orc.split_count(131072, 512, 256) == (256, 512)
+    assert orc.split_count(131072, 512, 64) == (64, 2048)  # capped
+    for n in range(1, 400):
+        for chunk in (16, 32, 48, 256):
+            ns, per = orc.split_count(n, chunk, 1 << 20)
+            assert per % 16 == 0 and per > 0
+            assert ns <= max(1, n // chunk)
+            assert (ns - 1) * per < n <= ns * per  # covers [0, n), last split non-empty
+
+
+def test_kv_write_hand_offsets(orc):
+    """Slot s goes to block s // 16, row s % 16 of every kv head; nothing else changes;
+    negative slots are skipped; out-of-range slots are reported."""
+    NB, Hkv, BS, D = 4, 2, 16, 64
+    sentinel = np.float32(-777.0)
+    kp = np.full((NB, Hkv, BS, D), sentinel, np.float32)
+    vp = np.full((NB, Hkv, BS, D), sentinel, np.float32)
+    kn = np.arange(3 * Hkv * D, dtype=np.float32).reshape(3, Hkv, D)
+    vn = -kn
+    slots = np.array([17, -1, 63], np.int64)
+    k2, v2, _, _ = orc.kv_cache_write(kn, vn, kp, vp, slots)
+    flat_k = k2.reshape(-1)
+    row = lambda blk, h, off: ((blk * Hkv + h) * BS + off) * D  # noqa: E731
+    np.testing.assert_array_equal(flat_k[row(1, 0, 1):row(1, 0, 1) + D], kn[0, 0])
+    np.testing.assert_array_equal(flat_k[row(1, 1, 1):row(1, 1, 1) + D], kn[0, 1])
+    np.testing.assert_array_equal(flat_k[row(3, 1, 15):row(3, 1, 15) + D], kn[2, 1])
+    changed = np.argwhere(np.any(k2 != sentinel, axis=-1))
+    assert sorted(map(tuple, changed)) == [(1, 0, 1), (1, 1, 1), (3, 0, 15), (3, 1, 15)]
+    np.testing.assert_array_equal(v2[1, :, 1], vn[0])
+    with pytest.raises(RuntimeError, match="slot"):
+        orc.kv_cache_write(kn, vn, kp, vp, np.array([0, 64, 1], np.int64))
+
+
+def test_kv_write_int8_moves_scales(orc):
+    NB, Hkv, BS, D = 2, 1, 16, 64
+    kp = np.zeros((NB, Hkv, BS, D), np.int8)
+    vp = np.zeros_like(kp)
+    ks = np.zeros((NB, Hkv, BS), np.float32)
+    vs = np.zeros_like(ks)
+    kn = np.full((1, Hkv, D), 5, np.int8)
+    vn = np.full((1, Hkv, D), -3, np.int8)
+    k2, v2, ks2, vs2 = orc.kv_cache_write(kn, vn, kp, vp, np.array([20], np.int64),
+                                          np.array([[0.5]], np.float32),
+                                          np.array([[0.25]], np.float32), ks, vs)
+    assert (k2[1, 0, 4] == 5).all() and (v2[1, 0, 4] == -3).all()
+    assert ks2[1, 0, 4] == 0.5 and vs2[1, 0, 4] == 0.25
+    assert np.count_nonzero(ks2) == 1 and np.count_nonzero(k2) == D
+
+
+def test_write_then_attend_sees_new_token(orc):
+    """Ordering: the step writes the new token, then attends over context_lens that count it."""
+    w = W.make_config(1)
+    kp, vp, _, _ = orc.kv_cache_write(w.k_new, w.v_new, w.k_pool, w.v_pool, w.slot_mapping)
+    out = orc.paged_decode_attention(w.q, kp, vp, w.block_tables, w.context_lens, w.scale)
+    # sequence 0 has one token: the new one
+    np.testing.assert_array_equal(out[0], w.v_new[0].astype(np.float64))
