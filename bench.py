@@ -1,0 +1,437 @@
+"""Benchmark of one paged-KV decode step on GB300: slot-mapped KV write + split-K paged decode
+attention (split kernel + merge kernel), through the C ABI, on a seeded synthetic workload.
+
+Prints one JSON line. `value` is algorithmic KV GB/s of the whole step (bytes the step must move
+divided by device time), `tokens_per_s` the decoded tokens per second of that one attention
+layer. L2 is flushed (a 512 MB write, outside the timed events) before every step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--chunk T]
+    python bench.py --impl reference ...   # the fp64 oracle on the host cores, same metric
+
+For N > 1 it runs under torchrun, one rank per GPU; every rank decodes its own batch (a seed
+of its own: weak scaling, no data-path collective); the barrier, the max over ranks and the
+sum of bytes are the only communication.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn: KV GB/s vs GB300 HBM peak; decoded tokens/s per step"
+DEFAULT_CONFIG = 2          # the Llama-3-8B-shaped GQA decode: the metric's workload
+FALLBACK_HBM_GBS = 6800.0   # used only when MEASURED_PEAKS.json is absent
+L2_FLUSH_BYTES = 512 << 20
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "paged_kv_decode_reshape_gb300", "csrc")
+
+
+# ------------------------------------------------------------------------------------------
+# host-side pieces (no GPU needed; covered by tests/test_bench_host.py)
+# ------------------------------------------------------------------------------------------
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment (1 process otherwise)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def rank_seed(cfg: int, rank: int) -> int:
+    """Each rank decodes its own batch: the config's seed for rank 0, distinct ones after."""
+    return cfg + 1000 * rank
+
+
+def aggregate(local_bytes: float, local_ms: float, group=None):
+    """Whole-job (bytes, ms): bytes summed over ranks, time the max over ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_bytes, local_ms
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_bytes], dtype=torch.float64, device=dev)
+    m = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item()), float(m.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary for this
+    workload, if the kernel sources are unchanged since the capture (else None)."""
+    path = os.path.join(PROFILES, f"split_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def attention_bytes(w: W.DecodeWorkload) -> int:
+    """Algorithmic bytes of the attention call alone (KV + scales + q + out + tables)."""
+    elem = {"f32": 4, "bf16": 2, "i8": 1}[w.kv_dtype]
+    per_tok = w.Hkv * w.D * elem * 2 + (w.Hkv * 8 if w.kv_dtype == "i8" else 0)
+    written = int((w.slot_mapping >= 0).sum())
+    wr = written * per_tok * 2 + 8 * w.T
+    return W.kv_bytes(w) - wr
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        with open(self.path) as f:
+            rows = [r.strip() for r in f if r.strip()]
+        os.unlink(self.path)
+        return parse_clock_rows(rows)
+
+
+def parse_clock_rows(rows):
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        parts = [p.strip() for p in r.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx = float(parts[2])
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def cuda_launches_per_step(w: W.DecodeWorkload, chunk_used: int) -> int:
+    """Kernels of this library one step launches: write, split, and merge when any split."""
+    splits = max(1, w.max_context_len // chunk_used)
+    return 2 + (1 if splits > 1 else 0)
+
+
+# ------------------------------------------------------------------------------------------
+# the fp64 oracle on the host cores (cpu_baseline and --impl reference)
+# ------------------------------------------------------------------------------------------
+
+def oracle_step_seconds(w: W.DecodeWorkload, rows, threads: int) -> float:
+    import oracle
+    kp, vp = w.k_pool, w.v_pool
+    ks, vs = w.k_scales, w.v_scales
+    rows = np.asarray(rows)
+    t0 = time.perf_counter()
+    oracle.kv_cache_write(w.k_new[rows], w.v_new[rows], kp, vp, w.slot_mapping[rows],
+                          None if w.k_new_scales is None else w.k_new_scales[rows],
+                          None if w.v_new_scales is None else w.v_new_scales[rows],
+                          ks, vs, inplace=True)
+    oracle.paged_decode_attention(w.q[rows], kp, vp, w.block_tables[rows], w.context_lens[rows],
+                                  w.scale, ks, vs, num_threads=threads)
+    return time.perf_counter() - t0
+
+
+def sample_rows(w: W.DecodeWorkload, cpu_budget_s: float):
+    """A prefix of the batch whose oracle step costs about cpu_budget_s seconds of CPU time,
+    from a single-thread probe of the first sequence."""
+    t0 = oracle_step_seconds(w, [0], 1)
+    per_tok = t0 / max(1, int(w.context_lens[0]))
+    n, cost = 0, 0.0
+    while n < w.B and cost + int(w.context_lens[n]) * per_tok <= cpu_budget_s:
+        cost += int(w.context_lens[n]) * per_tok
+        n += 1
+    return list(range(max(1, n)))
+
+
+def sample_bytes(w: W.DecodeWorkload, rows) -> int:
+    rows = np.asarray(rows)
+    sub = W.DecodeWorkload(**{**w.__dict__, "B": len(rows), "q": w.q[rows],
+                              "block_tables": w.block_tables[rows],
+                              "context_lens": w.context_lens[rows],
+                              "slot_mapping": w.slot_mapping[rows], "k_new": w.k_new[rows],
+                              "v_new": w.v_new[rows], "shared_prefix_blocks": 0})
+    if w.shared_prefix_blocks and len(rows) > 1:
+        sub.shared_prefix_blocks = w.shared_prefix_blocks
+    return W.kv_bytes(sub)
+
+
+def cpu_baseline(w: W.DecodeWorkload, cpu_budget_s: float = 20.0):
+    threads = os.cpu_count() or 1
+    rows = sample_rows(w, cpu_budget_s)
+    secs = oracle_step_seconds(w, rows, threads)
+    gbs = sample_bytes(w, rows) / secs / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {w.B} sequences of the {w.name} step (write + attention, "
+                      f"all {w.Hq} heads), fp64 C oracle, {threads} threads, {secs:.2f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return  # the oracle leg runs on rank 0 only
+    w = W.make_config(args.config, seed=rank_seed(args.config, 0))
+    threads = os.cpu_count() or 1
+    steps = max(1, args.steps)
+    # the whole run stays near two minutes of wall time on `threads` cores
+    rows = sample_rows(w, max(0.05, 120.0 * threads / (steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_step_seconds(w, rows, threads)
+    secs = sum(oracle_step_seconds(w, rows, threads) for _ in range(steps))
+    nbytes = sample_bytes(w, rows)
+    gbs = nbytes * steps / secs / 1e9
+    ms = secs / steps * 1e3
+    sample = (f"{len(rows)} of {w.B} sequences of the {w.name} step per timed step "
+              f"(write + attention, all heads), fp64 C oracle, {threads} threads")
+    line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "description": W.CONFIGS[args.config]},
+            "tokens_per_s": round(len(rows) * steps / secs, 2),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# the CUDA path
+# ------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_decode_reshape_gb300 as pkv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    pkv.load(build_if_missing=False)
+    dev = torch.device("cuda", local)
+
+    w = W.make_config(args.config, seed=rank_seed(args.config, rank))
+
+    def up(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    q, kp, vp = up(w.q), up(w.k_pool), up(w.v_pool)
+    ks, vs = up(w.k_scales), up(w.v_scales)
+    bt, cl, sm = up(w.block_tables), up(w.context_lens), up(w.slot_mapping)
+    kn, vn = up(w.k_new), up(w.v_new)
+    kns, vns = up(w.k_new_scales), up(w.v_new_scales)
+    out = torch.empty_like(q)
+    maxc = w.max_context_len
+    chunk = pkv.decode_split_chunk(w.B, maxc, args.chunk)
+    nws = pkv.decode_workspace_bytes(w.B, w.Hq, w.D, maxc, args.chunk)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def write():
+        pkv.kv_cache_write(kn, vn, kp, vp, sm, kns, vns, ks, vs, status=status, stream=stream)
+
+    def attend():
+        if w.kv_dtype == "i8":
+            pkv.paged_decode_attention_int8(out, q, kp, vp, ks, vs, bt, cl, maxc, w.scale,
+                                            args.chunk, ws, status, stream)
+        else:
+            pkv.paged_decode_attention(out, q, kp, vp, bt, cl, maxc, w.scale, args.chunk, ws,
+                                       status, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        write()
+        attend()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"kernels flagged bad inputs: status {int(status.item())}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for k in range(K):
+        flush.fill_(k & 0xFF)            # evict the previous step's lines (not timed)
+        ev[k][0].record(stream)
+        write()
+        ev[k][1].record(stream)
+        attend()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall_s = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+
+    step_bytes = W.kv_bytes(w)
+    total_bytes, max_ms = aggregate(step_bytes * K, step_ms)
+    ms_per_step = max_ms / K
+    value = total_bytes / (max_ms / 1e3) / 1e9
+    tokens_per_s = w.B * world * K / (max_ms / 1e3)
+
+    # e2e through the public API: inputs from pinned host memory each step, out read back
+    host_in = {n: t.cpu().pin_memory() for n, t in
+               dict(q=q, bt=bt, cl=cl, sm=sm, kn=kn, vn=vn).items()}
+    if kns is not None:
+        host_in.update(kns=kns.cpu().pin_memory(), vns=vns.cpu().pin_memory())
+    dev_in = dict(q=q, bt=bt, cl=cl, sm=sm, kn=kn, vn=vn, kns=kns, vns=vns)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = out.numel() * out.element_size()
+    KE = max(1, min(K, 200))
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
+    torch.cuda.synchronize()
+    for k in range(KE):
+        flush.fill_(k & 0xFF)
+        ee[k][0].record(stream)
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        write()
+        attend()
+        host_out.copy_(out, non_blocking=True)
+        ee[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in ee)
+    e2e_bytes, e2e_max = aggregate(step_bytes * KE, e2e_ms)
+    e2e_value = e2e_bytes / (e2e_max / 1e3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, peak_kind = measured_peaks()
+    attn_bytes = attention_bytes(w)
+    attn_avg_s = attn_ms / K / 1e3
+    achieved = attn_bytes / attn_avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "f32": "f32", "i8": "i8"}[w.kv_dtype], "data": "synthetic",
+        "config": {"workload": w.name, "description": W.CONFIGS[args.config],
+                   "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+                   "block_size": w.BS, "mean_context": float(w.context_lens.mean()),
+                   "max_context": maxc, "split_chunk": chunk,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write, untimed)",
+                   "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "peak_kind": f"of {peak_kind}",
+                     "kernel": "paged decode attention call (split kernel + merge kernel)",
+                     "traffic": profiled_traffic(w.name),
+                     "algorithmic_bytes_per_launch": attn_bytes,
+                     "avg_launch_us": round(attn_avg_s * 1e6, 3)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": KE},
+        "gpu_launches": cuda_launches_per_step(w, chunk) * K,
+        "wall_s": round(wall_s, 3),
+    }
+    if clk is not None:
+        line["clocks"] = clk
+    if not args.no_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
+    ap.add_argument("--chunk", type=int, default=0, help="split chunk in tokens (0 = auto)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: paged KV-cache decode on one NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, each the GPU form of a step the pages describe:
+ *   pkv_kv_cache_write                 -- store the new tokens' K and V into their slots of the
+ *                                         paged pool ("AMD ATOM inference engine", introduction:
+ *                                         the request-lifecycle step of writing into the KV
+ *                                         cache; section 5.1: 16-token blocks, one block table
+ *                                         per sequence).
+ *   pkv_paged_decode_attention         -- decode attention that gathers K and V through the
+ *                                         block tables ("LLM Primer VI, Chapter 8", section 8.1)
+ *                                         with split-K online softmax and a second merge kernel
+ *                                         ("EchoLLMServing inference framework notes", section 2,
+ *                                         PagedAttention V2 and FlashDecoding).
+ *   pkv_paged_decode_attention_int8    -- the same over an INT8 K/V cache with per-token scales,
+ *                                         dequantised inside the kernel (same notes, section 3).
+ *
+ * Layouts (all row-major, element strides implied by the shapes):
+ *   q, out       [num_seqs][num_q_heads][head_dim]
+ *   k_new, v_new [num_tokens][num_kv_heads][head_dim]
+ *   k/v pool     [num_blocks][num_kv_heads][block_size][head_dim]
+ *   k/v scales   [num_blocks][num_kv_heads][block_size]      (fp32, INT8 pools only)
+ *   block_tables [num_seqs][max_blocks_per_seq] int32; entry j of row b is the physical block
+ *                holding logical tokens [16 j, 16 j + 16) of sequence b
+ *   context_lens [num_seqs] int32: tokens of each sequence, counting this step's new token
+ *   slot_mapping [num_tokens] int64: physical slot block * block_size + offset; < 0 = padding
+ * Query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: every array pointer is DEVICE memory owned by the caller; the library allocates
+ * nothing, keeps no state between calls and never synchronises. Work is enqueued on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream) and is asynchronous to the host.
+ * Pointers to device arrays must be 16-byte aligned; `out` must not alias any input.
+ *
+ * Errors: argument checks run on the host before any launch; on failure nothing is enqueued
+ * and the status says why. PKV_ERR_CUDA means a launch was rejected by the CUDA runtime.
+ * Bad VALUES inside device arrays (a block id outside [0, num_blocks), a slot outside the pool,
+ * a context_len above max_blocks_per_seq * block_size) are never dereferenced: the kernels
+ * skip them and, when `status` is non-NULL, OR a PKV_FLAG_* bit into that device int32.
+ * The caller clears it; the library only sets bits.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misalignment, aliasing */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim not 64/128, block_size not 16 */
+    PKV_ERR_WORKSPACE = 3,     /* workspace smaller than pkv_decode_workspace_bytes() */
+    PKV_ERR_CUDA = 4           /* the CUDA runtime rejected a launch */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
+
+/* bits the kernels OR into *status (device int32) when they meet bad values */
+#define PKV_FLAG_BAD_SLOT 0x1         /* slot >= num_blocks * block_size: token not written */
+#define PKV_FLAG_BAD_BLOCK 0x2        /* block id outside [0, num_blocks): block skipped */
+#define PKV_FLAG_BAD_CONTEXT 0x4      /* context_len < 0 or > max_blocks_per_seq * block_size:
+                                         clamped to [0, max_blocks_per_seq * block_size] */
+#define PKV_FLAG_LONG_CONTEXT 0x8     /* context_len > max_context_len: still correct, the
+                                         sequence's splits were made longer (informational) */
+#define PKV_FLAG_TIMEOUT 0x10         /* a wait for a staged copy exceeded 1 s: that unit was
+                                         abandoned and its output rows are undefined */
+
+/* Static text for a status code. Never NULL. */
+const char* pkv_status_string(pkv_status s);
+
+/* Library build identification, e.g. "pkv 0.1 sm_103a". */
+const char* pkv_version(void);
+
+/*
+ * Slot-mapped KV write ("AMD ATOM inference engine", introduction and section 5.1;
+ * "LLM Primer VI, Chapter 8", section 8.1). For every token i < num_tokens with
+ * s = slot_mapping[i] >= 0, and every kv head h:
+ *     k_pool[s / block_size][h][s % block_size][:] = k_new[i][h][:]      (likewise v)
+ * as a bit copy. For dtype PKV_I8 the per-token scales move with the rows:
+ *     k_scales[s / block_size][h][s % block_size] = k_new_scales[i][h]   (likewise v)
+ * (the four scale pointers must be NULL for other dtypes). Slots must be unique within a
+ * call; negative slots are skipped; slots >= num_blocks * block_size are skipped and flagged.
+ */
+pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                              const float* k_new_scales, const float* v_new_scales,
+                              float* k_scales, float* v_scales, const int64_t* slot_mapping,
+                              int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, pkv_dtype dtype, int32_t* status, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode_attention[_int8] needs for the split-K partial
+ * states (m, l, acc) of a batch: the split count per sequence follows "EchoLLMServing
+ * inference framework notes", section 2 (split_num = max(1, context_len // chunk)), so the
+ * bound uses max_context_len. split_chunk_tokens = 0 selects the library's default chunk.
+ * Returns 0 for invalid arguments. Pure host arithmetic; no CUDA call.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                  int max_context_len, int split_chunk_tokens);
+
+/* The chunk (tokens per split before block rounding) the library uses for a request of
+ * split_chunk_tokens (0 = auto) and this batch shape; 0 for invalid arguments. The split
+ * extent (grid size along splits) is max(1, max_context_len / chunk). Pure host arithmetic. */
+int pkv_decode_split_chunk(int num_seqs, int max_context_len, int split_chunk_tokens);
+
+/*
+ * Paged decode attention ("LLM Primer VI, Chapter 8", section 8.1; "EchoLLMServing inference
+ * framework notes", section 2). For every sequence b and query head h, with n = context_lens[b]
+ * and kv head g = h / (num_q_heads / num_kv_heads):
+ *     K_t = k_pool[block_tables[b][t / bs]][g][t % bs][:],  V_t likewise,  t < n
+ *     out[b][h][:] = sum_t softmax_t(scale * <q[b][h], K_t>) V_t          (zeros if n == 0)
+ * Sequence b is cut into split_num = max(1, n // chunk) splits of whole blocks (capped at
+ * max(1, max_context_len // chunk)); one kernel computes each split's (m, l, acc) for the whole
+ * GQA group of a kv head, a second kernel merges them. Sequences with one split skip the merge.
+ * dtype is the element type of q, out, k_pool and v_pool: PKV_F32 or PKV_BF16. Accumulation is
+ * fp32; out is rounded to dtype (nearest-even). max_context_len >= every context_lens[b]
+ * (a larger context is still computed correctly and flagged). split_chunk_tokens: 0 = auto,
+ * else a multiple of block_size. workspace: device memory of at least
+ * pkv_decode_workspace_bytes(...) bytes, 256-byte aligned; its contents on entry do not matter.
+ */
+pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_pool,
+                                      const void* v_pool, const int32_t* block_tables,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, int max_blocks_per_seq,
+                                      int max_context_len, float scale, pkv_dtype dtype,
+                                      int split_chunk_tokens, void* workspace,
+                                      size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * INT8-KV paged decode attention ("EchoLLMServing inference framework notes", section 3:
+ * per-token dequantisation fused into the attention kernel). Identical to
+ * pkv_paged_decode_attention with q and out in bf16 and
+ *     K_t = k_pool[blk][g][off][:] * k_scales[blk][g][off]   (int8 times fp32)
+ *     V_t = v_pool[blk][g][off][:] * v_scales[blk][g][off]
+ * The scales are applied to the scores and to the softmax weights, not to every element.
+ */
+pkv_status pkv_paged_decode_attention_int8(void* out, const void* q, const int8_t* k_pool,
+                                           const int8_t* v_pool, const float* k_scales,
+                                           const float* v_scales, const int32_t* block_tables,
+                                           const int32_t* context_lens, int num_seqs,
+                                           int num_q_heads, int num_kv_heads, int head_dim,
+                                           int block_size, int num_blocks,
+                                           int max_blocks_per_seq, int max_context_len,
+                                           float scale, int split_chunk_tokens, void* workspace,
+                                           size_t workspace_bytes, int32_t* status,
+                                           void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -73,12 +73,18 @@ def bf16_to_double(bits: int) -> float:
 
 
 def kv_cache_write(k_new, v_new, k_pool, v_pool, slot_mapping, k_new_scales=None,
-                   v_new_scales=None, k_scales=None, v_scales=None, check=True):
-    """Write new tokens into (copies of) the pools; returns (k_pool, v_pool, k_scales, v_scales).
+                   v_new_scales=None, k_scales=None, v_scales=None, check=True, inplace=False):
+    """Write new tokens into copies of the pools (or, with inplace=True, into the given
+    C-contiguous arrays); returns (k_pool, v_pool, k_scales, v_scales).
     Pools are [NB, Hkv, BS, D]; k_new/v_new [T, Hkv, D]; slot_mapping int64 [T]."""
-    kp, vp = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
-    ks = None if k_scales is None else np.array(k_scales, dtype=np.float32, copy=True)
-    vs = None if v_scales is None else np.array(v_scales, dtype=np.float32, copy=True)
+    if inplace:
+        for a in (k_pool, v_pool, k_scales, v_scales):
+            assert a is None or a.flags.c_contiguous
+        kp, vp, ks, vs = k_pool, v_pool, k_scales, v_scales
+    else:
+        kp, vp = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+        ks = None if k_scales is None else np.array(k_scales, dtype=np.float32, copy=True)
+        vs = None if v_scales is None else np.array(v_scales, dtype=np.float32, copy=True)
     kn, vn = np.ascontiguousarray(k_new), np.ascontiguousarray(v_new)
     sm = _c(slot_mapping, np.int64)
     NB, Hkv, BS, D = kp.shape

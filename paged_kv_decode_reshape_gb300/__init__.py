@@ -1,0 +1,145 @@
+"""Paged KV-cache decode for GB300: Python binding of libpkv.so.
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels. Tensors
+are torch CUDA tensors (device memory and streams come from PyTorch); the calls and their
+semantics are those of include/pkv.h. There is no CPU fallback: if libpkv.so cannot be loaded
+(or built), every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+F32, BF16, I8 = 0, 1, 2
+FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_CONTEXT, FLAG_LONG_CONTEXT, FLAG_TIMEOUT = 1, 2, 4, 8, 16
+BLOCK_SIZE = 16
+
+# every exported symbol, with its ctypes signature (mirrors include/pkv.h)
+_P, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "pkv_status_string": ([_I], ctypes.c_char_p),
+    "pkv_version": ([], ctypes.c_char_p),
+    "pkv_kv_cache_write": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "pkv_decode_split_chunk": ([_I, _I, _I], _I),
+    "pkv_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                                    _I, _I, _P, _SZ, _P, _P], _I),
+    "pkv_paged_decode_attention_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                         _I, _I, _F, _I, _P, _SZ, _P, _P], _I),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libpkv.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libpkv.so not found at {path}: run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def version() -> str:
+    return load().pkv_version().decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise PkvError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _kv_code(t) -> int:
+    import torch
+    return {torch.float32: F32, torch.bfloat16: BF16, torch.int8: I8}[t.dtype]
+
+
+def kv_cache_write(k_new, v_new, k_pool, v_pool, slot_mapping, k_new_scales=None,
+                   v_new_scales=None, k_scales=None, v_scales=None, status=None, stream=None):
+    """pkv_kv_cache_write on torch tensors: k_new/v_new [T, Hkv, D], pools [NB, Hkv, 16, D],
+    slot_mapping int64 [T]; INT8 pools also take the four scale tensors."""
+    T, Hkv, D = k_new.shape
+    NB, _, BS, _ = k_pool.shape
+    rc = load().pkv_kv_cache_write(
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_new_scales),
+        _ptr(v_new_scales), _ptr(k_scales), _ptr(v_scales), _ptr(slot_mapping), T, Hkv, D, BS,
+        NB, _kv_code(k_pool), _ptr(status), _stream(stream))
+    _check(rc, "kv_cache_write")
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                           split_chunk_tokens=0) -> int:
+    return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                                 max_context_len, split_chunk_tokens))
+
+
+def decode_split_chunk(num_seqs, max_context_len, split_chunk_tokens=0) -> int:
+    return int(load().pkv_decode_split_chunk(num_seqs, max_context_len, split_chunk_tokens))
+
+
+def paged_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len,
+                           scale, split_chunk_tokens=0, workspace=None, status=None,
+                           stream=None):
+    """pkv_paged_decode_attention: out/q [B, Hq, D] (fp32 or bf16), pools [NB, Hkv, 16, D] of
+    the same dtype, block_tables int32 [B, MBPS], context_lens int32 [B]; workspace a uint8
+    CUDA tensor of at least decode_workspace_bytes(...) bytes (None if that is 0)."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
+        B, Hq, Hkv, D, BS, NB, block_tables.shape[1], int(max_context_len), float(scale),
+        _kv_code(q), int(split_chunk_tokens), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _check(rc, "paged_decode_attention")
+
+
+def paged_decode_attention_int8(out, q, k_pool, v_pool, k_scales, v_scales, block_tables,
+                                context_lens, max_context_len, scale, split_chunk_tokens=0,
+                                workspace=None, status=None, stream=None):
+    """pkv_paged_decode_attention_int8: q/out bf16, pools int8, scales fp32 [NB, Hkv, 16]."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_decode_attention_int8(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D, BS, NB, block_tables.shape[1],
+        int(max_context_len), float(scale), int(split_chunk_tokens), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _check(rc, "paged_decode_attention_int8")

@@ -1,0 +1,234 @@
+// pkv_api.cu -- the C ABI of libpkv.so (declared in include/pkv.h).
+//
+// Validates arguments on the host (nothing is enqueued on failure), chooses the split chunk,
+// sizes the grids and launches the kernels on the caller's stream. Allocates nothing, keeps no
+// state, never synchronises.
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace {
+
+using namespace pkv;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [a, a + na) and [b, b + nb) share a byte
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t elem_bytes(pkv_dtype t) { return t == PKV_F32 ? 4 : t == PKV_BF16 ? 2 : t == PKV_I8 ? 1 : 0; }
+
+// Tokens per split before block rounding: the request, or in auto mode the default chunk,
+// doubled until the split extent fits the merge kernel.
+int choose_chunk(int max_context_len, int requested) {
+    if (requested > 0) return requested;
+    int c = kDefaultChunk;
+    while (max_context_len / c > kMaxSplits) c *= 2;
+    return c;
+}
+
+int split_extent(int max_context_len, int chunk) {
+    const int s = max_context_len / chunk;
+    return s < 1 ? 1 : s;
+}
+
+size_t workspace_bytes_for(int B, int Hq, int D, int S) {
+    if (S <= 1) return 0;
+    return (size_t)B * Hq * S * ((size_t)D + 2) * sizeof(float);
+}
+
+int heads_per_cta(int g) { return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8; }
+
+struct Decode {
+    void* out; const void* q; const void* k_pool; const void* v_pool;
+    const float* k_scales; const float* v_scales;
+    const int32_t* block_tables; const int32_t* context_lens;
+    int B, Hq, Hkv, D, BS, NB, MBPS, max_ctx;
+    float scale;
+    pkv_dtype q_dtype, kv_dtype;
+    int chunk_req;
+    void* ws; size_t ws_bytes;
+    int32_t* status;
+    cudaStream_t stream;
+};
+
+pkv_status run_decode(const Decode& a) {
+    if (a.B < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.D <= 0 || a.NB <= 0 || a.MBPS <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (a.Hq % a.Hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (a.BS != kBlockSize || (a.D != 64 && a.D != 128)) return PKV_ERR_UNSUPPORTED;
+    if (a.max_ctx < 0 || (long long)a.max_ctx > (long long)a.MBPS * kBlockSize) return PKV_ERR_INVALID_ARG;
+    if (a.chunk_req < 0 || a.chunk_req % kBlockSize != 0) return PKV_ERR_INVALID_ARG;
+    if (!(a.scale == a.scale) || a.scale == INFINITY || a.scale == -INFINITY) return PKV_ERR_INVALID_ARG;
+    if (a.B == 0) return PKV_OK;
+    if (!a.out || !a.q || !a.k_pool || !a.v_pool || !a.block_tables || !a.context_lens)
+        return PKV_ERR_INVALID_ARG;
+    const bool i8 = a.kv_dtype == PKV_I8;
+    if (i8 && (!a.k_scales || !a.v_scales)) return PKV_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)a.out, a.q, a.k_pool, a.v_pool, (const void*)a.k_scales,
+                            (const void*)a.v_scales})
+        if (ptr && !aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(a.block_tables, 4) || !aligned(a.context_lens, 4)) return PKV_ERR_INVALID_ARG;
+    if (a.B > 65535) return PKV_ERR_UNSUPPORTED;  // grid.z
+    const int g = a.Hq / a.Hkv;
+    const int hg = heads_per_cta(g);
+    const int head_chunks = (g + hg - 1) / hg;
+    if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
+
+    const int chunk = choose_chunk(a.max_ctx, a.chunk_req);
+    const int S = split_extent(a.max_ctx, chunk);
+    if (S > kMaxSplits) return PKV_ERR_UNSUPPORTED;
+    const size_t need = workspace_bytes_for(a.B, a.Hq, a.D, S);
+    if (need > 0) {
+        if (!a.ws || a.ws_bytes < need) return PKV_ERR_WORKSPACE;
+        if (!aligned(a.ws, 256)) return PKV_ERR_INVALID_ARG;
+    }
+
+    // out must not alias an input or the workspace
+    const size_t qe = elem_bytes(a.q_dtype), ke = elem_bytes(a.kv_dtype);
+    const size_t out_b = (size_t)a.B * a.Hq * a.D * qe;
+    const size_t pool_b = (size_t)a.NB * a.Hkv * kBlockSize * a.D * ke;
+    const size_t sc_b = i8 ? (size_t)a.NB * a.Hkv * kBlockSize * 4 : 0;
+    if (overlap(a.out, out_b, a.q, out_b) || overlap(a.out, out_b, a.k_pool, pool_b) ||
+        overlap(a.out, out_b, a.v_pool, pool_b) || overlap(a.out, out_b, a.k_scales, sc_b) ||
+        overlap(a.out, out_b, a.v_scales, sc_b) ||
+        overlap(a.out, out_b, a.block_tables, (size_t)a.B * a.MBPS * 4) ||
+        overlap(a.out, out_b, a.context_lens, (size_t)a.B * 4) ||
+        overlap(a.out, out_b, a.ws, need))
+        return PKV_ERR_INVALID_ARG;
+
+    SplitParams p{};
+    p.out = a.out; p.q = a.q; p.k_pool = a.k_pool; p.v_pool = a.v_pool;
+    p.k_scales = a.k_scales; p.v_scales = a.v_scales;
+    p.block_tables = a.block_tables; p.context_lens = a.context_lens;
+    p.ws_acc = need ? static_cast<float*>(a.ws) : nullptr;
+    p.ws_ml = need ? static_cast<float*>(a.ws) + (size_t)a.B * a.Hq * S * a.D : nullptr;
+    p.status = a.status;
+    p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = g; p.NB = a.NB; p.MBPS = a.MBPS;
+    p.chunk = chunk; p.max_splits = S; p.head_chunks = head_chunks;
+    p.max_context_len = a.max_ctx;
+    p.scale_log2 = a.scale * kLog2e;
+
+    cudaError_t e;
+    if (a.kv_dtype == PKV_F32) e = launch_split_f32(p, a.D, hg, a.stream);
+    else if (a.kv_dtype == PKV_BF16) e = launch_split_bf16(p, a.D, hg, a.stream);
+    else e = launch_split_i8(p, a.D, hg, a.stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    if (S > 1) {
+        MergeParams m{};
+        m.out = a.out; m.ws_acc = p.ws_acc; m.ws_ml = p.ws_ml; m.context_lens = a.context_lens;
+        m.B = a.B; m.Hq = a.Hq; m.MBPS = a.MBPS; m.chunk = chunk; m.max_splits = S;
+        if (launch_merge(m, a.q_dtype, a.D, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_WORKSPACE: return "workspace too small";
+        case PKV_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+const char* pkv_version(void) { return "pkv 0.1 sm_103a"; }
+
+pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                              const float* k_new_scales, const float* v_new_scales,
+                              float* k_scales, float* v_scales, const int64_t* slot_mapping,
+                              int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, pkv_dtype dtype, int32_t* status, void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_I8) return PKV_ERR_INVALID_ARG;
+    if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+    const bool i8 = dtype == PKV_I8;
+    const bool any_scale = k_new_scales || v_new_scales || k_scales || v_scales;
+    const bool all_scale = k_new_scales && v_new_scales && k_scales && v_scales;
+    if (i8 ? !all_scale : any_scale) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    for (const void* ptr : {k_new, v_new, (const void*)k_pool, (const void*)v_pool})
+        if (!aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(slot_mapping, 8)) return PKV_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)k_new_scales, (const void*)v_new_scales,
+                            (const void*)k_scales, (const void*)v_scales})
+        if (ptr && !aligned(ptr, 4)) return PKV_ERR_INVALID_ARG;
+    const size_t row = (size_t)head_dim * elem_bytes(dtype);
+    const size_t new_b = (size_t)num_tokens * num_kv_heads * row;
+    const size_t pool_b = (size_t)num_blocks * num_kv_heads * kBlockSize * row;
+    if (overlap(k_pool, pool_b, v_pool, pool_b) || overlap(k_pool, pool_b, k_new, new_b) ||
+        overlap(k_pool, pool_b, v_new, new_b) || overlap(v_pool, pool_b, k_new, new_b) ||
+        overlap(v_pool, pool_b, v_new, new_b))
+        return PKV_ERR_INVALID_ARG;
+    WriteParams p{};
+    p.k_new = k_new; p.v_new = v_new; p.k_pool = k_pool; p.v_pool = v_pool;
+    p.k_new_scales = k_new_scales; p.v_new_scales = v_new_scales;
+    p.k_scales = k_scales; p.v_scales = v_scales;
+    p.slot_mapping = slot_mapping; p.status = status;
+    p.T = num_tokens; p.Hkv = num_kv_heads; p.row_bytes = (int)row; p.NB = num_blocks;
+    return launch_kv_write(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_decode_split_chunk(int num_seqs, int max_context_len, int split_chunk_tokens) {
+    (void)num_seqs;
+    if (max_context_len < 0 || split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize) return 0;
+    return choose_chunk(max_context_len, split_chunk_tokens);
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                  int max_context_len, int split_chunk_tokens) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize)
+        return 0;
+    const int chunk = choose_chunk(max_context_len, split_chunk_tokens);
+    return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
+}
+
+pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_pool,
+                                      const void* v_pool, const int32_t* block_tables,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, int max_blocks_per_seq,
+                                      int max_context_len, float scale, pkv_dtype dtype,
+                                      int split_chunk_tokens, void* workspace,
+                                      size_t workspace_bytes, int32_t* status, void* stream) {
+    if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    Decode a{out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens,
+             num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+             max_blocks_per_seq, max_context_len, scale, dtype, dtype, split_chunk_tokens,
+             workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
+    return run_decode(a);
+}
+
+pkv_status pkv_paged_decode_attention_int8(void* out, const void* q, const int8_t* k_pool,
+                                           const int8_t* v_pool, const float* k_scales,
+                                           const float* v_scales, const int32_t* block_tables,
+                                           const int32_t* context_lens, int num_seqs,
+                                           int num_q_heads, int num_kv_heads, int head_dim,
+                                           int block_size, int num_blocks,
+                                           int max_blocks_per_seq, int max_context_len,
+                                           float scale, int split_chunk_tokens, void* workspace,
+                                           size_t workspace_bytes, int32_t* status,
+                                           void* stream) {
+    Decode a{out, q, k_pool, v_pool, k_scales, v_scales, block_tables, context_lens,
+             num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+             max_blocks_per_seq, max_context_len, scale, PKV_BF16, PKV_I8, split_chunk_tokens,
+             workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
+    return run_decode(a);
+}
+
+}  // extern "C"

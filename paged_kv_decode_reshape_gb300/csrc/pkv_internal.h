@@ -1,0 +1,81 @@
+// pkv_internal.h -- internal interface between the C ABI (pkv_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;      // tokens per KV block (the only size built)
+constexpr int kMaxSplits = 8192;    // split extent the merge kernel supports
+constexpr int kDefaultChunk = 512;  // tokens per split before block rounding (auto mode)
+
+// Split rule ("EchoLLMServing inference framework notes", section 2, FlashDecoding):
+// split_num = max(1, n // chunk), capped at max_splits; each split is a whole number of
+// blocks, per = ceil(n / split_num) rounded up to the block size; split j covers
+// [j * per, min(n, (j + 1) * per)); trailing empty splits are dropped. n <= 0 -> 1 split.
+__host__ __device__ __forceinline__ int split_count(int n, int chunk, int max_splits, int* per) {
+    if (n <= 0) {
+        *per = 0;
+        return 1;
+    }
+    int s0 = n / chunk;
+    s0 = s0 < 1 ? 1 : (s0 > max_splits ? max_splits : s0);
+    int p = (n + s0 - 1) / s0;
+    p = (p + kBlockSize - 1) / kBlockSize * kBlockSize;
+    *per = p;
+    return (n + p - 1) / p;
+}
+
+struct SplitParams {
+    void* out;                  // [B][Hq][D], element type of q
+    const void* q;              // [B][Hq][D]
+    const void* k_pool;         // [NB][Hkv][16][D]
+    const void* v_pool;
+    const float* k_scales;      // [NB][Hkv][16] (int8 only)
+    const float* v_scales;
+    const int32_t* block_tables;  // [B][MBPS]
+    const int32_t* context_lens;  // [B]
+    float* ws_acc;              // [B][Hq][S][D]  unnormalised accumulators
+    float* ws_ml;               // [B][Hq][S][2]  (m in log2 units, l)
+    int32_t* status;
+    int B, Hq, Hkv, G, NB, MBPS;
+    int chunk, max_splits;      // S = max_splits
+    int head_chunks;            // CTAs per kv head along grid.y (ceil(G / heads per CTA))
+    int max_context_len;
+    float scale_log2;           // scale * log2(e): scores are kept in base-2 units
+};
+
+struct MergeParams {
+    void* out;
+    const float* ws_acc;
+    const float* ws_ml;
+    const int32_t* context_lens;
+    int B, Hq, MBPS, chunk, max_splits;
+};
+
+struct WriteParams {
+    const void* k_new;
+    const void* v_new;
+    void* k_pool;
+    void* v_pool;
+    const float* k_new_scales;
+    const float* v_new_scales;
+    float* k_scales;
+    float* v_scales;
+    const int64_t* slot_mapping;
+    int32_t* status;
+    int T, Hkv, row_bytes, NB;
+};
+
+// Launchers (return the cudaGetLastError() after the launch).
+cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s);
+cudaError_t launch_split_f32(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
+cudaError_t launch_split_bf16(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
+cudaError_t launch_split_i8(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, pkv_dtype out_dtype, int D, cudaStream_t s);
+
+}  // namespace pkv

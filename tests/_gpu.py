@@ -1,0 +1,101 @@
+"""Helpers for the GPU parity tests: move a seeded workload to the device, run one decode step
+through the C ABI binding, and compute the oracle's answer for the same inputs."""
+import numpy as np
+
+import oracle
+import paged_kv_decode_reshape_gb300 as P
+import workloads as W
+
+# (max-abs, mean-abs, relative L2) against the fp64 oracle. bf16 and INT8 bars as the pages'
+# task statement fixes them; fp32 is held to a tighter internal bar; the relative-L2 guard
+# keeps long contexts (|out| ~ 1e-2) honest.
+TOL = {"f32": (1e-5, 1e-6, 1e-5), "bf16": (2e-2, 2e-3, 2e-2), "i8": (5e-2, 5e-3, 2e-2)}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def to_dev(a, kind=None):
+    torch = _torch()
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:  # bf16 bit patterns
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(a).cuda()
+
+
+def to_f64(t):
+    torch = _torch()
+    return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
+
+
+def to_host_raw(t):
+    """Device tensor -> numpy array in the generator's encoding (bf16 as uint16 bits)."""
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+class DevWorkload:
+    def __init__(self, w: W.DecodeWorkload):
+        self.w = w
+        self.q = to_dev(w.q)
+        self.k_pool, self.v_pool = to_dev(w.k_pool), to_dev(w.v_pool)
+        self.k_scales, self.v_scales = to_dev(w.k_scales), to_dev(w.v_scales)
+        self.block_tables = to_dev(w.block_tables)
+        self.context_lens = to_dev(w.context_lens)
+        self.slot_mapping = to_dev(w.slot_mapping)
+        self.k_new, self.v_new = to_dev(w.k_new), to_dev(w.v_new)
+        self.k_new_scales, self.v_new_scales = to_dev(w.k_new_scales), to_dev(w.v_new_scales)
+
+    def write(self, status=None):
+        P.kv_cache_write(self.k_new, self.v_new, self.k_pool, self.v_pool, self.slot_mapping,
+                         self.k_new_scales, self.v_new_scales, self.k_scales, self.v_scales,
+                         status=status)
+
+    def attend(self, chunk=0, status=None, max_context_len=None, workspace=None, out=None):
+        torch = _torch()
+        w = self.w
+        maxc = w.max_context_len if max_context_len is None else max_context_len
+        nbytes = P.decode_workspace_bytes(w.B, w.Hq, w.D, maxc, chunk)
+        if workspace is None and nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        if out is None:
+            out = torch.empty(self.q.shape, dtype=self.q.dtype, device="cuda")
+        if w.kv_dtype == "i8":
+            P.paged_decode_attention_int8(out, self.q, self.k_pool, self.v_pool, self.k_scales,
+                                          self.v_scales, self.block_tables, self.context_lens,
+                                          maxc, w.scale, chunk, workspace, status)
+        else:
+            P.paged_decode_attention(out, self.q, self.k_pool, self.v_pool, self.block_tables,
+                                     self.context_lens, maxc, w.scale, chunk, workspace, status)
+        return out
+
+    def step(self, chunk=0, status=None):
+        self.write(status)
+        return self.attend(chunk, status)
+
+
+def oracle_step(w: W.DecodeWorkload, rows=None, num_threads=8):
+    """Oracle answer of one step (write, then attention) for all or the sampled sequences."""
+    kp, vp, ks, vs = oracle.kv_cache_write(w.k_new, w.v_new, w.k_pool, w.v_pool, w.slot_mapping,
+                                           w.k_new_scales, w.v_new_scales, w.k_scales, w.v_scales)
+    rows = np.arange(w.B) if rows is None else np.asarray(rows)
+    return oracle.paged_decode_attention(w.q[rows], kp, vp, w.block_tables[rows],
+                                         w.context_lens[rows], w.scale, ks, vs,
+                                         num_threads=num_threads)
+
+
+def assert_close(got, ref, kind, what=""):
+    mx, mean, rel = TOL[kind]
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    m, a = float(err.max()), float(err.mean())
+    r = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    assert m <= mx and a <= mean and r <= rel, (
+        f"{what}: max-abs {m:.3g} (<= {mx}), mean-abs {a:.3g} (<= {mean}), rel-L2 {r:.3g} (<= {rel})")
+    return m, a, r

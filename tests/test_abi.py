@@ -1,0 +1,137 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/pkv.h declares, and
+host-side argument checks reject bad calls before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_decode_reshape_gb300 as P
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pkv.h")
+
+# Fake, never-dereferenced device addresses: every call below fails validation before launch.
+# Host-logic tests for a machine without a GPU; skipped where a GPU exists, so that a
+# validation regression can never launch a kernel on fake pointers.
+A = 0x7F0000000000
+
+
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+fake_ptrs = pytest.mark.skipif(not _no_gpu(), reason="fake-pointer checks run on CPU-only hosts")
+FAKE = [ctypes.c_void_p(A + i * 0x1000000) for i in range(12)]
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(pkv):
+    names = declared_functions()
+    assert {"pkv_kv_cache_write", "pkv_paged_decode_attention",
+            "pkv_paged_decode_attention_int8", "pkv_decode_workspace_bytes"} <= set(names)
+    lib = ctypes.CDLL(P.library_path())
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
+        assert n in P.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings(pkv):
+    assert P.status_string(P.OK) == "ok"
+    assert "workspace" in P.status_string(P.ERR_WORKSPACE)
+    assert P.status_string(99) == "unknown status"
+    assert "sm_103a" in P.version()
+
+
+def test_workspace_arithmetic(pkv):
+    L = P.load()
+    # 8 seqs x 32 heads, 131072 tokens, auto chunk 512 -> 256 splits x (128 acc + m + l) fp32
+    assert L.pkv_decode_workspace_bytes(8, 32, 128, 131072, 0) == 8 * 32 * 256 * 130 * 4
+    assert L.pkv_decode_workspace_bytes(8, 32, 128, 131072, 1024) == 8 * 32 * 128 * 130 * 4
+    assert L.pkv_decode_workspace_bytes(4, 4, 64, 100, 0) == 0       # one split: no workspace
+    assert L.pkv_decode_workspace_bytes(4, 4, 64, 100, 17) == 0      # chunk not a block multiple
+    assert L.pkv_decode_split_chunk(1, 1 << 30, 0) >= 512            # auto keeps splits <= 8192
+    assert (1 << 30) // L.pkv_decode_split_chunk(1, 1 << 30, 0) <= 8192
+
+
+def _attn(L, **kw):
+    a = dict(out=FAKE[0], q=FAKE[1], k=FAKE[2], v=FAKE[3], bt=FAKE[4], cl=FAKE[5], B=2, Hq=8,
+             Hkv=2, D=128, BS=16, NB=64, MBPS=8, maxc=100, scale=0.1, dtype=P.BF16, chunk=0,
+             ws=None, wsb=0, status=None, stream=None)
+    a.update(kw)
+    return L.pkv_paged_decode_attention(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"],
+                                        a["Hq"], a["Hkv"], a["D"], a["BS"], a["NB"], a["MBPS"],
+                                        a["maxc"], a["scale"], a["dtype"], a["chunk"], a["ws"],
+                                        a["wsb"], a["status"], a["stream"])
+
+
+@fake_ptrs
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), P.ERR_INVALID_ARG),
+    (dict(out=None), P.ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), P.ERR_INVALID_ARG),
+    (dict(D=96), P.ERR_UNSUPPORTED),
+    (dict(BS=32), P.ERR_UNSUPPORTED),
+    (dict(maxc=8 * 16 + 1), P.ERR_INVALID_ARG),
+    (dict(maxc=-1), P.ERR_INVALID_ARG),
+    (dict(chunk=20), P.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), P.ERR_INVALID_ARG),
+    (dict(dtype=P.I8), P.ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p(A + 8)), P.ERR_INVALID_ARG),               # misaligned
+    (dict(out=FAKE[1]), P.ERR_INVALID_ARG),                            # out aliases q
+    (dict(maxc=128, MBPS=8, chunk=16), P.ERR_WORKSPACE),               # 8 splits, no workspace
+    (dict(maxc=128, MBPS=8, chunk=16, ws=FAKE[6], wsb=100), P.ERR_WORKSPACE),
+    (dict(maxc=128, MBPS=8, chunk=16, ws=ctypes.c_void_p(A + 0x6000010), wsb=1 << 30),
+     P.ERR_INVALID_ARG),                                               # workspace misaligned
+    (dict(B=70000), P.ERR_UNSUPPORTED),
+])
+def test_decode_argument_checks(pkv, kw, expect):
+    assert _attn(P.load(), **kw) == expect
+
+
+@fake_ptrs
+def test_empty_batch_is_a_no_op(pkv):
+    assert _attn(P.load(), B=0, out=None, q=None) == P.OK
+
+
+@fake_ptrs
+def test_int8_requires_scales(pkv):
+    L = P.load()
+    rc = L.pkv_paged_decode_attention_int8(FAKE[0], FAKE[1], FAKE[2], FAKE[3], None, FAKE[5],
+                                           FAKE[6], FAKE[7], 2, 8, 2, 128, 16, 64, 8, 100, 0.1,
+                                           0, None, 0, None, None)
+    assert rc == P.ERR_INVALID_ARG
+
+
+def _write(L, **kw):
+    a = dict(kn=FAKE[0], vn=FAKE[1], kp=FAKE[2], vp=FAKE[3], kns=None, vns=None, ks=None,
+             vs=None, sm=FAKE[8], T=4, Hkv=8, D=128, BS=16, NB=64, dtype=P.BF16)
+    a.update(kw)
+    return L.pkv_kv_cache_write(a["kn"], a["vn"], a["kp"], a["vp"], a["kns"], a["vns"], a["ks"],
+                                a["vs"], a["sm"], a["T"], a["Hkv"], a["D"], a["BS"], a["NB"],
+                                a["dtype"], None, None)
+
+
+@fake_ptrs
+@pytest.mark.parametrize("kw,expect", [
+    (dict(kn=None), P.ERR_INVALID_ARG),
+    (dict(sm=None), P.ERR_INVALID_ARG),
+    (dict(D=80), P.ERR_UNSUPPORTED),
+    (dict(BS=8), P.ERR_UNSUPPORTED),
+    (dict(dtype=P.I8), P.ERR_INVALID_ARG),                              # int8 without scales
+    (dict(ks=FAKE[9]), P.ERR_INVALID_ARG),                              # scales for bf16
+    (dict(vp=FAKE[2]), P.ERR_INVALID_ARG),                              # K and V pools alias
+    (dict(kp=ctypes.c_void_p(A + 0x2000004)), P.ERR_INVALID_ARG),      # misaligned
+    (dict(T=-1), P.ERR_INVALID_ARG),
+    (dict(T=0, kn=None, sm=None), P.OK),                               # nothing to write
+])
+def test_write_argument_checks(pkv, kw, expect):
+    assert _write(P.load(), **kw) == expect

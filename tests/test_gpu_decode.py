@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs.
+
+Element-by-element at sizes the oracle finishes in seconds (several splits, ragged tails), on
+sampled sequences at the five full workload sizes, plus the invariants and edge cases.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from _gpu import DevWorkload, assert_close, oracle_step, to_dev, to_f64, to_host_raw
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+REDUCED = {
+    1: dict(),
+    2: dict(B=6, ctx_lo=1, ctx_hi=1500),
+    3: dict(B=2, ctx_lo=3000, ctx_hi=9000),
+    4: dict(B=5, ctx_lo=17, ctx_hi=3000),
+    5: dict(B=6, ctx_lo=16, ctx_hi=300, prefix_tokens=256),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(pkv):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return pkv
+
+
+def status_tensor():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_kv_write_bit_exact(cfg):
+    w = W.make_config(cfg, **REDUCED[cfg])
+    d = DevWorkload(w)
+    st = status_tensor()
+    d.write(st)
+    torch.cuda.synchronize()
+    kp, vp, ks, vs = oracle.kv_cache_write(w.k_new, w.v_new, w.k_pool, w.v_pool, w.slot_mapping,
+                                           w.k_new_scales, w.v_new_scales, w.k_scales, w.v_scales)
+    assert np.array_equal(to_host_raw(d.k_pool), kp)
+    assert np.array_equal(to_host_raw(d.v_pool), vp)
+    if ks is not None:
+        assert np.array_equal(d.k_scales.cpu().numpy(), ks)
+        assert np.array_equal(d.v_scales.cpu().numpy(), vs)
+    assert int(st.item()) == 0
+
+
+def test_kv_write_skips_padding_and_flags_bad_slots():
+    w = W.make_config(2, B=4, ctx_lo=20, ctx_hi=60)
+    sm = w.slot_mapping.copy()
+    sm[1] = -1                       # padding token: not written
+    sm[2] = w.NB * 16 + 5            # outside the pool: not written, flagged
+    w2 = W.DecodeWorkload(**{**w.__dict__, "slot_mapping": sm})
+    d = DevWorkload(w2)
+    st = status_tensor()
+    d.write(st)
+    torch.cuda.synchronize()
+    kp, vp, _, _ = oracle.kv_cache_write(w2.k_new, w2.v_new, w2.k_pool, w2.v_pool, sm, check=False)
+    assert np.array_equal(to_host_raw(d.k_pool), kp)
+    assert np.array_equal(to_host_raw(d.v_pool), vp)
+    assert int(st.item()) & 1
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_decode_step_matches_oracle(cfg):
+    w = W.make_config(cfg, **REDUCED[cfg])
+    d = DevWorkload(w)
+    st = status_tensor()
+    got = to_f64(d.step(status=st))
+    ref = oracle_step(w)
+    assert_close(got, ref, w.kv_dtype, f"config {cfg}")
+    assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("cfg,rows", [(2, [0, 17, 63]), (3, [0, 5]), (4, [3, 64, 127]),
+                                      (5, [0, 128, 255])])
+def test_full_size_sampled_sequences(cfg, rows):
+    """The full workload in the launch configuration the bench times; the oracle checks a sample
+    of sequences (every head), including the longest one."""
+    w = W.make_config(cfg)
+    rows = sorted(set(rows) | {int(np.argmax(w.context_lens))})
+    d = DevWorkload(w)
+    got = to_f64(d.step())[rows]
+    ref = oracle_step(w, rows=rows, num_threads=16)
+    assert_close(got, ref, w.kv_dtype, f"config {cfg} rows {rows}")
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 64, 256, 4096])
+def test_forced_split_sizes(chunk):
+    w = W.make_config(2, B=5, ctx_lo=1, ctx_hi=900, seed=21)
+    ref = oracle_step(w)
+    d = DevWorkload(w)
+    got = to_f64(d.step(chunk=chunk))
+    assert_close(got, ref, "bf16", f"chunk {chunk}")
+
+
+def test_split_partials_match_oracle_partials():
+    """The workspace holds each split's (m, l, acc); m is kept in base-2 units."""
+    w = W.make_config(2, B=3, ctx_lo=100, ctx_hi=700, seed=4)
+    chunk = 64
+    d = DevWorkload(w)
+    d.write()
+    maxc = w.max_context_len
+    S = max(1, maxc // chunk)
+    nbytes = w.B * w.Hq * S * (w.D + 2) * 4
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    d.attend(chunk=chunk, workspace=ws)
+    torch.cuda.synchronize()
+    f = ws.view(torch.float32).cpu().numpy().astype(np.float64)
+    acc = f[: w.B * w.Hq * S * w.D].reshape(w.B, w.Hq, S, w.D)
+    ml = f[w.B * w.Hq * S * w.D:].reshape(w.B, w.Hq, S, 2)
+    kp, vp, _, _ = oracle.kv_cache_write(w.k_new, w.v_new, w.k_pool, w.v_pool, w.slot_mapping)
+    m, l, oacc, ns = oracle.paged_decode_partials(w.q, kp, vp, w.block_tables, w.context_lens,
+                                                  w.scale, chunk, S)
+    for b in range(w.B):
+        k = int(ns[b])
+        assert k > 1
+        np.testing.assert_allclose(ml[b, :, :k, 0] * math.log(2), m[b, :, :k], atol=1e-4)
+        np.testing.assert_allclose(ml[b, :, :k, 1], l[b, :, :k], rtol=1e-4)
+        np.testing.assert_allclose(acc[b, :, :k], oacc[b, :, :k], rtol=1e-3, atol=1e-3)
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_block_permutation_bit_identical(cfg):
+    w = W.make_config(cfg, B=6, ctx_lo=30, ctx_hi=1200)
+    p = W.permute_blocks(w, seed=123)
+    a = DevWorkload(w).step()
+    b = DevWorkload(p).step()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_shared_prefix_equals_copy_on_write_bit_identical():
+    w = W.make_config(5, B=8, ctx_lo=16, ctx_hi=500, prefix_tokens=512)
+    c = W.unshare_prefix(w)
+    a = DevWorkload(w).step()
+    b = DevWorkload(c).step()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert_close(to_f64(a), oracle_step(w), "bf16", "prefix-shared")
+
+
+@pytest.mark.parametrize("kv", ["f32", "bf16", "i8"])
+def test_edge_context_lengths(kv):
+    lens = [0, 1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1024, 1025]
+    w = W.make_decode(name="edges", B=len(lens), Hq=8, Hkv=2, D=128, context_lens=lens,
+                      kv_dtype=kv, q_dtype="f32" if kv == "f32" else "bf16", seed=31)
+    d = DevWorkload(w)
+    for chunk in (0, 16, 512):
+        got = to_f64(d.attend(chunk=chunk))
+        ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables,
+                                            w.context_lens, w.scale, w.k_scales, w.v_scales)
+        assert np.all(got[0] == 0.0)  # empty context -> zeros
+        assert_close(got, ref, kv, f"{kv} chunk {chunk}")
+    if kv == "bf16":  # one token: out is that token's V row exactly
+        got = to_f64(d.attend())
+        blk = w.block_tables[1, 0]
+        for h in range(8):
+            np.testing.assert_array_equal(got[1, h], W.bf16_bits_to_f32(w.v_pool[blk, h // 4, 0]))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_head_groups_and_dims(D, g, kv):
+    Hkv = 2
+    w = W.make_decode(name="groups", B=3, Hq=Hkv * g, Hkv=Hkv, D=D, context_lens=[5, 100, 700],
+                      kv_dtype=kv, q_dtype=kv, seed=g * 10 + D)
+    got = to_f64(DevWorkload(w).attend(chunk=256))
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    assert_close(got, ref, kv, f"g={g} D={D}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("g", [1, 4, 8])
+def test_int8_head_groups_and_dims(D, g):
+    w = W.make_decode(name="i8groups", B=3, Hq=2 * g, Hkv=2, D=D, context_lens=[9, 300, 1100],
+                      kv_dtype="i8", q_dtype="bf16", seed=g + D)
+    got = to_f64(DevWorkload(w).attend(chunk=256))
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                        w.scale, w.k_scales, w.v_scales)
+    assert_close(got, ref, "i8", f"int8 g={g} D={D}")
+
+
+def test_int8_every_byte_value_converts_exactly():
+    """Single-token contexts with unit V scales: out = the int8 V row, exact in bf16."""
+    D, Hkv = 128, 1
+    NB = 2
+    kp = np.zeros((NB, Hkv, 16, D), np.int8)
+    vp = np.zeros((NB, Hkv, 16, D), np.int8)
+    allv = np.arange(-128, 128, dtype=np.int16).astype(np.int8)
+    vp[0, 0, 0] = allv[:128]
+    vp[1, 0, 0] = allv[128:]
+    ks = np.ones((NB, Hkv, 16), np.float32)
+    vs = np.ones((NB, Hkv, 16), np.float32)
+    q = W.f32_to_bf16_bits(np.ones((2, 1, D), np.float32))
+    w = W.DecodeWorkload(name="bytes", B=2, Hq=1, Hkv=1, D=D, BS=16, NB=NB, kv_dtype="i8",
+                         q_dtype="bf16", q=q, k_pool=kp, v_pool=vp,
+                         block_tables=np.array([[0], [1]], np.int32),
+                         context_lens=np.array([1, 1], np.int32),
+                         slot_mapping=np.array([-1, -1], np.int64),
+                         k_new=np.zeros((2, 1, D), np.int8), v_new=np.zeros((2, 1, D), np.int8),
+                         scale=0.1, ref_count=np.ones(NB, np.int32), k_scales=ks, v_scales=vs,
+                         k_new_scales=np.ones((2, 1), np.float32),
+                         v_new_scales=np.ones((2, 1), np.float32))
+    got = to_f64(DevWorkload(w).attend())
+    np.testing.assert_array_equal(got[:, 0].reshape(-1), allv.astype(np.float64))
+
+
+def test_identical_keys_give_mean_of_v():
+    w = W.make_config(2, B=3, ctx_lo=200, ctx_hi=800, seed=8)
+    kp = w.k_pool.copy()
+    kp[:] = kp[0, :, 0:1, :]  # every row of every block: the same key per kv head
+    w2 = W.DecodeWorkload(**{**w.__dict__, "k_pool": kp})
+    got = to_f64(DevWorkload(w2).attend())
+    vf = W.bf16_bits_to_f32(w.v_pool).astype(np.float64)
+    for b in range(w.B):
+        n = int(w.context_lens[b])
+        rows = np.stack([vf[w.block_tables[b, t // 16], :, t % 16] for t in range(n)])
+        mean = rows.mean(0)  # [Hkv, D]
+        for h in range(w.Hq):
+            np.testing.assert_allclose(got[b, h], mean[h // w.group], atol=4e-3)
+
+
+def test_bad_block_ids_are_skipped_and_flagged():
+    w = W.make_config(2, B=4, ctx_lo=100, ctx_hi=400, seed=3)
+    bt = w.block_tables.copy()
+    bt[1, 2] = w.NB + 1000
+    bt[2, 0] = -7
+    w2 = W.DecodeWorkload(**{**w.__dict__, "block_tables": bt})
+    st = status_tensor()
+    got = to_f64(DevWorkload(w2).attend(status=st))
+    assert int(st.item()) & 2
+    ref = oracle.paged_decode_attention(w.q[[0, 3]], w.k_pool, w.v_pool, w.block_tables[[0, 3]],
+                                        w.context_lens[[0, 3]], w.scale)
+    assert np.all(np.isfinite(got))
+    assert_close(got[[0, 3]], ref, "bf16", "untouched sequences")
+
+
+def test_understated_max_context_len_is_still_correct():
+    w = W.make_config(2, B=4, ctx_lo=600, ctx_hi=3000, seed=12)
+    st = status_tensor()
+    got = to_f64(DevWorkload(w).attend(status=st, max_context_len=1024))
+    assert int(st.item()) & 8
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    assert_close(got, ref, "bf16", "long context")
+
+
+def test_context_beyond_table_is_clamped_and_flagged():
+    w = W.make_config(2, B=2, ctx_lo=40, ctx_hi=60, seed=2)
+    lens = w.context_lens.copy()
+    lens[0] = w.MBPS * 16 + 100
+    w2 = W.DecodeWorkload(**{**w.__dict__, "context_lens": lens})
+    st = status_tensor()
+    d = DevWorkload(w2)
+    d.attend(status=st, max_context_len=w.MBPS * 16)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 4
+
+
+def test_runs_on_the_callers_stream():
+    w = W.make_config(2, B=8, ctx_lo=500, ctx_hi=2000, seed=9)
+    d = DevWorkload(w)
+    ref = to_f64(d.step())
+    d2 = DevWorkload(w)
+    torch.cuda.synchronize()  # uploads ran on the default stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = d2.step()
+    s.synchronize()
+    assert np.array_equal(to_f64(out), ref)
