@@ -1,0 +1,63 @@
+// decode_mma.cu -- instantiates the tensor-core split kernel (bf16 and INT8 K/V, head_dim 128)
+// and builds the TMA tensor maps that describe a K or V pool to the copy engine.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "decode_mma.cuh"
+
+namespace pkv {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    // The driver entry point is looked up once per process (a function pointer, not state of
+    // any call).
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+template <bool kI8>
+cudaError_t launch_t(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+    using G = MmaGeom<kI8>;
+    auto kern = mma_split_kernel<kI8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.max_splits, p.Hkv * p.head_chunks, p.B);
+    kern<<<grid, kMmaThreads, G::SMEM, s>>>(p, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// A pool [NB][Hkv][16][128] seen as a 2-D tensor of NB*Hkv*16 rows of 128 elements; one box is
+// 16 rows x 128 bytes (64 bf16 or 128 int8), written to shared memory with the 128-byte swizzle.
+bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, bool i8) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t rows = (cuuint64_t)num_blocks * num_kv_heads * kBlockSize;
+    const cuuint64_t dims[2] = {(cuuint64_t)kMmaD, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kMmaD * (i8 ? 1 : 2)};
+    const cuuint32_t box[2] = {i8 ? 128u : 64u, (cuuint32_t)kBlockSize};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_split_mma(const SplitParams& p, bool i8, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t s) {
+    return i8 ? launch_t<true>(p, tk, tv, s) : launch_t<false>(p, tk, tv, s);
+}
+
+}  // namespace pkv

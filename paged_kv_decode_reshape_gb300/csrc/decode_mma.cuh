@@ -1,0 +1,490 @@
+// decode_mma.cuh -- split-K paged decode attention, kernel 1 of 2, tensor-core path (head_dim 128,
+// bf16 or INT8 K/V, up to 8 query heads per kv head).
+//
+// Same unit and outputs as the CUDA-core kernel (decode_split.cuh): one CTA per (sequence b,
+// kv head, split) for the GQA group of that kv head ("EchoLLMServing inference framework
+// notes", section 2: one program per split emitting (m, l, acc); "LLM Primer VI, Chapter 8",
+// section 8.1: K/V gathered through the block table). What changes is how a 16-token block is
+// consumed: the per-block work is a dense [16 tokens x 128] x [128 x 8 heads] product and its
+// transpose, done with warp-level mma.sync m16n8k16 so that one instruction covers what took
+// 64 FMAs plus conversions, and the kernel stays far from the issue limit at HBM speed.
+//
+// Warp roles (160 threads): warp 4 is the producer -- it reads the split's block ids (validated),
+// and its lane 0 issues, per block, 2-D TMA tensor copies of the K and V tiles into a STAGES-deep
+// ring with 128-byte swizzle (bank-conflict-free ldmatrix), plus 1-D bulk copies of the INT8
+// scale rows, completing on a per-stage "full" mbarrier. Warps 0-3 are consumers: warp w takes
+// blocks w, w+4, ... of the split, keeps its own online-softmax state, and releases each stage on
+// a per-stage "empty" mbarrier. The four states are merged in shared memory at the end.
+//
+// Per block and consumer warp (tokens on the MMA M dimension, heads on N):
+//   S^T[16 x 8]   = K[16 x 128] . Q^T[128 x 8]      8 MMAs (k = 16 dims each)
+//   online softmax on S^T (scores in base-2 units; the running max is only raised when a block
+//   exceeds it by more than 2^8, so rescaling the accumulators is rare -- exact in real arithmetic
+//   because l and acc always share the reference max)
+//   P^T fragments = movmatrix.trans of the score fragments (no shared-memory round trip)
+//   O^T[128 x 8] += V^T[128 x 16] . P^T[16 x 8]       8 MMAs (k = 16 tokens)
+// bf16: K fragments by ldmatrix, V^T fragments by ldmatrix.trans, P rounded to bf16.
+// INT8 ("EchoLLMServing notes", section 3): K bytes by ldmatrix, V bytes by 16-byte loads; both
+// widened exactly to fp16 with the byte-permute conversion of Kim et al. 2022 (1024 + 128 + x as
+// fp16, minus 1152); q is pre-scaled by scale*log2(e) into fp16; the per-token K scale multiplies
+// the score and the V scale the softmax weight. Dims are consumed in a fixed permuted order that
+// q's fragments follow too, which leaves the dot products unchanged.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+constexpr int kMmaD = 128;          // head_dim of this path
+constexpr int kMmaHeads = 8;        // MMA N: query heads per CTA
+constexpr int kMmaConsumers = 4;    // consumer warps
+constexpr int kMmaThreads = 32 * (kMmaConsumers + 1);
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
+
+template <bool kI8>
+struct MmaGeom {
+    static constexpr int TILE = kBlockSize * kMmaD * (kI8 ? 1 : 2);  // one K (or V) tile
+    static constexpr int BOX = kBlockSize * 128;                     // bytes of one TMA box
+    static constexpr int BOXES = TILE / BOX;                         // boxes per tile (2 or 1)
+    static constexpr int STAGE = 2 * TILE;                           // K then V
+    // Stage s is only ever consumed by warp s % kMmaConsumers (STAGES is a multiple of the
+    // consumer count), so each warp waits on a stage's phases strictly in order and a parity wait
+    // can never match a phase two behind. 8 stages = two blocks in flight per consumer warp.
+    static constexpr int STAGES = 8;
+    static constexpr int RING = STAGES * STAGE;
+    static constexpr int SCALES = kI8 ? STAGES * 2 * kBlockSize * 4 : 0;
+    static constexpr int MERGE = kMmaConsumers * kMmaHeads * (kMmaD + 2) * 4;
+    static constexpr int MAIN = RING > MERGE ? RING : MERGE;
+    // + 1024 for aligning the ring to the 128-byte-swizzle atom
+    static constexpr int SMEM = 1024 + MAIN + SCALES + ((STAGES * 4 + 7) & ~7) + 2 * STAGES * 8;
+    static_assert(RING % 1024 == 0 && STAGE % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+    static_assert(STAGES % kMmaConsumers == 0, "a stage must belong to one consumer warp");
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <bool kI8>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (kI8) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// 2-D TMA tile load (box of the tensor map at coordinates (x, y)) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                           uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// byte-permute int8 -> fp16 helpers: w holds 4 int8 already XOR-ed with 0x80 (biased to x+128)
+__device__ __forceinline__ uint32_t s8b_pair_to_h2(uint32_t w, uint32_t sel) {
+    // bytes of w picked by sel go to the low byte of each fp16 half; high bytes 0x64: 1024 + b
+    uint32_t h = __byte_perm(w, 0x00006464u, sel);
+    __half2 v = __hsub2(*reinterpret_cast<__half2*>(&h), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <bool kI8>
+__global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParams p,
+                                                               const __grid_constant__ CUtensorMap tmk,
+                                                               const __grid_constant__ CUtensorMap tmv) {
+    using G = MmaGeom<kI8>;
+    constexpr int STAGES = G::STAGES, STAGE = G::STAGE, TILE = G::TILE;
+    constexpr float kNegInf = -INFINITY;
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned
+    float* scl = reinterpret_cast<float*>(smem + G::MAIN);              // [STAGES][K16 | V16]
+    int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + G::MAIN + G::SCALES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::MAIN + G::SCALES + ((STAGES * 4 + 7) & ~7));
+    uint64_t* empty = full + STAGES;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y / p.head_chunks;
+    const int hc = blockIdx.y - kvh * p.head_chunks;
+    const int b = blockIdx.z;
+    const int h0 = kvh * p.G + hc * kMmaHeads;
+    const int nh = p.G - hc * kMmaHeads < kMmaHeads ? p.G - hc * kMmaHeads : kMmaHeads;
+
+    int n = p.context_lens[b];
+    const int ncap = p.MBPS * kBlockSize;
+    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0;
+    if (n < 0 || n > ncap) {
+        if (reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
+        n = n < 0 ? 0 : ncap;
+    } else if (n > p.max_context_len && reporter) {
+        flag(p.status, PKV_FLAG_LONG_CONTEXT);
+    }
+    int per;
+    const int ns = split_count(n, p.chunk, p.max_splits, &per);
+    if (split >= ns) return;
+    const int t0 = split * per;
+    const int t1 = n < t0 + per ? n : t0 + per;
+    const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
+    const int blk0 = t0 / kBlockSize;
+
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t full0 = smem_addr(full), empty0 = smem_addr(empty);
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    // per-lane MMA coordinates
+    const int r = lane >> 2;  // fragment row group: token (QK) / head (B operand)
+    const int c = lane & 3;   // thread in group: head pair 2c, 2c+1 of the C fragments
+
+    float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    if (warp == kMmaConsumers) {
+        // ------------------------------ producer warp ------------------------------
+        const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS + blk0;
+        bool dead = false;
+        for (int j0 = 0; j0 < nblk && !dead; j0 += 32) {
+            int id = -1;
+            if (j0 + lane < nblk) {
+                id = bt_row[j0 + lane];
+                if (id < 0 || id >= p.NB) {
+                    flag(p.status, PKV_FLAG_BAD_BLOCK);
+                    id = -1;
+                }
+            }
+            const int cnt = nblk - j0 < 32 ? nblk - j0 : 32;
+            for (int jj = 0; jj < cnt; ++jj) {
+                const int j = j0 + jj;
+                const int bid = __shfl_sync(0xffffffffu, id, jj);
+                if (lane == 0) {
+                    const int st = j % STAGES;
+                    if (j >= STAGES && !mbar_wait_bounded(empty0 + 8 * st, ((j / STAGES) - 1) & 1)) {
+                        dead = true;
+                    } else {
+                        const uint32_t bar = full0 + 8 * st;
+                        const uint32_t dst = ring + st * STAGE;
+                        stage_ok[st] = bid >= 0;
+                        if (bid >= 0) {
+                            const int row = (bid * p.Hkv + kvh) * kBlockSize;
+                            mbar_arrive_expect_tx(bar, STAGE + (kI8 ? 2 * kBlockSize * 4 : 0));
+#pragma unroll
+                            for (int x = 0; x < G::BOXES; ++x) {
+                                tma_load_2d(dst + x * G::BOX, &tmk, x * 64 * (kI8 ? 2 : 1), row, bar);
+                                tma_load_2d(dst + TILE + x * G::BOX, &tmv, x * 64 * (kI8 ? 2 : 1), row, bar);
+                            }
+                            if constexpr (kI8) {
+                                const size_t srow = (size_t)bid * p.Hkv + kvh;
+                                const uint32_t sd = smem_addr(scl + st * 2 * kBlockSize);
+                                bulk_g2s(sd, p.k_scales + srow * kBlockSize, kBlockSize * 4, bar);
+                                bulk_g2s(sd + kBlockSize * 4, p.v_scales + srow * kBlockSize, kBlockSize * 4, bar);
+                            }
+                        } else {
+                            mbar_arrive(bar);
+                        }
+                    }
+                }
+                dead = __shfl_sync(0xffffffffu, dead, 0);
+                if (dead) break;
+            }
+        }
+        if (dead && lane == 0) {
+            flag(p.status, PKV_FLAG_TIMEOUT);
+            atomicExch(&abort_flag, 1);
+        }
+    } else {
+        // ------------------------------ consumer warps ------------------------------
+        // q as the B operand of S^T = K Q^T: b0b1 = (dims k0 + 2c, +1; head r), b2b3 = (+8, +9)
+        uint32_t qb[8][2];
+        {
+            const bool hv = r < nh;
+            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + h0 + (hv ? r : 0)) * kMmaD;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                if constexpr (kI8) {
+                    // permuted dims: k-pos 2c,2c+1 <- dims 16ks+4c, +1; k-pos 2c+8,2c+9 <- +2, +3
+                    const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
+                    float f0, f1, f2, f3;
+                    bf16x2_to_f32(raw4.x, f0, f1);
+                    bf16x2_to_f32(raw4.y, f2, f3);
+                    const float sc = p.scale_log2;
+                    qb[ks][0] = hv ? pack_h2(f0 * sc, f1 * sc) : 0u;
+                    qb[ks][1] = hv ? pack_h2(f2 * sc, f3 * sc) : 0u;
+                } else {
+                    qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c) : 0u;
+                    qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c + 8) : 0u;
+                }
+            }
+        }
+        for (int j = warp; j < nblk; j += kMmaConsumers) {
+            const int st = j % STAGES;
+            if (!mbar_wait_bounded(full0 + 8 * st, (j / STAGES) & 1)) {
+                if (lane == 0) {
+                    flag(p.status, PKV_FLAG_TIMEOUT);
+                    atomicExch(&abort_flag, 1);
+                }
+                break;
+            }
+            if (stage_ok[st]) {
+                const uint32_t kt = ring + st * STAGE;
+                const uint32_t vt = kt + TILE;
+                // ---- S^T = K . Q^T ----
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                const int lr = lane & 7, mi = lane >> 3;
+                if constexpr (kI8) {
+#pragma unroll
+                    for (int kp = 0; kp < 4; ++kp) {  // chunks 2kp, 2kp+1 (16 dims each)
+                        const int y = (mi & 1) * 8 + lr;
+                        const int ch = 2 * kp + (mi >> 1);
+                        uint32_t rr[4];
+                        ldsm_x4(kt + y * 128 + ((ch ^ (y & 7)) << 4), rr);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t lo = rr[2 * h] ^ 0x80808080u;      // rows r
+                            const uint32_t hi = rr[2 * h + 1] ^ 0x80808080u;  // rows r + 8
+                            uint32_t a[4];
+                            a[0] = s8b_pair_to_h2(lo, 0x5140);
+                            a[1] = s8b_pair_to_h2(hi, 0x5140);
+                            a[2] = s8b_pair_to_h2(lo, 0x5342);
+                            a[3] = s8b_pair_to_h2(hi, 0x5342);
+                            mma16816<true>(s, a, qb[2 * kp + h][0], qb[2 * kp + h][1]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int y = (mi & 1) * 8 + lr;
+                        const int ch = (ks & 3) * 2 + (mi >> 1);
+                        uint32_t a[4];
+                        ldsm_x4(kt + (ks >> 2) * G::BOX + y * 128 + ((ch ^ (y & 7)) << 4), a);
+                        mma16816<false>(s, a, qb[ks][0], qb[ks][1]);
+                    }
+                }
+                // s[0] = (tok r, head 2c), s[1] = (tok r, 2c+1), s[2] = (tok r+8, 2c), s[3] = (tok r+8, 2c+1)
+                const int nvalid = t1 - (t0 + j * kBlockSize);  // >= 1; >= 16 for full blocks
+                const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+                float vs0 = 1.f, vs1 = 1.f;
+                if constexpr (kI8) {
+                    const float* sc = scl + st * 2 * kBlockSize;
+                    const float ks0 = sc[r], ks1 = sc[r + 8];
+                    vs0 = sc[kBlockSize + r];
+                    vs1 = sc[kBlockSize + r + 8];
+                    s[0] *= ks0; s[1] *= ks0; s[2] *= ks1; s[3] *= ks1;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[e] *= p.scale_log2;
+                }
+                s[0] = v0 ? s[0] : kNegInf;
+                s[1] = v0 ? s[1] : kNegInf;
+                s[2] = v1 ? s[2] : kNegInf;
+                s[3] = v1 ? s[3] : kNegInf;
+                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int off = 4; off <= 16; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const bool up0 = mx0 > m[0] + kRescaleThreshold;
+                const bool up1 = mx1 > m[1] + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, up0 || up1)) {
+                    const float n0 = up0 ? mx0 : m[0], n1 = up1 ? mx1 : m[1];
+                    const float a0 = up0 ? ex2(m[0] - n0) : 1.f, a1 = up1 ? ex2(m[1] - n1) : 1.f;
+                    m[0] = n0;
+                    m[1] = n1;
+                    l[0] *= a0;
+                    l[1] *= a1;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        o[i][0] *= a0; o[i][2] *= a0;
+                        o[i][1] *= a1; o[i][3] *= a1;
+                    }
+                }
+                const float ms0 = m[0] == kNegInf ? 0.f : m[0], ms1 = m[1] == kNegInf ? 0.f : m[1];
+                const float p0 = ex2(s[0] - ms0), p1 = ex2(s[1] - ms1);
+                const float p2 = ex2(s[2] - ms0), p3 = ex2(s[3] - ms1);
+                l[0] += p0 + p2;
+                l[1] += p1 + p3;
+                // ---- O^T += V^T . P^T ----
+                uint32_t pb0, pb1;
+                if constexpr (kI8) {
+                    pb0 = movm_t(pack_h2(p0 * vs0, p1 * vs0));
+                    pb1 = movm_t(pack_h2(p2 * vs1, p3 * vs1));
+                } else {
+                    pb0 = movm_t(pack_bf16(p0, p1));
+                    pb1 = movm_t(pack_bf16(p2, p3));
+                }
+                const bool partial = nvalid < kBlockSize;
+                if constexpr (kI8) {
+                    // tokens 2c, 2c+1, 2c+8, 2c+9; bytes [16r, 16r+16) of each row (chunk r)
+                    uint4 vr[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int tok = 2 * c + (q & 1) + (q >> 1) * 8;
+                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(vr[q].x), "=r"(vr[q].y), "=r"(vr[q].z), "=r"(vr[q].w)
+                                     : "r"(vt + tok * 128 + ((r ^ (tok & 7)) << 4)));
+                        if (partial && tok >= nvalid) vr[q] = make_uint4(0u, 0u, 0u, 0u);  // int8 zeros
+                        vr[q].x ^= 0x80808080u; vr[q].y ^= 0x80808080u;
+                        vr[q].z ^= 0x80808080u; vr[q].w ^= 0x80808080u;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        // m-tile i: A row r <- dim 16r + 2i, row r+8 <- dim 16r + 2i + 1
+                        const int bo = 2 * (i & 1);
+                        const uint32_t sel = bo | ((4 + bo) << 4) | ((bo + 1) << 8) | ((5 + bo) << 12);
+                        const uint32_t* x0 = reinterpret_cast<const uint32_t*>(&vr[0]);
+                        const uint32_t* x1 = reinterpret_cast<const uint32_t*>(&vr[1]);
+                        const uint32_t* x2 = reinterpret_cast<const uint32_t*>(&vr[2]);
+                        const uint32_t* x3 = reinterpret_cast<const uint32_t*>(&vr[3]);
+                        const uint32_t tA = __byte_perm(x0[i >> 1], x1[i >> 1], sel);  // tokens 2c, 2c+1
+                        const uint32_t tB = __byte_perm(x2[i >> 1], x3[i >> 1], sel);  // tokens 2c+8, 2c+9
+                        uint32_t a[4];
+                        a[0] = s8b_pair_to_h2(tA, 0x5140);
+                        a[1] = s8b_pair_to_h2(tA, 0x5342);
+                        a[2] = s8b_pair_to_h2(tB, 0x5140);
+                        a[3] = s8b_pair_to_h2(tB, 0x5342);
+                        mma16816<true>(o[i], a, pb0, pb1);
+                    }
+                } else {
+                    const int lr2 = lane & 7, mi2 = lane >> 3;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int y = (mi2 >> 1) * 8 + lr2;
+                        const int ch = (i & 3) * 2 + (mi2 & 1);
+                        uint32_t a[4];
+                        ldsm_x4_t(vt + (i >> 2) * G::BOX + y * 128 + ((ch ^ (y & 7)) << 4), a);
+                        if (partial) {  // zero the token columns past the context
+                            const bool k0 = 2 * c < nvalid, k1 = 2 * c + 1 < nvalid;
+                            const bool k8 = 2 * c + 8 < nvalid, k9 = 2 * c + 9 < nvalid;
+                            const uint32_t mlo = (k0 ? 0xffffu : 0u) | (k1 ? 0xffff0000u : 0u);
+                            const uint32_t mhi = (k8 ? 0xffffu : 0u) | (k9 ? 0xffff0000u : 0u);
+                            a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
+                        }
+                        mma16816<false>(o[i], a, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        }
+        // finish l over the 8 token rows (lanes with the same c)
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+        }
+    }
+
+    __syncthreads();  // every consumer is done with the ring
+    if (abort_flag) {
+        if (warp == kMmaConsumers && lane == 0) {  // let issued copies land before exiting
+            for (int j = nblk - STAGES < 0 ? 0 : nblk - STAGES; j < nblk; ++j)
+                mbar_wait_bounded(full0 + 8 * (j % STAGES), (j / STAGES) & 1);
+        }
+        return;
+    }
+    // ---- merge the consumer warps' states (ring memory reused) ----
+    float* sm_m = reinterpret_cast<float*>(smem);               // [4][8]
+    float* sm_l = sm_m + kMmaConsumers * kMmaHeads;               // [4][8]
+    float* sm_o = sm_l + kMmaConsumers * kMmaHeads;               // [4][8][128]
+    if (warp < kMmaConsumers) {
+        if (r == 0) {
+            sm_m[warp * 8 + 2 * c] = m[0];
+            sm_m[warp * 8 + 2 * c + 1] = m[1];
+            sm_l[warp * 8 + 2 * c] = l[0];
+            sm_l[warp * 8 + 2 * c + 1] = l[1];
+        }
+        float* ow = sm_o + warp * kMmaHeads * kMmaD;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int d0 = kI8 ? 16 * r + 2 * i : 16 * i + r;
+            const int d1 = kI8 ? d0 + 1 : d0 + 8;
+            ow[(2 * c) * kMmaD + d0] = o[i][0];
+            ow[(2 * c + 1) * kMmaD + d0] = o[i][1];
+            ow[(2 * c) * kMmaD + d1] = o[i][2];
+            ow[(2 * c + 1) * kMmaD + d1] = o[i][3];
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < kMmaHeads * kMmaD; e += kMmaThreads) {
+        const int hh = e / kMmaD, d = e % kMmaD;
+        if (hh >= nh) continue;
+        float M = kNegInf;
+#pragma unroll
+        for (int w = 0; w < kMmaConsumers; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
+        float L = 0.f, A = 0.f;
+        if (M != kNegInf) {
+#pragma unroll
+            for (int w = 0; w < kMmaConsumers; ++w) {
+                const float wt = ex2(sm_m[w * 8 + hh] - M);
+                L = fmaf(wt, sm_l[w * 8 + hh], L);
+                A = fmaf(wt, sm_o[(w * kMmaHeads + hh) * kMmaD + d], A);
+            }
+        }
+        const size_t qh = (size_t)b * p.Hq + h0 + hh;
+        if (ns == 1) {
+            store_out<__nv_bfloat16>(static_cast<__nv_bfloat16*>(p.out) + qh * kMmaD + d, L > 0.f ? A / L : 0.f);
+        } else {
+            const size_t u = qh * p.max_splits + split;
+            p.ws_acc[u * kMmaD + d] = A;
+            if (d == 0) {
+                p.ws_ml[2 * u] = M;
+                p.ws_ml[2 * u + 1] = L;
+            }
+        }
+    }
+}
+
+}  // namespace pkv

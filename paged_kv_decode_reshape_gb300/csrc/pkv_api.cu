@@ -77,8 +77,12 @@ pkv_status run_decode(const Decode& a) {
     if (!aligned(a.block_tables, 4) || !aligned(a.context_lens, 4)) return PKV_ERR_INVALID_ARG;
     if (a.B > 65535) return PKV_ERR_UNSUPPORTED;  // grid.z
     const int g = a.Hq / a.Hkv;
-    const int hg = heads_per_cta(g);
+    // head_dim 128 bf16 / INT8 pools run on the tensor-core kernel (8 heads per CTA); fp32 and
+    // head_dim 64 on the CUDA-core kernel
+    const bool mma = a.D == 128 && (a.kv_dtype == PKV_BF16 || a.kv_dtype == PKV_I8);
+    const int hg = mma ? 8 : heads_per_cta(g);
     const int head_chunks = (g + hg - 1) / hg;
+    if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
     const int chunk = choose_chunk(a.max_ctx, a.chunk_req);
@@ -116,7 +120,14 @@ pkv_status run_decode(const Decode& a) {
     p.scale_log2 = a.scale * kLog2e;
 
     cudaError_t e;
-    if (a.kv_dtype == PKV_F32) e = launch_split_f32(p, a.D, hg, a.stream);
+    if (mma) {
+        CUtensorMap tk, tv;
+        const bool i8m = a.kv_dtype == PKV_I8;
+        if (!make_pool_tensor_map(&tk, a.k_pool, a.NB, a.Hkv, i8m) ||
+            !make_pool_tensor_map(&tv, a.v_pool, a.NB, a.Hkv, i8m))
+            return PKV_ERR_CUDA;
+        e = launch_split_mma(p, i8m, tk, tv, a.stream);
+    } else if (a.kv_dtype == PKV_F32) e = launch_split_f32(p, a.D, hg, a.stream);
     else if (a.kv_dtype == PKV_BF16) e = launch_split_bf16(p, a.D, hg, a.stream);
     else e = launch_split_i8(p, a.D, hg, a.stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;

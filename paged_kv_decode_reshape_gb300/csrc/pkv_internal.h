@@ -1,6 +1,7 @@
 // pkv_internal.h -- internal interface between the C ABI (pkv_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -77,5 +78,11 @@ cudaError_t launch_split_f32(const SplitParams& p, int D, int heads_per_cta, cud
 cudaError_t launch_split_bf16(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_split_i8(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, pkv_dtype out_dtype, int D, cudaStream_t s);
+
+// Tensor-core split kernel for head_dim 128, bf16 or INT8 pools, 8 query heads per CTA; the K and
+// V pools are described by TMA tensor maps built with make_pool_tensor_map (false on failure).
+bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, bool i8);
+cudaError_t launch_split_mma(const SplitParams& p, bool i8, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t s);
 
 }  // namespace pkv

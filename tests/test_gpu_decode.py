@@ -103,7 +103,10 @@ def test_forced_split_sizes(chunk):
 
 
 def test_split_partials_match_oracle_partials():
-    """The workspace holds each split's (m, l, acc); m is kept in base-2 units."""
+    """The workspace holds each split's (m, l, acc), m in base-2 units. m is a reference max
+    (the kernel only raises it when scores exceed it by more than 2^8), so a split's state is
+    compared through what does not depend on the reference: the log-sum-exp m + log(l) and the
+    normalised accumulator acc / l."""
     w = W.make_config(2, B=3, ctx_lo=100, ctx_hi=700, seed=4)
     chunk = 64
     d = DevWorkload(w)
@@ -123,9 +126,12 @@ def test_split_partials_match_oracle_partials():
     for b in range(w.B):
         k = int(ns[b])
         assert k > 1
-        np.testing.assert_allclose(ml[b, :, :k, 0] * math.log(2), m[b, :, :k], atol=1e-4)
-        np.testing.assert_allclose(ml[b, :, :k, 1], l[b, :, :k], rtol=1e-4)
-        np.testing.assert_allclose(acc[b, :, :k], oacc[b, :, :k], rtol=1e-3, atol=1e-3)
+        gm, gl = ml[b, :, :k, 0] * math.log(2), ml[b, :, :k, 1]
+        assert np.all(gm <= m[b, :, :k] + 1e-3)                      # never above the true max
+        assert np.all(gm >= m[b, :, :k] - 8 * math.log(2) - 1e-3)    # within 2^8 of it
+        np.testing.assert_allclose(gm + np.log(gl), m[b, :, :k] + np.log(l[b, :, :k]), atol=2e-3)
+        np.testing.assert_allclose(acc[b, :, :k] / gl[..., None],
+                                   oacc[b, :, :k] / l[b, :, :k, None], atol=5e-3)
 
 
 @pytest.mark.parametrize("cfg", [2, 4])
