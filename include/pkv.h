@@ -148,6 +148,39 @@ pkv_status pkv_paged_decode_attention_int8(void* out, const void* q, const int8_
                                            size_t workspace_bytes, int32_t* status,
                                            void* stream);
 
+/*
+ * Paged decode attention that allocates nothing and takes no workspace argument.
+ *
+ * The pages this library follows have no counterpart of this entry point: it exists for callers
+ * that cannot call cudaMalloc -- a plugin running inside another runtime's memory plan, where the
+ * host framework owns every device allocation and offers none for scratch, or a latency-critical
+ * loop where an allocation and the device-wide synchronisation it can bring are not acceptable.
+ *
+ * Same arguments, semantics and errors as pkv_paged_decode_attention without `workspace` and
+ * `workspace_bytes`: the split-K partial states go to a fixed array of
+ * PKV_STATIC_WORKSPACE_BYTES bytes inside the library (a file-scope __device__ array; every GPU
+ * that loads the library holds it until the process exits). A batch whose partial states need
+ * more than that (pkv_decode_workspace_bytes(...) > PKV_STATIC_WORKSPACE_BYTES) is refused with
+ * PKV_ERR_WORKSPACE before anything is enqueued; a larger split_chunk_tokens needs less.
+ * The first call made while a given device is current looks up the array's device address on
+ * that device (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture. The current device must be the one `stream` belongs to.
+ * All calls share the one array per device and it keeps the last call's contents (nothing in it
+ * needs to start at zero): calls whose work overlaps on the GPU -- on different streams, or from
+ * different host threads -- race on it and must be serialised by the caller.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (32u << 20)
+
+pkv_status pkv_paged_decode_attention_static_ws(void* out, const void* q, const void* k_pool,
+                                                const void* v_pool, const int32_t* block_tables,
+                                                const int32_t* context_lens, int num_seqs,
+                                                int num_q_heads, int num_kv_heads, int head_dim,
+                                                int block_size, int num_blocks,
+                                                int max_blocks_per_seq, int max_context_len,
+                                                float scale, pkv_dtype dtype,
+                                                int split_chunk_tokens, int32_t* status,
+                                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,10 @@ SIGNATURES = {
                                     _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_decode_attention_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                          _I, _I, _F, _I, _P, _SZ, _P, _P], _I),
+    "pkv_paged_decode_attention_static_ws": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                              _I, _F, _I, _I, _P, _P], _I),
 }
+STATIC_WORKSPACE_BYTES = 32 << 20  # PKV_STATIC_WORKSPACE_BYTES
 
 _lib = None
 
@@ -143,3 +146,19 @@ def paged_decode_attention_int8(out, q, k_pool, v_pool, k_scales, v_scales, bloc
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream))
     _check(rc, "paged_decode_attention_int8")
+
+
+def paged_decode_attention_static_ws(out, q, k_pool, v_pool, block_tables, context_lens,
+                                     max_context_len, scale, split_chunk_tokens=0, status=None,
+                                     stream=None):
+    """pkv_paged_decode_attention_static_ws: as paged_decode_attention, with the split-K partial
+    states in the library's fixed device array instead of a caller-allocated workspace (for
+    callers that cannot allocate device memory). Calls that overlap on the GPU race on that
+    array."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_decode_attention_static_ws(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
+        B, Hq, Hkv, D, BS, NB, block_tables.shape[1], int(max_context_len), float(scale),
+        _kv_code(q), int(split_chunk_tokens), _ptr(status), _stream(stream))
+    _check(rc, "paged_decode_attention_static_ws")

@@ -1,0 +1,85 @@
+"""pkv_paged_decode_attention_static_ws: the entry point for callers that cannot allocate device
+memory (a plugin inside another runtime's memory plan, a loop where an allocation's implicit
+synchronisation is not acceptable). It takes the split-K scratch from a fixed array inside the
+library, so its answers must match the entry point that takes a caller-allocated workspace.
+
+Collected last on purpose (file name), so a run that stops at the first failure has already run
+every other test; it also passes alone in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import paged_kv_decode_reshape_gb300 as P
+import workloads as W
+
+torch = pytest.importorskip("torch")
+
+
+def _call_static(w, dev, out, chunk, stream):
+    L = P.load()
+    return L.pkv_paged_decode_attention_static_ws(
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(dev["q"].data_ptr()),
+        ctypes.c_void_p(dev["k"].data_ptr()), ctypes.c_void_p(dev["v"].data_ptr()),
+        ctypes.c_void_p(dev["bt"].data_ptr()), ctypes.c_void_p(dev["cl"].data_ptr()),
+        w.B, w.Hq, w.Hkv, w.D, w.BS, w.NB, w.MBPS, w.max_context_len, w.scale,
+        P.BF16 if w.kv_dtype == "bf16" else P.F32, chunk, None,
+        ctypes.c_void_p(stream.cuda_stream))
+
+
+def _upload(w):
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(a).cuda()
+    return dict(q=up(w.q), k=up(w.k_pool), v=up(w.v_pool), bt=up(w.block_tables),
+                cl=up(w.context_lens))
+
+
+@pytest.mark.gpu
+def test_static_workspace_matches_caller_workspace_on_two_calls_in_a_row():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    P.load()
+    stream = torch.cuda.current_stream()
+    # two different batches, each forced into several splits so the scratch is really used
+    cases = [(W.make_config(2, seed=41, B=6, ctx_lo=300, ctx_hi=1500), 64),
+             (W.make_config(2, seed=42, B=9, ctx_lo=50, ctx_hi=2500), 128)]
+    for w, chunk in cases:
+        assert P.decode_workspace_bytes(w.B, w.Hq, w.D, w.max_context_len, chunk) > 0
+    results = []
+    for w, chunk in cases:  # back to back on the same stream, sharing the one static array
+        dev = _upload(w)
+        torch.cuda.synchronize()
+        out = torch.empty_like(dev["q"])
+        assert _call_static(w, dev, out, chunk, stream) == P.OK
+        results.append((w, chunk, dev, out))
+    torch.cuda.synchronize()
+    for w, chunk, dev, out in results:
+        ref = torch.empty_like(dev["q"])
+        P.paged_decode_attention(ref, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"],
+                                 w.max_context_len, w.scale, chunk,
+                                 torch.empty(P.decode_workspace_bytes(w.B, w.Hq, w.D,
+                                                                      w.max_context_len, chunk),
+                                             dtype=torch.uint8, device="cuda"))
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy().astype(np.float64)
+        exp = ref.float().cpu().numpy().astype(np.float64)
+        # the bf16 bar the parity tests use (max-abs 2e-2, mean-abs 2e-3)
+        err = np.abs(got - exp)
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
+
+
+def test_static_workspace_refuses_batches_beyond_its_size():
+    """Partial states larger than the fixed array are refused before anything is enqueued (no
+    CUDA call is made on this path, so it runs without a GPU)."""
+    L = P.load()
+    fake = [ctypes.c_void_p(0x7F0000000000 + i * 0x1000000) for i in range(6)]
+    # 64 seqs x 64 heads x 512 splits (chunk 16, 8192 tokens) x 130 floats >> 32 MiB
+    need = P.decode_workspace_bytes(64, 64, 128, 8192, 16)
+    assert need > P.STATIC_WORKSPACE_BYTES
+    rc = L.pkv_paged_decode_attention_static_ws(*fake, 64, 64, 8, 128, 16, 40000, 512, 8192, 0.1,
+                                                P.BF16, 16, None, None)
+    assert rc == P.ERR_WORKSPACE
