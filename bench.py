@@ -300,8 +300,8 @@ def run_ours(args):
     kns, vns = up(w.k_new_scales), up(w.v_new_scales)
     out = torch.empty_like(q)
     maxc = w.max_context_len
-    chunk = pkv.decode_split_chunk(w.B, maxc, args.chunk)
-    nws = pkv.decode_workspace_bytes(w.B, w.Hq, w.D, maxc, args.chunk)
+    chunk = pkv.decode_split_chunk(w.B, w.Hkv, maxc, args.chunk)
+    nws = pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, args.chunk)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)

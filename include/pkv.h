@@ -94,16 +94,21 @@ pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, void* k_pool
  * Bytes of device workspace pkv_paged_decode_attention[_int8] needs for the split-K partial
  * states (m, l, acc) of a batch: the split count per sequence follows "EchoLLMServing
  * inference framework notes", section 2 (split_num = max(1, context_len // chunk)), so the
- * bound uses max_context_len. split_chunk_tokens = 0 selects the library's default chunk.
- * Returns 0 for invalid arguments. Pure host arithmetic; no CUDA call.
+ * bound uses max_context_len. split_chunk_tokens = 0 selects the library's chunk for this batch
+ * shape (pkv_decode_split_chunk). Returns 0 for invalid arguments. Pure host arithmetic.
  */
-size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len, int split_chunk_tokens);
 
-/* The chunk (tokens per split before block rounding) the library uses for a request of
- * split_chunk_tokens (0 = auto) and this batch shape; 0 for invalid arguments. The split
- * extent (grid size along splits) is max(1, max_context_len / chunk). Pure host arithmetic. */
-int pkv_decode_split_chunk(int num_seqs, int max_context_len, int split_chunk_tokens);
+/* The chunk (tokens per split before block rounding) used for a request of split_chunk_tokens
+ * (0 = auto) and this batch shape; 0 for invalid arguments. The same notes call the chunk a
+ * value calibrated from the GPU's SM count and cache size; the auto rule here aims at about
+ * 4096 (sequence, kv head, split) units for the 152 SMs of a GB300 -- the power of two in
+ * [256, 4096] nearest below num_seqs * num_kv_heads * max_context_len / 4096 -- and grows the
+ * chunk until the split extent max(1, max_context_len / chunk) is at most 8192.
+ * Pure host arithmetic. */
+int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int max_context_len,
+                           int split_chunk_tokens);
 
 /*
  * Paged decode attention ("LLM Primer VI, Chapter 8", section 8.1; "EchoLLMServing inference

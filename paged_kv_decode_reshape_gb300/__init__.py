@@ -23,8 +23,8 @@ SIGNATURES = {
     "pkv_status_string": ([_I], ctypes.c_char_p),
     "pkv_version": ([], ctypes.c_char_p),
     "pkv_kv_cache_write": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
-    "pkv_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
-    "pkv_decode_split_chunk": ([_I, _I, _I], _I),
+    "pkv_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "pkv_decode_split_chunk": ([_I, _I, _I, _I], _I),
     "pkv_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                     _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_decode_attention_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
@@ -106,14 +106,15 @@ def kv_cache_write(k_new, v_new, k_pool, v_pool, slot_mapping, k_new_scales=None
     _check(rc, "kv_cache_write")
 
 
-def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                            split_chunk_tokens=0) -> int:
-    return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
+    return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  max_context_len, split_chunk_tokens))
 
 
-def decode_split_chunk(num_seqs, max_context_len, split_chunk_tokens=0) -> int:
-    return int(load().pkv_decode_split_chunk(num_seqs, max_context_len, split_chunk_tokens))
+def decode_split_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens=0) -> int:
+    return int(load().pkv_decode_split_chunk(num_seqs, num_kv_heads, max_context_len,
+                                             split_chunk_tokens))
 
 
 def paged_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len,

@@ -50,7 +50,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+        tune = os.environ.get("PKV_NVCC_FLAGS", "").split()  # build-time tuning defines
+        cmd = [nvcc(), *ARCH, *FLAGS, *tune, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")

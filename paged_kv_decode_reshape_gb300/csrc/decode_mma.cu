@@ -31,9 +31,8 @@ cudaError_t launch_t(const SplitParams& p, const CUtensorMap& tk, const CUtensor
     auto kern = mma_split_kernel<kI8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.max_splits, p.Hkv * p.head_chunks, p.B);
-    kern<<<grid, kMmaThreads, G::SMEM, s>>>(p, tk, tv);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.B), dim3(G::THREADS), G::SMEM, s,
+                      p, tk, tv);
 }
 
 }  // namespace

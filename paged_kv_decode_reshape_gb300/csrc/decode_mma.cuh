@@ -9,12 +9,14 @@
 // transpose, done with warp-level mma.sync m16n8k16 so that one instruction covers what took
 // 64 FMAs plus conversions, and the kernel stays far from the issue limit at HBM speed.
 //
-// Warp roles (160 threads): warp 4 is the producer -- it reads the split's block ids (validated),
-// and its lane 0 issues, per block, 2-D TMA tensor copies of the K and V tiles into a STAGES-deep
-// ring with 128-byte swizzle (bank-conflict-free ldmatrix), plus 1-D bulk copies of the INT8
-// scale rows, completing on a per-stage "full" mbarrier. Warps 0-3 are consumers: warp w takes
-// blocks w, w+4, ... of the split, keeps its own online-softmax state, and releases each stage on
-// a per-stage "empty" mbarrier. The four states are merged in shared memory at the end.
+// Warp roles: every warp is its own producer and consumer. Warp w takes blocks w, w+NC, ... of
+// the split (NC warps per CTA) and owns the stages w, w+NC, ... of a STAGES-deep shared-memory
+// ring (STAGES = NC * stages per warp). Its lane 0 issues, per block, 2-D TMA tensor copies of
+// the K and V tiles with 128-byte swizzle (bank-conflict-free ldmatrix), plus 1-D bulk copies of
+// the INT8 scale rows, completing on the stage's mbarrier; as soon as the warp has consumed a
+// block it refills that stage with its block STAGES further on. No warp waits for another until
+// the end, where the NC online-softmax states are merged in shared memory. Block ids come from
+// the table 32 at a time (one per lane, validated) a window ahead of use.
 //
 // Per block and consumer warp (tokens on the MMA M dimension, heads on N):
 //   S^T[16 x 8]   = K[16 x 128] . Q^T[128 x 8]      8 MMAs (k = 16 dims each)
@@ -24,11 +26,14 @@
 //   P^T fragments = movmatrix.trans of the score fragments (no shared-memory round trip)
 //   O^T[128 x 8] += V^T[128 x 16] . P^T[16 x 8]       8 MMAs (k = 16 tokens)
 // bf16: K fragments by ldmatrix, V^T fragments by ldmatrix.trans, P rounded to bf16.
-// INT8 ("EchoLLMServing notes", section 3): K bytes by ldmatrix, V bytes by 16-byte loads; both
-// widened exactly to fp16 with the byte-permute conversion of Kim et al. 2022 (1024 + 128 + x as
-// fp16, minus 1152); q is pre-scaled by scale*log2(e) into fp16; the per-token K scale multiplies
-// the score and the V scale the softmax weight. Dims are consumed in a fixed permuted order that
-// q's fragments follow too, which leaves the dot products unchanged.
+// INT8 ("EchoLLMServing notes", section 3): K fragments by ldmatrix and V^T fragments by
+// ldmatrix.trans of the int8 tiles read as 16-bit pairs; each register of 4 int8 becomes two
+// fp16x2 operands holding 1152 + x exactly (byte-permute conversion of Kim et al. 2022), and the
+// constant 1152 is taken out once per score (1152 * sum q') and once per output (1152 * sum of
+// the fp16 weights), not per element. q is pre-scaled by scale*log2(e) into fp16; the per-token
+// K scale multiplies the score and the V scale the softmax weight. Dims are consumed in a fixed
+// permuted order that q's fragments and the output mapping follow, which leaves the dot
+// products unchanged.
 #pragma once
 
 #include <cuda.h>
@@ -41,28 +46,44 @@ namespace pkv {
 
 constexpr int kMmaD = 128;          // head_dim of this path
 constexpr int kMmaHeads = 8;        // MMA N: query heads per CTA
-constexpr int kMmaConsumers = 4;    // consumer warps
-constexpr int kMmaThreads = 32 * (kMmaConsumers + 1);
+// warps per CTA and stages per warp, per element type (build-time tunables)
+#ifndef PKV_MMA_WARPS_BF16
+#define PKV_MMA_WARPS_BF16 4
+#endif
+#ifndef PKV_MMA_SPW_BF16
+#define PKV_MMA_SPW_BF16 2
+#endif
+#ifndef PKV_MMA_WARPS_I8
+#define PKV_MMA_WARPS_I8 4
+#endif
+#ifndef PKV_MMA_SPW_I8
+#define PKV_MMA_SPW_I8 2
+#endif
+#ifndef PKV_MMA_PROXY_FENCE
+#define PKV_MMA_PROXY_FENCE 1
+#endif
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 
 template <bool kI8>
 struct MmaGeom {
+    static constexpr int NC = kI8 ? PKV_MMA_WARPS_I8 : PKV_MMA_WARPS_BF16;  // warps per CTA
+    static constexpr int SPW = kI8 ? PKV_MMA_SPW_I8 : PKV_MMA_SPW_BF16;     // stages per warp
+    static constexpr int THREADS = 32 * NC;
     static constexpr int TILE = kBlockSize * kMmaD * (kI8 ? 1 : 2);  // one K (or V) tile
     static constexpr int BOX = kBlockSize * 128;                     // bytes of one TMA box
     static constexpr int BOXES = TILE / BOX;                         // boxes per tile (2 or 1)
     static constexpr int STAGE = 2 * TILE;                           // K then V
-    // Stage s is only ever consumed by warp s % kMmaConsumers (STAGES is a multiple of the
-    // consumer count), so each warp waits on a stage's phases strictly in order and a parity wait
-    // can never match a phase two behind. 8 stages = two blocks in flight per consumer warp.
-    static constexpr int STAGES = 8;
+    // Stage s is only ever used by warp s % NC, so each warp waits on a stage's phases strictly
+    // in order and a parity wait can never match a phase two behind.
+    static constexpr int STAGES = NC * SPW;
     static constexpr int RING = STAGES * STAGE;
     static constexpr int SCALES = kI8 ? STAGES * 2 * kBlockSize * 4 : 0;
-    static constexpr int MERGE = kMmaConsumers * kMmaHeads * (kMmaD + 2) * 4;
+    static constexpr int MERGE = NC * kMmaHeads * (kMmaD + 2) * 4;
     static constexpr int MAIN = RING > MERGE ? RING : MERGE;
     // + 1024 for aligning the ring to the 128-byte-swizzle atom
-    static constexpr int SMEM = 1024 + MAIN + SCALES + ((STAGES * 4 + 7) & ~7) + 2 * STAGES * 8;
+    static constexpr int SMEM = 1024 + MAIN + SCALES + STAGES * 8;
     static_assert(RING % 1024 == 0 && STAGE % 1024 == 0, "swizzled boxes need 1024-byte alignment");
-    static_assert(STAGES % kMmaConsumers == 0, "a stage must belong to one consumer warp");
+
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -111,13 +132,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// byte-permute int8 -> fp16 helpers: w holds 4 int8 already XOR-ed with 0x80 (biased to x+128)
-__device__ __forceinline__ uint32_t s8b_pair_to_h2(uint32_t w, uint32_t sel) {
-    // bytes of w picked by sel go to the low byte of each fp16 half; high bytes 0x64: 1024 + b
-    uint32_t h = __byte_perm(w, 0x00006464u, sel);
-    __half2 v = __hsub2(*reinterpret_cast<__half2*>(&h), __half2half2(__ushort_as_half(0x6480)));
-    return *reinterpret_cast<uint32_t*>(&v);
-}
+// int8 -> biased fp16, two values per instruction (the byte-permute / magic-number conversion
+// of Kim et al. 2022): placing the byte x + 128 (x XOR 0x80) in the low byte of the fp16 1024
+// gives exactly 1152 + x. For a word of four int8 [b0 b1 b2 b3], lo -> fp16x2(1152+b0, 1152+b2)
+// and hi -> fp16x2(1152+b1, 1152+b3); the sign flip and the exponent byte are one XOR with
+// 0x64806480 after masking. The 1152 offset is removed once per score / per output (below),
+// never per element.
+constexpr float kI8Bias = 1152.0f;
+__device__ __forceinline__ uint32_t i8_lo_h2(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x64806480u; }
+__device__ __forceinline__ uint32_t i8_hi_h2(uint32_t w) { return ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u; }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -130,7 +153,7 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 template <bool kI8>
-__global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParams p,
+__global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const SplitParams p,
                                                                const __grid_constant__ CUtensorMap tmk,
                                                                const __grid_constant__ CUtensorMap tmv) {
     using G = MmaGeom<kI8>;
@@ -141,9 +164,7 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned
     float* scl = reinterpret_cast<float*>(smem + G::MAIN);              // [STAGES][K16 | V16]
-    int32_t* stage_ok = reinterpret_cast<int32_t*>(smem + G::MAIN + G::SCALES);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::MAIN + G::SCALES + ((STAGES * 4 + 7) & ~7));
-    uint64_t* empty = full + STAGES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::MAIN + G::SCALES);
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -153,6 +174,8 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
     const int b = blockIdx.z;
     const int h0 = kvh * p.G + hc * kMmaHeads;
     const int nh = p.G - hc * kMmaHeads < kMmaHeads ? p.G - hc * kMmaHeads : kMmaHeads;
+
+    grid_dependency_wait();  // inputs (new K/V rows, tables) may come from the previous kernel
 
     int n = p.context_lens[b];
     const int ncap = p.MBPS * kBlockSize;
@@ -172,12 +195,9 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
     const int blk0 = t0 / kBlockSize;
 
     const uint32_t ring = smem_addr(smem);
-    const uint32_t full0 = smem_addr(full), empty0 = smem_addr(empty);
+    const uint32_t full0 = smem_addr(full);
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
+        for (int s = 0; s < STAGES; ++s) mbar_init(full0 + 8 * s, 1);
         abort_flag = 0;
         mbar_init_fence();
     }
@@ -192,92 +212,114 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    if (warp == kMmaConsumers) {
-        // ------------------------------ producer warp ------------------------------
-        const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS + blk0;
-        bool dead = false;
-        for (int j0 = 0; j0 < nblk && !dead; j0 += 32) {
-            int id = -1;
-            if (j0 + lane < nblk) {
-                id = bt_row[j0 + lane];
-                if (id < 0 || id >= p.NB) {
-                    flag(p.status, PKV_FLAG_BAD_BLOCK);
-                    id = -1;
-                }
+    // ---- this warp's blocks: k-th is split block j = warp + k * NC, in stage warp + (k % SPW) * NC ----
+    constexpr int NC = G::NC, SPW = G::SPW;
+    const int nmine = nblk > warp ? (nblk - warp + NC - 1) / NC : 0;
+    const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS + blk0;
+    auto load_window = [&](int w) {  // lane i: id of this warp's block 32 * w + i (-1: none / bad)
+        const int k = 32 * w + lane;
+        int id = -1;
+        if (k < nmine) {
+            id = bt_row[warp + k * NC];
+            if (id < 0 || id >= p.NB) {
+                flag(p.status, PKV_FLAG_BAD_BLOCK);
+                id = -1;
             }
-            const int cnt = nblk - j0 < 32 ? nblk - j0 : 32;
-            for (int jj = 0; jj < cnt; ++jj) {
-                const int j = j0 + jj;
-                const int bid = __shfl_sync(0xffffffffu, id, jj);
-                if (lane == 0) {
-                    const int st = j % STAGES;
-                    if (j >= STAGES && !mbar_wait_bounded(empty0 + 8 * st, ((j / STAGES) - 1) & 1)) {
-                        dead = true;
-                    } else {
-                        const uint32_t bar = full0 + 8 * st;
-                        const uint32_t dst = ring + st * STAGE;
-                        stage_ok[st] = bid >= 0;
-                        if (bid >= 0) {
-                            const int row = (bid * p.Hkv + kvh) * kBlockSize;
-                            mbar_arrive_expect_tx(bar, STAGE + (kI8 ? 2 * kBlockSize * 4 : 0));
+        }
+        return id;
+    };
+    int win = 0;
+    int ids_a = load_window(0), ids_b = nmine > 32 ? load_window(1) : -1;
+    auto id_of = [&](int k) {  // warp-uniform; k within windows win, win + 1
+        const int va = __shfl_sync(0xffffffffu, ids_a, k & 31);
+        const int vb = __shfl_sync(0xffffffffu, ids_b, k & 31);
+        return (k >> 5) == win ? va : vb;
+    };
+    auto issue = [&](int k, int bid) {  // lane 0: start this warp's k-th block into its stage
+        const int st = warp + (k % SPW) * NC;
+        const uint32_t bar = full0 + 8 * st;
+        const uint32_t dst = ring + st * STAGE;
+        if (bid >= 0) {
+            const int row = (bid * p.Hkv + kvh) * kBlockSize;
+            mbar_arrive_expect_tx(bar, STAGE + (kI8 ? 2 * kBlockSize * 4 : 0));
 #pragma unroll
-                            for (int x = 0; x < G::BOXES; ++x) {
-                                tma_load_2d(dst + x * G::BOX, &tmk, x * 64 * (kI8 ? 2 : 1), row, bar);
-                                tma_load_2d(dst + TILE + x * G::BOX, &tmv, x * 64 * (kI8 ? 2 : 1), row, bar);
-                            }
-                            if constexpr (kI8) {
-                                const size_t srow = (size_t)bid * p.Hkv + kvh;
-                                const uint32_t sd = smem_addr(scl + st * 2 * kBlockSize);
-                                bulk_g2s(sd, p.k_scales + srow * kBlockSize, kBlockSize * 4, bar);
-                                bulk_g2s(sd + kBlockSize * 4, p.v_scales + srow * kBlockSize, kBlockSize * 4, bar);
-                            }
-                        } else {
-                            mbar_arrive(bar);
-                        }
-                    }
-                }
-                dead = __shfl_sync(0xffffffffu, dead, 0);
-                if (dead) break;
+            for (int x = 0; x < G::BOXES; ++x) {
+                tma_load_2d(dst + x * G::BOX, &tmk, x * 64 * (kI8 ? 2 : 1), row, bar);
+                tma_load_2d(dst + TILE + x * G::BOX, &tmv, x * 64 * (kI8 ? 2 : 1), row, bar);
             }
+            if constexpr (kI8) {
+                const size_t srow = (size_t)bid * p.Hkv + kvh;
+                const uint32_t sd = smem_addr(scl + st * 2 * kBlockSize);
+                bulk_g2s(sd, p.k_scales + srow * kBlockSize, kBlockSize * 4, bar);
+                bulk_g2s(sd + kBlockSize * 4, p.v_scales + srow * kBlockSize, kBlockSize * 4, bar);
+            }
+        } else {
+            mbar_arrive(bar);  // nothing to load: complete the phase so the wait stays in step
         }
-        if (dead && lane == 0) {
-            flag(p.status, PKV_FLAG_TIMEOUT);
-            atomicExch(&abort_flag, 1);
-        }
-    } else {
-        // ------------------------------ consumer warps ------------------------------
+    };
+#pragma unroll 1
+    for (int k = 0; k < SPW && k < nmine; ++k) {
+        const int bid = id_of(k);
+        if (lane == 0) issue(k, bid);
+    }
+
+    {
         // q as the B operand of S^T = K Q^T: b0b1 = (dims k0 + 2c, +1; head r), b2b3 = (+8, +9)
         uint32_t qb[8][2];
+        float qsum = 0.f;  // INT8: sum of this lane's fp16 q' values of head r (as the MMA sees them)
         {
             const bool hv = r < nh;
             const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + h0 + (hv ? r : 0)) * kMmaD;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 if constexpr (kI8) {
-                    // permuted dims: k-pos 2c,2c+1 <- dims 16ks+4c, +1; k-pos 2c+8,2c+9 <- +2, +3
+                    // permuted dims: k-pos 2c,2c+1 <- dims 16ks+4c+0, +2; k-pos 2c+8,2c+9 <- +1, +3
+                    // (the order in which i8_lo_h2 / i8_hi_h2 deliver a row's bytes)
                     const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
                     float f0, f1, f2, f3;
                     bf16x2_to_f32(raw4.x, f0, f1);
                     bf16x2_to_f32(raw4.y, f2, f3);
                     const float sc = p.scale_log2;
-                    qb[ks][0] = hv ? pack_h2(f0 * sc, f1 * sc) : 0u;
-                    qb[ks][1] = hv ? pack_h2(f2 * sc, f3 * sc) : 0u;
+                    qb[ks][0] = hv ? pack_h2(f0 * sc, f2 * sc) : 0u;
+                    qb[ks][1] = hv ? pack_h2(f1 * sc, f3 * sc) : 0u;
+                    const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[ks][0]));
+                    const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[ks][1]));
+                    qsum += (u0.x + u0.y) + (u1.x + u1.y);
                 } else {
                     qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c) : 0u;
                     qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c + 8) : 0u;
                 }
             }
         }
-        for (int j = warp; j < nblk; j += kMmaConsumers) {
-            const int st = j % STAGES;
-            if (!mbar_wait_bounded(full0 + 8 * st, (j / STAGES) & 1)) {
+        // INT8: 1152 * sum_d q'_d of heads 2c and 2c+1 is what the biased K adds to each score
+        float kcorr0 = 0.f, kcorr1 = 0.f, psum[2] = {0.f, 0.f};
+        if constexpr (kI8) {
+            qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+            qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // lanes 4r..4r+3: head r's full sum
+            kcorr0 = kI8Bias * __shfl_sync(0xffffffffu, qsum, 4 * (2 * c));
+            kcorr1 = kI8Bias * __shfl_sync(0xffffffffu, qsum, 4 * (2 * c + 1));
+        }
+#pragma unroll 1
+        for (int k = 0; k < nmine; ++k) {
+            const int j = warp + k * NC;
+            const int st = warp + (k % SPW) * NC;
+            if ((k & 31) == 0 && k > 0) {  // consumption enters the next id window
+                ++win;
+                ids_a = ids_b;
+                ids_b = nmine > 32 * (win + 1) ? load_window(win + 1) : -1;
+            }
+            const int bid = id_of(k);
+            if (!mbar_wait_bounded(full0 + 8 * st, (k / SPW) & 1)) {
                 if (lane == 0) {
                     flag(p.status, PKV_FLAG_TIMEOUT);
                     atomicExch(&abort_flag, 1);
+                    // let this warp's copies already issued land before giving up
+                    for (int q = k; q < k + SPW && q < nmine; ++q)
+                        mbar_wait_bounded(full0 + 8 * (warp + (q % SPW) * NC), (q / SPW) & 1);
                 }
                 break;
             }
-            if (stage_ok[st]) {
+            if (bid >= 0) {
                 const uint32_t kt = ring + st * STAGE;
                 const uint32_t vt = kt + TILE;
                 // ---- S^T = K . Q^T ----
@@ -292,13 +334,13 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
                         ldsm_x4(kt + y * 128 + ((ch ^ (y & 7)) << 4), rr);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const uint32_t lo = rr[2 * h] ^ 0x80808080u;      // rows r
-                            const uint32_t hi = rr[2 * h + 1] ^ 0x80808080u;  // rows r + 8
+                            const uint32_t lo = rr[2 * h];      // token r: bytes 4c..4c+3
+                            const uint32_t hi = rr[2 * h + 1];  // token r + 8
                             uint32_t a[4];
-                            a[0] = s8b_pair_to_h2(lo, 0x5140);
-                            a[1] = s8b_pair_to_h2(hi, 0x5140);
-                            a[2] = s8b_pair_to_h2(lo, 0x5342);
-                            a[3] = s8b_pair_to_h2(hi, 0x5342);
+                            a[0] = i8_lo_h2(lo);
+                            a[1] = i8_lo_h2(hi);
+                            a[2] = i8_hi_h2(lo);
+                            a[3] = i8_hi_h2(hi);
                             mma16816<true>(s, a, qb[2 * kp + h][0], qb[2 * kp + h][1]);
                         }
                     }
@@ -321,7 +363,8 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
                     const float ks0 = sc[r], ks1 = sc[r + 8];
                     vs0 = sc[kBlockSize + r];
                     vs1 = sc[kBlockSize + r + 8];
-                    s[0] *= ks0; s[1] *= ks0; s[2] *= ks1; s[3] *= ks1;
+                    s[0] = (s[0] - kcorr0) * ks0; s[1] = (s[1] - kcorr1) * ks0;
+                    s[2] = (s[2] - kcorr0) * ks1; s[3] = (s[3] - kcorr1) * ks1;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[e] *= p.scale_log2;
@@ -345,6 +388,8 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
                     m[1] = n1;
                     l[0] *= a0;
                     l[1] *= a1;
+                    psum[0] *= a0;
+                    psum[1] *= a1;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         o[i][0] *= a0; o[i][2] *= a0;
@@ -359,43 +404,45 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
                 // ---- O^T += V^T . P^T ----
                 uint32_t pb0, pb1;
                 if constexpr (kI8) {
-                    pb0 = movm_t(pack_h2(p0 * vs0, p1 * vs0));
-                    pb1 = movm_t(pack_h2(p2 * vs1, p3 * vs1));
+                    const uint32_t h01 = pack_h2(p0 * vs0, p1 * vs0);
+                    const uint32_t h23 = pack_h2(p2 * vs1, p3 * vs1);
+                    // the weights exactly as the MMA uses them: their sum times 1152 is what
+                    // the biased V adds to each output
+                    const float2 w01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+                    const float2 w23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+                    psum[0] += w01.x + w23.x;
+                    psum[1] += w01.y + w23.y;
+                    pb0 = movm_t(h01);
+                    pb1 = movm_t(h23);
                 } else {
                     pb0 = movm_t(pack_bf16(p0, p1));
                     pb1 = movm_t(pack_bf16(p2, p3));
                 }
                 const bool partial = nvalid < kBlockSize;
                 if constexpr (kI8) {
-                    // tokens 2c, 2c+1, 2c+8, 2c+9; bytes [16r, 16r+16) of each row (chunk r)
-                    uint4 vr[4];
+                    // V^T fragments by ldmatrix.trans of the int8 tile read as 16-bit pairs: for
+                    // 16-byte chunk j the lane gets [V(2c,d) V(2c,d+1) V(2c+1,d) V(2c+1,d+1)] with
+                    // d = 16j + 2r, i.e. A rows r <- dim d and r + 8 <- dim d + 1 of m-tile j.
+                    // Tokens past the context need no masking: their weight is 0 and every biased
+                    // int8 value is finite.
+                    const int lr2 = lane & 7, mi2 = lane >> 3;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int tok = 2 * c + (q & 1) + (q >> 1) * 8;
-                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                     : "=r"(vr[q].x), "=r"(vr[q].y), "=r"(vr[q].z), "=r"(vr[q].w)
-                                     : "r"(vt + tok * 128 + ((r ^ (tok & 7)) << 4)));
-                        if (partial && tok >= nvalid) vr[q] = make_uint4(0u, 0u, 0u, 0u);  // int8 zeros
-                        vr[q].x ^= 0x80808080u; vr[q].y ^= 0x80808080u;
-                        vr[q].z ^= 0x80808080u; vr[q].w ^= 0x80808080u;
-                    }
+                    for (int jp = 0; jp < 4; ++jp) {  // chunks 2jp, 2jp+1
+                        const int y = (mi2 & 1) * 8 + lr2;
+                        const int ch = 2 * jp + (mi2 >> 1);
+                        uint32_t rr[4];
+                        ldsm_x4_t(vt + y * 128 + ((ch ^ (y & 7)) << 4), rr);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        // m-tile i: A row r <- dim 16r + 2i, row r+8 <- dim 16r + 2i + 1
-                        const int bo = 2 * (i & 1);
-                        const uint32_t sel = bo | ((4 + bo) << 4) | ((bo + 1) << 8) | ((5 + bo) << 12);
-                        const uint32_t* x0 = reinterpret_cast<const uint32_t*>(&vr[0]);
-                        const uint32_t* x1 = reinterpret_cast<const uint32_t*>(&vr[1]);
-                        const uint32_t* x2 = reinterpret_cast<const uint32_t*>(&vr[2]);
-                        const uint32_t* x3 = reinterpret_cast<const uint32_t*>(&vr[3]);
-                        const uint32_t tA = __byte_perm(x0[i >> 1], x1[i >> 1], sel);  // tokens 2c, 2c+1
-                        const uint32_t tB = __byte_perm(x2[i >> 1], x3[i >> 1], sel);  // tokens 2c+8, 2c+9
-                        uint32_t a[4];
-                        a[0] = s8b_pair_to_h2(tA, 0x5140);
-                        a[1] = s8b_pair_to_h2(tA, 0x5342);
-                        a[2] = s8b_pair_to_h2(tB, 0x5140);
-                        a[3] = s8b_pair_to_h2(tB, 0x5342);
-                        mma16816<true>(o[i], a, pb0, pb1);
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t t0w = rr[2 * h];      // tokens 2c, 2c+1
+                            const uint32_t t8w = rr[2 * h + 1];  // tokens 2c+8, 2c+9
+                            uint32_t a[4];
+                            a[0] = i8_lo_h2(t0w);
+                            a[1] = i8_hi_h2(t0w);
+                            a[2] = i8_lo_h2(t8w);
+                            a[3] = i8_hi_h2(t8w);
+                            mma16816<true>(o[2 * jp + h], a, pb0, pb1);
+                        }
                     }
                 } else {
                     const int lr2 = lane & 7, mi2 = lane >> 3;
@@ -416,30 +463,44 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            __syncwarp();  // every lane is done reading the stage
+            if (k + SPW < nmine) {
+                const int nb = id_of(k + SPW);
+                if (lane == 0) {
+#if PKV_MMA_PROXY_FENCE
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads before the async write
+#endif
+                    issue(k + SPW, nb);
+                }
+            }
         }
-        // finish l over the 8 token rows (lanes with the same c)
+        // finish l (and the INT8 weight sums) over the 8 token rows (lanes with the same c)
 #pragma unroll
         for (int off = 4; off <= 16; off <<= 1) {
             l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
             l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+            if constexpr (kI8) {
+                psum[0] += __shfl_xor_sync(0xffffffffu, psum[0], off);
+                psum[1] += __shfl_xor_sync(0xffffffffu, psum[1], off);
+            }
+        }
+        if constexpr (kI8) {  // remove the 1152 offset of the biased V from every output
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i][0] -= kI8Bias * psum[0]; o[i][2] -= kI8Bias * psum[0];
+                o[i][1] -= kI8Bias * psum[1]; o[i][3] -= kI8Bias * psum[1];
+            }
         }
     }
 
-    __syncthreads();  // every consumer is done with the ring
-    if (abort_flag) {
-        if (warp == kMmaConsumers && lane == 0) {  // let issued copies land before exiting
-            for (int j = nblk - STAGES < 0 ? 0 : nblk - STAGES; j < nblk; ++j)
-                mbar_wait_bounded(full0 + 8 * (j % STAGES), (j / STAGES) & 1);
-        }
-        return;
-    }
+    __syncthreads();  // every warp is done with the ring (its copies all consumed or drained)
+    if (abort_flag) return;
+    grid_dependents_launch();  // the merge kernel may start launching
     // ---- merge the consumer warps' states (ring memory reused) ----
-    float* sm_m = reinterpret_cast<float*>(smem);               // [4][8]
-    float* sm_l = sm_m + kMmaConsumers * kMmaHeads;               // [4][8]
-    float* sm_o = sm_l + kMmaConsumers * kMmaHeads;               // [4][8][128]
-    if (warp < kMmaConsumers) {
+    float* sm_m = reinterpret_cast<float*>(smem);               // [NC][8]
+    float* sm_l = sm_m + G::NC * kMmaHeads;               // [NC][8]
+    float* sm_o = sm_l + G::NC * kMmaHeads;               // [NC][8][128]
+    {
         if (r == 0) {
             sm_m[warp * 8 + 2 * c] = m[0];
             sm_m[warp * 8 + 2 * c + 1] = m[1];
@@ -449,7 +510,7 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
         float* ow = sm_o + warp * kMmaHeads * kMmaD;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int d0 = kI8 ? 16 * r + 2 * i : 16 * i + r;
+            const int d0 = kI8 ? 16 * i + 2 * r : 16 * i + r;
             const int d1 = kI8 ? d0 + 1 : d0 + 8;
             ow[(2 * c) * kMmaD + d0] = o[i][0];
             ow[(2 * c + 1) * kMmaD + d0] = o[i][1];
@@ -458,16 +519,16 @@ __global__ void __launch_bounds__(kMmaThreads) mma_split_kernel(const SplitParam
         }
     }
     __syncthreads();
-    for (int e = tid; e < kMmaHeads * kMmaD; e += kMmaThreads) {
+    for (int e = tid; e < kMmaHeads * kMmaD; e += G::THREADS) {
         const int hh = e / kMmaD, d = e % kMmaD;
         if (hh >= nh) continue;
         float M = kNegInf;
 #pragma unroll
-        for (int w = 0; w < kMmaConsumers; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
+        for (int w = 0; w < G::NC; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
         float L = 0.f, A = 0.f;
         if (M != kNegInf) {
 #pragma unroll
-            for (int w = 0; w < kMmaConsumers; ++w) {
+            for (int w = 0; w < G::NC; ++w) {
                 const float wt = ex2(sm_m[w * 8 + hh] - M);
                 L = fmaf(wt, sm_l[w * 8 + hh], L);
                 A = fmaf(wt, sm_o[(w * kMmaHeads + hh) * kMmaD + d], A);

@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
     const int h0 = kvh * p.G + hc * HG;          // first query head of this CTA
     const int nh = cmin(HG, p.G - hc * HG);      // query heads this CTA produces
 
+    grid_dependency_wait();  // inputs (new K/V rows, tables) may come from the previous kernel
+
     // context length, clamped to what the block table can address
     int n = p.context_lens[b];
     const int ncap = p.MBPS * kBlockSize;
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
         }
     }
 
+    grid_dependents_launch();  // the merge kernel may start launching
     // merge the per-thread states of the CTA (the ring is idle: every issued copy was consumed)
     float* red_m = reinterpret_cast<float*>(smem);
     float* red_l = red_m + TPP * HG;
@@ -362,9 +365,7 @@ cudaError_t launch_split_t(const SplitParams& p, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid(p.max_splits, p.Hkv * p.head_chunks, p.B);
-    kern<<<grid, G::NT, G::SMEM, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.B), dim3(G::NT), G::SMEM, s, p);
 }
 
 template <typename KV, typename QT>

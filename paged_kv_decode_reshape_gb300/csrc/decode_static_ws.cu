@@ -46,7 +46,7 @@ extern "C" pkv_status pkv_paged_decode_attention_static_ws(
     int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
     pkv_dtype dtype, int split_chunk_tokens, int32_t* status, void* stream) {
     // bytes of partial states this batch needs; beyond the array's size the call is refused
-    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
+    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                    max_context_len, split_chunk_tokens);
     if (need > (size_t)PKV_STATIC_WORKSPACE_BYTES) return PKV_ERR_WORKSPACE;
     void* ws = nullptr;

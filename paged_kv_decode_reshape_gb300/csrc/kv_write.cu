@@ -15,6 +15,8 @@ namespace pkv {
 namespace {
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
+    grid_dependency_wait();    // the new K/V rows may come from the kernel before this one
+    grid_dependents_launch();  // let the attention kernel start its launch meanwhile
     const int vpr = p.row_bytes / 16;
     const long long per_pool = (long long)p.T * p.Hkv * vpr;
     const long long total = 2 * per_pool;
@@ -53,8 +55,7 @@ cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s) {
     if (total == 0) return cudaSuccess;
     long long blocks = (total + 255) / 256;
     if (blocks > 152 * 32) blocks = 152 * 32;  // grid-stride beyond 32 CTAs per SM
-    kv_write_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kv_write_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
 }
 
 }  // namespace pkv

@@ -24,11 +24,15 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 size_t elem_bytes(pkv_dtype t) { return t == PKV_F32 ? 4 : t == PKV_BF16 ? 2 : t == PKV_I8 ? 1 : 0; }
 
-// Tokens per split before block rounding: the request, or in auto mode the default chunk,
-// doubled until the split extent fits the merge kernel.
-int choose_chunk(int max_context_len, int requested) {
+// Tokens per split before block rounding: the request, or in auto mode the power of two in
+// [kMinAutoChunk, kMaxAutoChunk] nearest below (work units of the batch) / kTargetUnits, so that
+// a batch yields about kTargetUnits units for the GPU's SMs to share; doubled further while the
+// split extent exceeds what the merge kernel supports.
+int choose_chunk(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
     if (requested > 0) return requested;
-    int c = kDefaultChunk;
+    const long long tokens = (long long)num_seqs * num_kv_heads * max_context_len;
+    int c = kMinAutoChunk;
+    while (c < kMaxAutoChunk && tokens / (2LL * c) >= kTargetUnits) c *= 2;
     while (max_context_len / c > kMaxSplits) c *= 2;
     return c;
 }
@@ -85,7 +89,7 @@ pkv_status run_decode(const Decode& a) {
     if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
-    const int chunk = choose_chunk(a.max_ctx, a.chunk_req);
+    const int chunk = choose_chunk(a.B, a.Hkv, a.max_ctx, a.chunk_req);
     const int S = split_extent(a.max_ctx, chunk);
     if (S > kMaxSplits) return PKV_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes_for(a.B, a.Hq, a.D, S);
@@ -194,18 +198,20 @@ pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, void* k_pool
     return launch_kv_write(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-int pkv_decode_split_chunk(int num_seqs, int max_context_len, int split_chunk_tokens) {
-    (void)num_seqs;
-    if (max_context_len < 0 || split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize) return 0;
-    return choose_chunk(max_context_len, split_chunk_tokens);
+int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int max_context_len,
+                           int split_chunk_tokens) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0 || split_chunk_tokens < 0 ||
+        split_chunk_tokens % kBlockSize)
+        return 0;
+    return choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens);
 }
 
-size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len, int split_chunk_tokens) {
-    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
-        split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize)
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_context_len < 0 || split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize)
         return 0;
-    const int chunk = choose_chunk(max_context_len, split_chunk_tokens);
+    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens);
     return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
 }
 

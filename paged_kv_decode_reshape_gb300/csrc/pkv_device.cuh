@@ -56,12 +56,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier to complete; false if kWaitLimitNs elapsed first.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Same test, but the warp may be suspended in hardware for up to `hint_ns` waiting for the phase
+// (it resumes as soon as the phase completes), so a waiting warp does not spin on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete; false if kWaitLimitNs elapsed first. The
+// clock is read once per 64 polls so the loop costs few issue slots. With `backoff_ns` > 0 the
+// warp also sleeps between polls (for waits whose latency matters less than the issue slots
+// they would take from other warps).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t backoff_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i) {
+            if (mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
+            if (backoff_ns) __nanosleep(backoff_ns);
+        }
         if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
@@ -150,6 +171,14 @@ template <>
 __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float v) {
     *p = __float2bfloat16_rn(v);
 }
+
+// Programmatic dependent launch: every kernel of this library is launched so that it may start
+// while the kernel before it in the stream is finishing. grid_dependency_wait() blocks until that
+// kernel has completed and its memory is visible -- each kernel calls it before its first read of
+// anything a previous kernel may have written. grid_dependents_launch() lets the next kernel in
+// the stream begin launching once every CTA of this one has called it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);

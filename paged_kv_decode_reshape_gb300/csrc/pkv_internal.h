@@ -6,13 +6,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/pkv.h"
+#include "pkv.h"  // include/ is on the compiler include path
 
 namespace pkv {
 
 constexpr int kBlockSize = 16;      // tokens per KV block (the only size built)
 constexpr int kMaxSplits = 8192;    // split extent the merge kernel supports
-constexpr int kDefaultChunk = 512;  // tokens per split before block rounding (auto mode)
+constexpr int kMinAutoChunk = 256;   // auto chunk range (tokens per split before block rounding)
+constexpr int kMaxAutoChunk = 4096;
+constexpr long long kTargetUnits = 4096;  // (sequence, kv head, split) units the auto chunk aims at
 
 // Split rule ("EchoLLMServing inference framework notes", section 2, FlashDecoding):
 // split_num = max(1, n // chunk), capped at max_splits; each split is a whole number of
@@ -72,7 +74,24 @@ struct WriteParams {
     int T, Hkv, row_bytes, NB;
 };
 
-// Launchers (return the cudaGetLastError() after the launch).
+// Launch `kern` on `s` with programmatic stream serialization (see grid_dependency_wait()).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// Launchers (return the launch's error code).
 cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_split_f32(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_split_bf16(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);

@@ -61,7 +61,7 @@ class DevWorkload:
         torch = _torch()
         w = self.w
         maxc = w.max_context_len if max_context_len is None else max_context_len
-        nbytes = P.decode_workspace_bytes(w.B, w.Hq, w.D, maxc, chunk)
+        nbytes = P.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, chunk)
         if workspace is None and nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         if out is None:

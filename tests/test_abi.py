@@ -53,13 +53,21 @@ def test_status_strings(pkv):
 
 def test_workspace_arithmetic(pkv):
     L = P.load()
-    # 8 seqs x 32 heads, 131072 tokens, auto chunk 512 -> 256 splits x (128 acc + m + l) fp32
-    assert L.pkv_decode_workspace_bytes(8, 32, 128, 131072, 0) == 8 * 32 * 256 * 130 * 4
-    assert L.pkv_decode_workspace_bytes(8, 32, 128, 131072, 1024) == 8 * 32 * 128 * 130 * 4
-    assert L.pkv_decode_workspace_bytes(4, 4, 64, 100, 0) == 0       # one split: no workspace
-    assert L.pkv_decode_workspace_bytes(4, 4, 64, 100, 17) == 0      # chunk not a block multiple
-    assert L.pkv_decode_split_chunk(1, 1 << 30, 0) >= 512            # auto keeps splits <= 8192
-    assert (1 << 30) // L.pkv_decode_split_chunk(1, 1 << 30, 0) <= 8192
+    # 8 seqs x 32 q / 8 kv heads, 131072 tokens: auto chunk 2048 -> 64 splits x (128 acc + m + l)
+    assert L.pkv_decode_split_chunk(8, 8, 131072, 0) == 2048
+    assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 0) == 8 * 32 * 64 * 130 * 4
+    assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 1024) == 8 * 32 * 128 * 130 * 4
+    assert L.pkv_decode_workspace_bytes(4, 4, 4, 64, 100, 0) == 0    # one split: no workspace
+    assert L.pkv_decode_workspace_bytes(4, 4, 4, 64, 100, 17) == 0   # chunk not a block multiple
+    # auto chunk: ~4096 units, powers of two in [256, 4096], more only to keep splits <= 8192
+    assert L.pkv_decode_split_chunk(64, 8, 4055, 0) == 256
+    assert L.pkv_decode_split_chunk(128, 8, 8083, 0) == 1024
+    assert L.pkv_decode_split_chunk(256, 8, 4090, 0) == 1024
+    assert L.pkv_decode_split_chunk(4, 4, 100, 0) == 256
+    assert L.pkv_decode_split_chunk(1024, 64, 1 << 20, 0) == 4096
+    assert L.pkv_decode_split_chunk(1, 1, 1 << 30, 0) >= 4096
+    assert (1 << 30) // L.pkv_decode_split_chunk(1, 1, 1 << 30, 0) <= 8192
+    assert L.pkv_decode_split_chunk(4, 4, 100, 48) == 48             # explicit request kept
 
 
 def _attn(L, **kw):

@@ -48,7 +48,7 @@ def test_static_workspace_matches_caller_workspace_on_two_calls_in_a_row():
     cases = [(W.make_config(2, seed=41, B=6, ctx_lo=300, ctx_hi=1500), 64),
              (W.make_config(2, seed=42, B=9, ctx_lo=50, ctx_hi=2500), 128)]
     for w, chunk in cases:
-        assert P.decode_workspace_bytes(w.B, w.Hq, w.D, w.max_context_len, chunk) > 0
+        assert P.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.max_context_len, chunk) > 0
     results = []
     for w, chunk in cases:  # back to back on the same stream, sharing the one static array
         dev = _upload(w)
@@ -61,7 +61,7 @@ def test_static_workspace_matches_caller_workspace_on_two_calls_in_a_row():
         ref = torch.empty_like(dev["q"])
         P.paged_decode_attention(ref, dev["q"], dev["k"], dev["v"], dev["bt"], dev["cl"],
                                  w.max_context_len, w.scale, chunk,
-                                 torch.empty(P.decode_workspace_bytes(w.B, w.Hq, w.D,
+                                 torch.empty(P.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D,
                                                                       w.max_context_len, chunk),
                                              dtype=torch.uint8, device="cuda"))
         torch.cuda.synchronize()
@@ -78,7 +78,7 @@ def test_static_workspace_refuses_batches_beyond_its_size():
     L = P.load()
     fake = [ctypes.c_void_p(0x7F0000000000 + i * 0x1000000) for i in range(6)]
     # 64 seqs x 64 heads x 512 splits (chunk 16, 8192 tokens) x 130 floats >> 32 MiB
-    need = P.decode_workspace_bytes(64, 64, 128, 8192, 16)
+    need = P.decode_workspace_bytes(64, 64, 8, 128, 8192, 16)
     assert need > P.STATIC_WORKSPACE_BYTES
     rc = L.pkv_paged_decode_attention_static_ws(*fake, 64, 64, 8, 128, 16, 40000, 512, 8192, 0.1,
                                                 P.BF16, 16, None, None)
