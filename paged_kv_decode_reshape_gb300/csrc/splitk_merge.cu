@@ -6,11 +6,11 @@
 //     M = max_j m_j,   w_j = 2^(m_j - M),   L = sum_j w_j l_j,   out = sum_j w_j acc_j / L
 // Sequences with a single split were finished by kernel 1 and are skipped here.
 //
-// One CTA of 256 threads per (query head, sequence): J = 256 / (D/4) groups of D/4 threads, each
-// group reading whole accumulator rows as float4. A group folds its rows j = g, g + J, ... into a
-// running (m, l, acc) of its own as it loads them (the same online rescaling kernel 1 uses), so
-// the row loads do not wait for the global maximum; the J group states are then combined once in
-// shared memory. Two dependent global round trips in all: context_lens, then the rows.
+// One warp per (sequence, query head), eight per CTA, so the whole batch is one wave of CTAs.
+// Lane i owns D/32 consecutive columns. The warp loads its split rows eight at a time as
+// independent loads and folds each into a running (m, l, acc) (the online rescaling kernel 1
+// uses), so no load waits for the global maximum: two dependent global round trips in all
+// (context_lens, then the rows).
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -19,18 +19,24 @@ namespace pkv {
 
 namespace {
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 8;  // rows in flight per warp
+
+template <int V> struct Vec;
+template <> struct Vec<2> { using T = float2; };
+template <> struct Vec<4> { using T = float4; };
 
 template <typename OT, int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-    constexpr int DQ = D / 4;                   // float4 columns per row
-    constexpr int J = kMergeThreads / DQ;       // row groups
-    __shared__ float g_m[J], g_l[J];
-    __shared__ __align__(16) float g_acc[J][D];
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p) {
+    constexpr int V = D / 32;  // columns per lane
+    using VT = typename Vec<V>::T;
 
     grid_dependency_wait();  // partial states of the split kernel before this one in the stream
 
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int pair = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (pair >= p.B * p.Hq) return;
+    const int b = pair / p.Hq;
     int n = p.context_lens[b];
     const int ncap = p.MBPS * kBlockSize;
     n = n < 0 ? 0 : (n > ncap ? ncap : n);
@@ -38,54 +44,45 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const int ns = split_count(n, p.chunk, p.max_splits, &per);
     if (ns <= 1) return;
 
-    const size_t base = ((size_t)b * p.Hq + h) * p.max_splits;
-    const float* ml = p.ws_ml + 2 * base;
-    const int dq = tid % DQ, g = tid / DQ;
-    const float4* accp = reinterpret_cast<const float4*>(p.ws_acc + base * D) + dq;
-
-    float m = -INFINITY, l = 0.f;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-    for (int j = g; j < ns; j += J) {
-        const float mj = ml[2 * j], lj = ml[2 * j + 1];
-        const float4 v = accp[(size_t)j * DQ];
-        if (mj == -INFINITY) continue;  // a split with no valid token contributes nothing
-        const float mn = fmaxf(m, mj);
-        const float s0 = ex2(m - mn), s1 = ex2(mj - mn);  // m == -inf: s0 = 0
-        l = l * s0 + lj * s1;
-        a.x = a.x * s0 + v.x * s1;
-        a.y = a.y * s0 + v.y * s1;
-        a.z = a.z * s0 + v.z * s1;
-        a.w = a.w * s0 + v.w * s1;
-        m = mn;
-    }
-    if (dq == 0) {
-        g_m[g] = m;
-        g_l[g] = l;
-    }
-    reinterpret_cast<float4*>(g_acc[g])[dq] = a;
-    __syncthreads();
-    OT* out = static_cast<OT*>(p.out) + ((size_t)b * p.Hq + h) * D;
-    for (int d = tid; d < D; d += kMergeThreads) {
-        float M = -INFINITY;
+    const size_t base = (size_t)pair * p.max_splits;
+    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + base;
+    const VT* acc = reinterpret_cast<const VT*>(p.ws_acc + base * D) + lane;
+    float m = -INFINITY, l = 0.f, a[V];
 #pragma unroll
-        for (int r = 0; r < J; ++r) M = fmaxf(M, g_m[r]);
-        float L = 0.f, A = 0.f;
-        if (M != -INFINITY) {
+    for (int e = 0; e < V; ++e) a[e] = 0.f;
+    for (int j0 = 0; j0 < ns; j0 += kMergeBatch) {
+        float2 st[kMergeBatch];
+        VT v[kMergeBatch];
 #pragma unroll
-            for (int r = 0; r < J; ++r) {
-                const float w = ex2(g_m[r] - M);
-                L = fmaf(w, g_l[r], L);
-                A = fmaf(w, g_acc[r][d], A);
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (j0 + u < ns) {
+                st[u] = ml[j0 + u];
+                v[u] = acc[(size_t)(j0 + u) * (D / V)];
             }
         }
-        store_out<OT>(out + d, L > 0.f ? A / L : 0.f);
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (j0 + u >= ns || st[u].x == -INFINITY) continue;  // empty split: no contribution
+            const float mn = fmaxf(m, st[u].x);
+            const float s0 = ex2(m - mn), s1 = ex2(st[u].x - mn);  // m == -inf: s0 = 0
+            l = l * s0 + st[u].y * s1;
+            const float* vv = reinterpret_cast<const float*>(&v[u]);
+#pragma unroll
+            for (int e = 0; e < V; ++e) a[e] = a[e] * s0 + vv[e] * s1;
+            m = mn;
+        }
     }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    OT* out = static_cast<OT*>(p.out) + (size_t)pair * D + lane * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) store_out<OT>(out + e, a[e] * inv);
 }
 
 template <typename OT, int D>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
-    return launch_pdl(merge_kernel<OT, D>, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, s, p);
+    const int pairs = p.B * p.Hq;
+    return launch_pdl(merge_kernel<OT, D>, dim3((pairs + kMergeWarps - 1) / kMergeWarps),
+                      dim3(32 * kMergeWarps), 0, s, p);
 }
 
 }  // namespace
