@@ -39,6 +39,10 @@ def lib():
         L.orc_paged_decode_partials.restype = I
         L.orc_merge_partials.argtypes = [P, P, P, P, P, I, I, I, I]
         L.orc_merge_partials.restype = I
+        L.orc_kv_cache_write_quant.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I]
+        L.orc_kv_cache_write_quant.restype = I
+        L.orc_quantize_row_int8.argtypes = [P, ctypes.c_size_t, I, I, P, P]
+        L.orc_quantize_row_int8.restype = None
         L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
         L.orc_bf16_to_double.restype = D
         _lib = L
@@ -93,6 +97,37 @@ def kv_cache_write(k_new, v_new, k_pool, v_pool, slot_mapping, k_new_scales=None
                                   _ptr(_c(k_new_scales, np.float32)),
                                   _ptr(_c(v_new_scales, np.float32)), _ptr(ks), _ptr(vs),
                                   _ptr(sm), T, Hkv, D, BS, NB, _code(kp))
+    if check:
+        _check(rc)
+    return kp, vp, ks, vs
+
+
+def quantize_rows_int8(x):
+    """int8 codes and fp32 scales of each last-axis row of x (float32 or bf16 bits)."""
+    x = np.ascontiguousarray(x)
+    D = x.shape[-1]
+    rows = x.reshape(-1, D)
+    codes = np.zeros(rows.shape, np.int8)
+    scales = np.zeros(rows.shape[0], np.float32)
+    for r in range(rows.shape[0]):
+        lib().orc_quantize_row_int8(_ptr(rows), r * D, D, _code(rows),
+                                    _ptr(codes[r:r + 1]), _ptr(scales[r:r + 1]))
+    return codes.reshape(x.shape), scales.reshape(x.shape[:-1])
+
+
+def kv_cache_write_quant(k_new, v_new, k_pool, v_pool, k_scales, v_scales, slot_mapping,
+                         check=True):
+    """Quantise new rows (float32 or bf16 bits, [T, Hkv, D]) into copies of the int8 pools and
+    scale arrays; returns (k_pool, v_pool, k_scales, v_scales)."""
+    kp, vp = np.array(k_pool, dtype=np.int8, copy=True), np.array(v_pool, dtype=np.int8, copy=True)
+    ks = np.array(k_scales, dtype=np.float32, copy=True)
+    vs = np.array(v_scales, dtype=np.float32, copy=True)
+    kn, vn = np.ascontiguousarray(k_new), np.ascontiguousarray(v_new)
+    sm = _c(slot_mapping, np.int64)
+    NB, Hkv, BS, D = kp.shape
+    rc = lib().orc_kv_cache_write_quant(_ptr(kn), _ptr(vn), _ptr(kp), _ptr(vp), _ptr(ks),
+                                        _ptr(vs), _ptr(sm), sm.shape[0], Hkv, D, BS, NB,
+                                        _code(kn))
     if check:
         _check(rc)
     return kp, vp, ks, vs

@@ -111,6 +111,63 @@ int orc_kv_cache_write(const void* k_new, const void* v_new, void* k_pool, void*
 }
 
 /* ------------------------------------------------------------------------------------------
+ * Quantising KV write [ECHO3: INT8 KV cache with a per-token scale]. Each (token, kv head) row x
+ * of D values (fp32 or bf16) is stored as int8 codes with one fp32 scale, in fp32 arithmetic:
+ *   amax = max_d |x_d|,  scale = amax / 127 (1 if that is 0),
+ *   code_d = clamp(rint(x_d / scale), -127, 127)   (rint: round half to even)
+ * The scale is symmetric per row, so the largest-magnitude element maps to +-127. Reading where
+ * the page is silent: the divisor 127 and half-even rounding follow the int8 recipe of the input
+ * generator; codes never use -128. Then the row goes to its slot as in orc_kv_cache_write.
+ * ---------------------------------------------------------------------------------------- */
+static float load_f32(const void* base, size_t idx, int dtype) {
+    if (dtype == ORC_F32) return ((const float*)base)[idx];
+    uint32_t u = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void orc_quantize_row_int8(const void* src, size_t off, int D, int dtype, int8_t* codes,
+                           float* scale_out) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(load_f32(src, off + d, dtype));
+        if (a > amax) amax = a;
+    }
+    float scale = amax / 127.0f;
+    if (scale == 0.0f) scale = 1.0f;
+    for (int d = 0; d < D; ++d) {
+        float q = rintf(load_f32(src, off + d, dtype) / scale);
+        if (q > 127.0f) q = 127.0f;
+        if (q < -127.0f) q = -127.0f;
+        codes[d] = (int8_t)q;
+    }
+    *scale_out = scale;
+}
+
+int orc_kv_cache_write_quant(const void* k_new, const void* v_new, int8_t* k_pool, int8_t* v_pool,
+                             float* k_scales, float* v_scales, const int64_t* slot_mapping, int T,
+                             int Hkv, int D, int BS, int NB, int src_dtype) {
+    if ((src_dtype != ORC_F32 && src_dtype != ORC_BF16) || T < 0 || Hkv <= 0 || D <= 0 ||
+        BS <= 0 || NB < 0)
+        return ORC_BAD_ARG;
+    int status = ORC_OK;
+    for (int i = 0; i < T; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= (int64_t)NB * BS) { status = ORC_BAD_SLOT; continue; }
+        int64_t blk = s / BS, off = s % BS;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t dst = ((size_t)blk * Hkv + h) * BS + (size_t)off;
+            size_t src = ((size_t)i * Hkv + h) * (size_t)D;
+            orc_quantize_row_int8(k_new, src, D, src_dtype, k_pool + dst * D, &k_scales[dst]);
+            orc_quantize_row_int8(v_new, src, D, src_dtype, v_pool + dst * D, &v_scales[dst]);
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------------------------
  * Split rule [ECHO2, FlashDecoding answer]: split_num = max(1, n // chunk), capped at
  * max_splits (the grid's split extent, max(1, max_context_len // chunk)). Each split covers
  * a whole number of blocks: per = ceil(n / split_num) rounded up to BS; split j is

@@ -278,3 +278,62 @@ def test_write_then_attend_sees_new_token(orc):
     out = orc.paged_decode_attention(w.q, kp, vp, w.block_tables, w.context_lens, w.scale)
     # sequence 0 has one token: the new one
     np.testing.assert_array_equal(out[0], w.v_new[0].astype(np.float64))
+
+
+# ---- quantising INT8 write (EchoLLMServing notes, section 3: per-token scale) -------------------
+
+def test_quantize_rounds_half_to_even_at_unit_scale(orc):
+    """amax 127 makes the scale exactly 1, so codes are rint(x): halves go to the even code."""
+    x = np.zeros((1, 64), np.float32)
+    vals = [127.0, -127.0, 2.5, 3.5, -2.5, 0.5, 1.5, -0.5, 126.5, 0.0]
+    x[0, :len(vals)] = vals
+    codes, scale = orc.quantize_rows_int8(x)
+    assert scale[0] == 1.0
+    assert list(codes[0, :len(vals)]) == [127, -127, 2, 4, -2, 0, 2, 0, 126, 0]
+
+
+def test_quantize_zero_row_and_power_of_two_scaling(orc):
+    codes, scale = orc.quantize_rows_int8(np.zeros((1, 128), np.float32))
+    assert scale[0] == 1.0 and not codes.any()
+    x = np.random.default_rng(2).standard_normal((6, 128)).astype(np.float32)
+    c0, s0 = orc.quantize_rows_int8(x)
+    for k in (-3, 5):  # a power-of-two factor scales the scale exactly and leaves the codes
+        c1, s1 = orc.quantize_rows_int8((x * np.float32(2.0 ** k)).astype(np.float32))
+        assert np.array_equal(c0, c1) and np.array_equal(s1, s0 * np.float32(2.0 ** k))
+
+
+def test_quantize_error_bound_and_extremes(orc):
+    x = np.random.default_rng(4).standard_normal((50, 128)).astype(np.float32) * 3
+    codes, scale = orc.quantize_rows_int8(x)
+    err = np.abs(codes.astype(np.float64) * scale[:, None] - x)
+    assert (err <= scale[:, None].astype(np.float64) * (0.5 + 1e-5)).all()
+    amax_at = np.argmax(np.abs(x), axis=1)
+    assert (np.abs(codes[np.arange(50), amax_at]) == 127).all()
+    assert codes.min() >= -127
+
+
+def test_quantize_matches_generator_recipe_bit_exact(orc):
+    """The numpy input recipe (workloads) is an independent statement of the same rule."""
+    x = np.random.default_rng(6).standard_normal((40, 128)).astype(np.float32)
+    c_np, s_np = W.quantize_int8_rows(x)
+    c_or, s_or = orc.quantize_rows_int8(x)
+    assert np.array_equal(c_np, c_or) and np.array_equal(s_np, s_or)
+    xb = W.f32_to_bf16_bits(x)  # bf16 source rows widen exactly before quantising
+    c_b, s_b = orc.quantize_rows_int8(xb)
+    c_n2, s_n2 = W.quantize_int8_rows(W.bf16_bits_to_f32(xb))
+    assert np.array_equal(c_b, c_n2) and np.array_equal(s_b, s_n2)
+
+
+def test_kv_write_quant_places_rows_like_the_copy_write(orc):
+    NB, Hkv, BS, D = 3, 2, 16, 64
+    kn = np.random.default_rng(8).standard_normal((2, Hkv, D)).astype(np.float32)
+    vn = -kn
+    slots = np.array([20, 47], np.int64)
+    kp = np.zeros((NB, Hkv, BS, D), np.int8)
+    ks = np.zeros((NB, Hkv, BS), np.float32)
+    k2, v2, ks2, vs2 = orc.kv_cache_write_quant(kn, vn, kp, kp.copy(), ks, ks.copy(), slots)
+    c, sc = orc.quantize_rows_int8(kn)
+    assert np.array_equal(k2[1, :, 4], c[0]) and np.array_equal(ks2[1, :, 4], sc[0])
+    assert np.array_equal(k2[2, :, 15], c[1]) and np.array_equal(ks2[2, :, 15], sc[1])
+    assert np.array_equal(v2[1, :, 4], -c[0])
+    assert np.count_nonzero(ks2) == 4
