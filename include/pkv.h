@@ -91,6 +91,24 @@ pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, void* k_pool
                               int num_blocks, pkv_dtype dtype, int32_t* status, void* stream);
 
 /*
+ * Quantising KV write for an INT8 cache ("EchoLLMServing inference framework notes", section 3:
+ * INT8 KV cache with a per-token scale, dequantised inside the attention kernel). For every token
+ * i with s = slot_mapping[i] >= 0 and kv head h, the row x = k_new[i][h][:] (fp32 or bf16,
+ * src_dtype) is stored as
+ *     scale = max_d |x_d| / 127            (1 if the row is all zeros)
+ *     k_pool[s / 16][h][s % 16][d] = clamp(rint(x_d / scale), -127, 127)   (round half to even)
+ *     k_scales[s / 16][h][s % 16]   = scale
+ * in IEEE fp32 arithmetic (so it is bit-reproducible), and likewise for V. Codes never use -128.
+ * Slot rules, flags and errors as pkv_kv_cache_write. Dequantised values x_d ~ code * scale are
+ * within scale / 2 of x_d.
+ */
+pkv_status pkv_kv_cache_write_int8(const void* k_new, const void* v_new, int8_t* k_pool,
+                                   int8_t* v_pool, float* k_scales, float* v_scales,
+                                   const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks,
+                                   pkv_dtype src_dtype, int32_t* status, void* stream);
+
+/*
  * Bytes of device workspace pkv_paged_decode_attention[_int8] needs for the split-K partial
  * states (m, l, acc) of a batch: the split count per sequence follows "EchoLLMServing
  * inference framework notes", section 2 (split_num = max(1, context_len // chunk)), so the

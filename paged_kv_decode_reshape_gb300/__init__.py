@@ -23,6 +23,7 @@ SIGNATURES = {
     "pkv_status_string": ([_I], ctypes.c_char_p),
     "pkv_version": ([], ctypes.c_char_p),
     "pkv_kv_cache_write": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_kv_cache_write_int8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
     "pkv_decode_split_chunk": ([_I, _I, _I, _I], _I),
     "pkv_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
@@ -104,6 +105,18 @@ def kv_cache_write(k_new, v_new, k_pool, v_pool, slot_mapping, k_new_scales=None
         _ptr(v_new_scales), _ptr(k_scales), _ptr(v_scales), _ptr(slot_mapping), T, Hkv, D, BS,
         NB, _kv_code(k_pool), _ptr(status), _stream(stream))
     _check(rc, "kv_cache_write")
+
+
+def kv_cache_write_int8(k_new, v_new, k_pool, v_pool, k_scales, v_scales, slot_mapping,
+                        status=None, stream=None):
+    """pkv_kv_cache_write_int8: quantise fp32/bf16 rows k_new/v_new [T, Hkv, D] into int8 pools
+    [NB, Hkv, 16, D] and fp32 scales [NB, Hkv, 16] at their slots."""
+    T, Hkv, D = k_new.shape
+    NB, _, BS, _ = k_pool.shape
+    rc = load().pkv_kv_cache_write_int8(
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+        _ptr(slot_mapping), T, Hkv, D, BS, NB, _kv_code(k_new), _ptr(status), _stream(stream))
+    _check(rc, "kv_cache_write_int8")
 
 
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,

@@ -48,7 +48,74 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
     }
 }
 
+// Quantising write ("EchoLLMServing inference framework notes", section 3: an INT8 KV cache
+// with a per-token scale): each (token, kv head) row of K or V becomes int8 codes plus one fp32
+// scale, scale = max|x| / 127 (1 for an all-zero row), code = clamp(rint(x / scale), -127, 127),
+// all in IEEE fp32 (correctly rounded divide, round-half-even rint) so the result is bit-exact.
+// One warp per row: lane i holds D/32 consecutive values, the row maximum is a warp reduction,
+// and the codes go out as one 32- or 16-bit store per lane.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) kv_write_quant_kernel(const QuantWriteParams p) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    constexpr int V = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long rows = (long long)p.T * p.Hkv;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < 2 * rows; w += nwarps) {
+        const int which = w >= rows;  // 0: K, 1: V
+        const long long r = w - which * rows;
+        const int h = (int)(r % p.Hkv);
+        const long long i = r / p.Hkv;
+        const long long s = p.slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= (long long)p.NB * kBlockSize) {
+            if (lane == 0 && h == 0 && which == 0) flag(p.status, PKV_FLAG_BAD_SLOT);
+            continue;
+        }
+        const T* src = static_cast<const T*>(which ? p.v_new : p.k_new) + r * D + lane * V;
+        float x[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            if constexpr (sizeof(T) == 4) x[e] = reinterpret_cast<const float*>(src)[e];
+            else x[e] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[e]);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float scale = amax / 127.0f;
+        if (scale == 0.0f) scale = 1.0f;
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            float q = rintf(x[e] / scale);
+            q = fminf(fmaxf(q, -127.0f), 127.0f);
+            packed |= (uint32_t)(uint8_t)(int8_t)q << (8 * e);
+        }
+        const long long dst_row = ((s / kBlockSize) * p.Hkv + h) * kBlockSize + s % kBlockSize;
+        int8_t* dst = (which ? p.v_pool : p.k_pool) + dst_row * D + lane * V;
+        if constexpr (V == 4) *reinterpret_cast<uint32_t*>(dst) = packed;
+        else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+        if (lane == 0) (which ? p.v_scales : p.k_scales)[dst_row] = scale;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_write_quant(const QuantWriteParams& p, pkv_dtype src, int D, cudaStream_t s) {
+    const long long rows = 2LL * p.T * p.Hkv;
+    if (rows == 0) return cudaSuccess;
+    long long blocks = (rows + 7) / 8;  // 8 warps (rows) per CTA
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    const dim3 g((unsigned)blocks), b(256);
+    if (src == PKV_F32)
+        return D == 128 ? launch_pdl(kv_write_quant_kernel<float, 128>, g, b, 0, s, p)
+                        : launch_pdl(kv_write_quant_kernel<float, 64>, g, b, 0, s, p);
+    return D == 128 ? launch_pdl(kv_write_quant_kernel<__nv_bfloat16, 128>, g, b, 0, s, p)
+                    : launch_pdl(kv_write_quant_kernel<__nv_bfloat16, 64>, g, b, 0, s, p);
+}
 
 cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s) {
     const long long total = 2LL * p.T * p.Hkv * (p.row_bytes / 16);

@@ -198,6 +198,42 @@ pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, void* k_pool
     return launch_kv_write(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_kv_cache_write_int8(const void* k_new, const void* v_new, int8_t* k_pool,
+                                   int8_t* v_pool, float* k_scales, float* v_scales,
+                                   const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks,
+                                   pkv_dtype src_dtype, int32_t* status, void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (src_dtype != PKV_F32 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_pool || !v_pool || !k_scales || !v_scales || !slot_mapping)
+        return PKV_ERR_INVALID_ARG;
+    for (const void* ptr : {k_new, v_new, (const void*)k_pool, (const void*)v_pool})
+        if (!aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_scales, 4) || !aligned(v_scales, 4) || !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    const size_t new_b = (size_t)num_tokens * num_kv_heads * head_dim * elem_bytes(src_dtype);
+    const size_t pool_b = (size_t)num_blocks * num_kv_heads * kBlockSize * head_dim;
+    const size_t sc_b = (size_t)num_blocks * num_kv_heads * kBlockSize * 4;
+    const void* outs[4] = {k_pool, v_pool, k_scales, v_scales};
+    const size_t out_b[4] = {pool_b, pool_b, sc_b, sc_b};
+    for (int i = 0; i < 4; ++i) {
+        if (overlap(outs[i], out_b[i], k_new, new_b) || overlap(outs[i], out_b[i], v_new, new_b))
+            return PKV_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], out_b[i], outs[j], out_b[j])) return PKV_ERR_INVALID_ARG;
+    }
+    QuantWriteParams p{};
+    p.k_new = k_new; p.v_new = v_new; p.k_pool = k_pool; p.v_pool = v_pool;
+    p.k_scales = k_scales; p.v_scales = v_scales; p.slot_mapping = slot_mapping; p.status = status;
+    p.T = num_tokens; p.Hkv = num_kv_heads; p.NB = num_blocks;
+    return launch_kv_write_quant(p, src_dtype, head_dim, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int max_context_len,
                            int split_chunk_tokens) {
     if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0 || split_chunk_tokens < 0 ||

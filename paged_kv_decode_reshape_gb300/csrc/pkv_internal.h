@@ -91,8 +91,21 @@ cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t sm
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+struct QuantWriteParams {
+    const void* k_new;          // [T][Hkv][D] fp32 or bf16
+    const void* v_new;
+    int8_t* k_pool;             // [NB][Hkv][16][D]
+    int8_t* v_pool;
+    float* k_scales;            // [NB][Hkv][16]
+    float* v_scales;
+    const int64_t* slot_mapping;
+    int32_t* status;
+    int T, Hkv, NB;
+};
+
 // Launchers (return the launch's error code).
 cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s);
+cudaError_t launch_kv_write_quant(const QuantWriteParams& p, pkv_dtype src, int D, cudaStream_t s);
 cudaError_t launch_split_f32(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_split_bf16(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_split_i8(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);

@@ -143,3 +143,23 @@ def _write(L, **kw):
 ])
 def test_write_argument_checks(pkv, kw, expect):
     assert _write(P.load(), **kw) == expect
+
+
+@fake_ptrs
+@pytest.mark.parametrize("kw,expect", [
+    (dict(kn=None), P.ERR_INVALID_ARG),
+    (dict(ks=None), P.ERR_INVALID_ARG),
+    (dict(src=P.I8), P.ERR_INVALID_ARG),                               # source must be fp32/bf16
+    (dict(D=96), P.ERR_UNSUPPORTED),
+    (dict(vp=FAKE[2]), P.ERR_INVALID_ARG),                              # K and V pools alias
+    (dict(vs=FAKE[4]), P.ERR_INVALID_ARG),                              # K and V scales alias
+    (dict(T=0, kn=None), P.OK),
+])
+def test_quant_write_argument_checks(pkv, kw, expect):
+    a = dict(kn=FAKE[0], vn=FAKE[1], kp=FAKE[2], vp=FAKE[3], ks=FAKE[4], vs=FAKE[5], sm=FAKE[6],
+             T=4, Hkv=8, D=128, BS=16, NB=64, src=P.BF16)
+    a.update(kw)
+    rc = P.load().pkv_kv_cache_write_int8(a["kn"], a["vn"], a["kp"], a["vp"], a["ks"], a["vs"],
+                                          a["sm"], a["T"], a["Hkv"], a["D"], a["BS"], a["NB"],
+                                          a["src"], None, None)
+    assert rc == expect

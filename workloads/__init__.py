@@ -103,6 +103,8 @@ class DecodeWorkload:
     k_new_scales: Optional[np.ndarray] = None  # float32 [T, Hkv]
     v_new_scales: Optional[np.ndarray] = None
     shared_prefix_blocks: int = 0
+    k_new_src: Optional[np.ndarray] = None     # bf16 bits [T, Hkv, D]: unquantised new rows (int8)
+    v_new_src: Optional[np.ndarray] = None
 
     @property
     def MBPS(self) -> int:
@@ -179,15 +181,24 @@ def make_decode(*, name, B, Hq, Hkv, D, context_lens, kv_dtype, q_dtype, seed,
         n = int(lens[b])
         if n > 0:
             slots[b] = int(bt[b, (n - 1) // BS]) * BS + (n - 1) % BS
-    k_new, k_new_scales = _draw_kv(rng, (B, Hkv, D), kv_dtype)
-    v_new, v_new_scales = _draw_kv(rng, (B, Hkv, D), kv_dtype)
+    if kv_dtype == "i8":
+        # new rows arrive from the model in bf16; the pre-quantised copies follow the same recipe
+        k_new_src = f32_to_bf16_bits(rng.standard_normal(size=(B, Hkv, D), dtype=np.float32))
+        v_new_src = f32_to_bf16_bits(rng.standard_normal(size=(B, Hkv, D), dtype=np.float32))
+        k_new, k_new_scales = quantize_int8_rows(bf16_bits_to_f32(k_new_src))
+        v_new, v_new_scales = quantize_int8_rows(bf16_bits_to_f32(v_new_src))
+    else:
+        k_new_src = v_new_src = None
+        k_new, k_new_scales = _draw_kv(rng, (B, Hkv, D), kv_dtype)
+        v_new, v_new_scales = _draw_kv(rng, (B, Hkv, D), kv_dtype)
     return DecodeWorkload(
         name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, BS=BS, NB=NB, kv_dtype=kv_dtype,
         q_dtype=q_dtype, q=q, k_pool=k_pool, v_pool=v_pool, block_tables=bt,
         context_lens=lens.astype(np.int32), slot_mapping=slots, k_new=k_new, v_new=v_new,
         scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
         ref_count=pool.ref_count, k_scales=k_scales, v_scales=v_scales,
-        k_new_scales=k_new_scales, v_new_scales=v_new_scales, shared_prefix_blocks=npre)
+        k_new_scales=k_new_scales, v_new_scales=v_new_scales, shared_prefix_blocks=npre,
+        k_new_src=k_new_src, v_new_src=v_new_src)
 
 
 # --- the five workloads (sizes as the pages' settings suggest; see the design notes) ----------
