@@ -34,6 +34,9 @@ def lib():
         L.orc_paged_decode_attention.argtypes = [P, P, I, P, P, I, P, P, P, P,
                                                  I, I, I, I, I, I, I, D, I]
         L.orc_paged_decode_attention.restype = I
+        L.orc_paged_decode_attention_multi.argtypes = [P, P, I, P, P, I, P, P, P, P,
+                                                       I, I, I, I, I, I, I, I, D]
+        L.orc_paged_decode_attention_multi.restype = I
         L.orc_paged_decode_partials.argtypes = [P, P, P, P, P, I, P, P, I, P, P, P, P,
                                                 I, I, I, I, I, I, I, D, I, I]
         L.orc_paged_decode_partials.restype = I
@@ -155,6 +158,25 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale,
         _ptr(out), _ptr(q), _code(q), _ptr(kp), _ptr(vp), _code(kp),
         _ptr(_c(k_scales, np.float32)), _ptr(_c(v_scales, np.float32)), _ptr(bt), _ptr(cl),
         B, Hq, Hkv, D, BS, NB, bt.shape[1], float(scale), int(num_threads))
+    _check(rc)
+    return out
+
+
+def paged_decode_attention_multi(q, k_pool, v_pool, block_tables, context_lens, scale,
+                                 k_scales=None, v_scales=None):
+    """Multi-token decode: q [B, L, Hq, D]; query token l of sequence b sees its first
+    context_lens[b] - (L - 1 - l) tokens. Returns fp64 [B, L, Hq, D]."""
+    q = np.ascontiguousarray(q)
+    kp, vp = np.ascontiguousarray(k_pool), np.ascontiguousarray(v_pool)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, L, Hq, D = q.shape
+    NB, Hkv, BS, _ = kp.shape
+    out = np.zeros((B, L, Hq, D), dtype=np.float64)
+    rc = lib().orc_paged_decode_attention_multi(
+        _ptr(out), _ptr(q), _code(q), _ptr(kp), _ptr(vp), _code(kp),
+        _ptr(_c(k_scales, np.float32)), _ptr(_c(v_scales, np.float32)), _ptr(bt), _ptr(cl),
+        B, L, Hq, Hkv, D, BS, NB, bt.shape[1], float(scale))
     _check(rc)
     return out
 

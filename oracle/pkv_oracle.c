@@ -212,30 +212,30 @@ static int gather_row(const orc_problem* P, int b, int kvh, int t, int which_v, 
     return ORC_OK;
 }
 
-/* s_t = scale * sum_d q[d] * k_t[d] for t in [lo, hi). */
-static int scores(const orc_problem* P, int b, int h, int lo, int hi, double* s, double* row) {
+/* s_t = scale * sum_d q[d] * k_t[d] for t in [lo, hi); qrow is element index of q's first dim. */
+static int scores(const orc_problem* P, size_t qrow, int b, int h, int lo, int hi, double* s,
+                  double* row) {
     int kvh = h / (P->Hq / P->Hkv);
-    size_t qbase = ((size_t)b * P->Hq + h) * P->D;
     for (int t = lo; t < hi; ++t) {
         int rc = gather_row(P, b, kvh, t, 0, row);
         if (rc) return rc;
         double dot = 0.0;
-        for (int d = 0; d < P->D; ++d) dot += load_elem(P->q, qbase + d, P->q_dtype) * row[d];
+        for (int d = 0; d < P->D; ++d) dot += load_elem(P->q, qrow + d, P->q_dtype) * row[d];
         s[t - lo] = P->scale * dot;
     }
     return ORC_OK;
 }
 
-/* Softmax attention of one (b, h) pair over tokens [lo, hi) in the partial form of [ECHO2]:
- * m = max_t s_t, l = sum_t exp(s_t - m), acc = sum_t exp(s_t - m) v_t. Empty range: m = -inf,
- * l = 0, acc = 0. */
-static int partial(const orc_problem* P, int b, int h, int lo, int hi, double* m_out,
-                   double* l_out, double* acc, double* s, double* row) {
+/* Softmax attention of query vector q[qrow ..] (head h, K/V of sequence b's table) over tokens
+ * [lo, hi) in the partial form of [ECHO2]: m = max_t s_t, l = sum_t exp(s_t - m),
+ * acc = sum_t exp(s_t - m) v_t. Empty range: m = -inf, l = 0, acc = 0. */
+static int partial_q(const orc_problem* P, size_t qrow, int b, int h, int lo, int hi,
+                     double* m_out, double* l_out, double* acc, double* s, double* row) {
     for (int d = 0; d < P->D; ++d) acc[d] = 0.0;
     *m_out = -INFINITY;
     *l_out = 0.0;
     if (hi <= lo) return ORC_OK;
-    int rc = scores(P, b, h, lo, hi, s, row);
+    int rc = scores(P, qrow, b, h, lo, hi, s, row);
     if (rc) return rc;
     double m = s[0];
     for (int t = 1; t < hi - lo; ++t) if (s[t] > m) m = s[t];
@@ -251,6 +251,12 @@ static int partial(const orc_problem* P, int b, int h, int lo, int hi, double* m
     *m_out = m;
     *l_out = l;
     return ORC_OK;
+}
+
+/* The decode case: query row (b, h) of q [B][Hq][D]. */
+static int partial(const orc_problem* P, int b, int h, int lo, int hi, double* m_out,
+                   double* l_out, double* acc, double* s, double* row) {
+    return partial_q(P, ((size_t)b * P->Hq + h) * P->D, b, h, lo, hi, m_out, l_out, acc, s, row);
 }
 
 typedef struct {
@@ -319,6 +325,49 @@ int orc_paged_decode_attention(double* out, const void* q, int q_dtype, const vo
         for (int i = 0; i < num_threads; ++i) pthread_join(th[i], NULL);
     for (int i = 0; i < num_threads; ++i) if (jobs[i].status) rc = jobs[i].status;
     free(jobs); free(th);
+    return rc;
+}
+
+/* Multi-token decode ("AMD ATOM inference engine", section 4, decode scheduling: with MTP
+ * speculative decoding a decode step reserves num_new_tokens = mtp_k + 1 cache slots per
+ * sequence; the target model verifies all of them in one pass). Sequence b's L new tokens are
+ * its last L context positions; query token l (0 <= l < L) attends causally to positions
+ * t <= n_b - L + l, i.e. to the first n_b - (L - 1 - l) tokens. q and out are [B][L][Hq][D].
+ * n_b < L is a bad argument. Computed by the plain definition per (b, l, h). */
+int orc_paged_decode_attention_multi(double* out, const void* q, int q_dtype, const void* k_pool,
+                                     const void* v_pool, int kv_dtype, const float* k_scales,
+                                     const float* v_scales, const int32_t* block_tables,
+                                     const int32_t* context_lens, int B, int L, int Hq, int Hkv,
+                                     int D, int BS, int NB, int MBPS, double scale) {
+    if (L < 1) return ORC_BAD_ARG;
+    orc_problem P = {q, q_dtype, k_pool, v_pool, kv_dtype, k_scales, v_scales,
+                     block_tables, context_lens, B, Hq, Hkv, D, BS, NB, MBPS, scale};
+    int rc = check_problem(&P);
+    if (rc) return rc;
+    int maxn = 1;
+    for (int b = 0; b < B; ++b) {
+        if (context_lens[b] < L) return ORC_BAD_ARG;
+        if (context_lens[b] > maxn) maxn = context_lens[b];
+    }
+    double* s = (double*)malloc(sizeof(double) * (size_t)maxn);
+    double* row = (double*)malloc(sizeof(double) * (size_t)D);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!s || !row || !acc) { free(s); free(row); free(acc); return ORC_NO_MEMORY; }
+    /* query token l of sequence b: q row (b * L + l), sequence b's block table */
+    for (int b = 0; b < B && rc == ORC_OK; ++b) {
+        for (int l = 0; l < L && rc == ORC_OK; ++l) {
+            int n_l = context_lens[b] - (L - 1 - l);
+            for (int h = 0; h < Hq; ++h) {
+                size_t r = (size_t)(b * L + l) * Hq + h;
+                double m, lsum;
+                rc = partial_q(&P, r * D, b, h, 0, n_l, &m, &lsum, acc, s, row);
+                if (rc) break;
+                double* o = out + r * D;
+                for (int d = 0; d < D; ++d) o[d] = acc[d] / lsum;
+            }
+        }
+    }
+    free(s); free(row); free(acc);
     return rc;
 }
 

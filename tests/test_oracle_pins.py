@@ -337,3 +337,58 @@ def test_kv_write_quant_places_rows_like_the_copy_write(orc):
     assert np.array_equal(k2[2, :, 15], c[1]) and np.array_equal(ks2[2, :, 15], sc[1])
     assert np.array_equal(v2[1, :, 4], -c[0])
     assert np.count_nonzero(ks2) == 4
+
+
+# ---- multi-token decode (ATOM page, section 4: num_new_tokens = mtp_k + 1) ------------------------
+
+def test_multi_token_with_one_token_is_decode(orc):
+    w = W.make_config(2, B=3, ctx_lo=20, ctx_hi=200, seed=3)
+    m = W.make_multi_token(w, 1, seed=5)
+    a = orc.paged_decode_attention_multi(m.q, m.k_pool, m.v_pool, m.block_tables, m.context_lens, m.scale)
+    b = orc.paged_decode_attention(m.q[:, 0], m.k_pool, m.v_pool, m.block_tables, m.context_lens, m.scale)
+    assert np.array_equal(a[:, 0], b)
+
+
+def test_multi_token_is_causal_over_the_new_tokens(orc):
+    """Query token l sees exactly the first n - (L - 1 - l) tokens: changing the rows after that
+    leaves it unchanged, and token l equals a plain decode with that context length."""
+    L = 4
+    w = W.make_config(2, B=3, ctx_lo=30, ctx_hi=90, seed=9)
+    m = W.make_multi_token(w, L, seed=2)
+    base = orc.paged_decode_attention_multi(m.q, m.k_pool, m.v_pool, m.block_tables, m.context_lens, m.scale)
+    for l in range(L):
+        cut = m.context_lens - (L - 1 - l)
+        ref = orc.paged_decode_attention(m.q[:, l], m.k_pool, m.v_pool, m.block_tables, cut, m.scale)
+        assert np.array_equal(base[:, l], ref)
+    # perturb the last new token of sequence 0: only its own query (l = L - 1) may change
+    kp = m.k_pool.copy()
+    t = int(m.context_lens[0]) - 1
+    kp[m.block_tables[0, t // 16], :, t % 16, :] ^= np.uint16(0x4000)
+    pert = orc.paged_decode_attention_multi(m.q, kp, m.v_pool, m.block_tables, m.context_lens, m.scale)
+    assert np.array_equal(pert[0, :L - 1], base[0, :L - 1]) and not np.array_equal(pert[0, L - 1], base[0, L - 1])
+    assert np.array_equal(pert[1:], base[1:])
+
+
+def test_multi_token_matches_library_masked_attention(orc):
+    """Against torch scaled_dot_product_attention (fp64, CPU) with an explicit causal mask."""
+    torch = pytest.importorskip("torch")
+    L, n, D, Hkv, g = 3, 40, 64, 2, 2
+    rng = np.random.default_rng(12)
+    K = rng.standard_normal((2, n, Hkv, D)).astype(np.float32)
+    V = rng.standard_normal((2, n, Hkv, D)).astype(np.float32)
+    q = rng.standard_normal((2, L, Hkv * g, D)).astype(np.float32)
+    kp, vp, bt, cl = _pool_from_contiguous(K, V, perm_seed=7)
+    out = orc.paged_decode_attention_multi(q, kp, vp, bt, cl, 0.125)
+    tq = torch.from_numpy(q.astype(np.float64)).permute(0, 2, 1, 3)                  # [B, Hq, L, D]
+    tk = torch.from_numpy(K.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(g, 1)
+    tv = torch.from_numpy(V.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(g, 1)
+    mask = torch.tensor([[t <= n - L + l for t in range(n)] for l in range(L)])
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.125)
+    np.testing.assert_allclose(out, ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+
+
+def test_multi_token_needs_context_for_every_new_token(orc):
+    w = W.make_config(2, B=2, ctx_lo=3, ctx_hi=3, seed=1)
+    q = np.zeros((2, 4, w.Hq, w.D), np.uint16)
+    with pytest.raises(RuntimeError):
+        orc.paged_decode_attention_multi(q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)

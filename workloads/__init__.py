@@ -307,3 +307,32 @@ def kv_bytes(w: DecodeWorkload, unique: bool = True) -> int:
     written = int((w.slot_mapping >= 0).sum())
     wr = written * per_tok * 2 + 8 * w.T  # read new rows + write pool rows; slot ids
     return kv + qo + tables + wr
+
+
+def make_multi_token(w: DecodeWorkload, L: int, seed: int) -> DecodeWorkload:
+    """A multi-token decode step built on workload w: every sequence's last L context positions
+    are new tokens (written this step, verified together, as MTP speculative decoding does with
+    mtp_k + 1 tokens). q becomes [B, L, Hq, D]; slot_mapping / k_new / v_new cover the B * L
+    new tokens, sequence-major. Needs context_lens >= L."""
+    assert L >= 1 and (w.context_lens >= L).all()
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B, Hkv, D = w.B, w.Hkv, w.D
+    q = _draw(rng, (B, L, w.Hq, D), w.q_dtype)
+    slots = np.empty(B * L, dtype=np.int64)
+    for b in range(B):
+        n = int(w.context_lens[b])
+        for l in range(L):
+            t = n - L + l
+            slots[b * L + l] = int(w.block_tables[b, t // w.BS]) * w.BS + t % w.BS
+    extra = {}
+    if w.kv_dtype == "i8":
+        ks = f32_to_bf16_bits(rng.standard_normal(size=(B * L, Hkv, D), dtype=np.float32))
+        vs = f32_to_bf16_bits(rng.standard_normal(size=(B * L, Hkv, D), dtype=np.float32))
+        kn, kns = quantize_int8_rows(bf16_bits_to_f32(ks))
+        vn, vns = quantize_int8_rows(bf16_bits_to_f32(vs))
+        extra = dict(k_new_src=ks, v_new_src=vs, k_new_scales=kns, v_new_scales=vns)
+    else:
+        kn, _ = _draw_kv(rng, (B * L, Hkv, D), w.kv_dtype)
+        vn, _ = _draw_kv(rng, (B * L, Hkv, D), w.kv_dtype)
+    return DecodeWorkload(**{**w.__dict__, "name": f"{w.name}_mtp{L}", "q": q,
+                             "slot_mapping": slots, "k_new": kn, "v_new": vn, **extra})
