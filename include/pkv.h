@@ -109,6 +109,31 @@ pkv_status pkv_kv_cache_write_int8(const void* k_new, const void* v_new, int8_t*
                                    pkv_dtype src_dtype, int32_t* status, void* stream);
 
 /*
+ * Multi-token decode: L = num_query_tokens new tokens per sequence, verified in one pass, as MTP
+ * speculative decoding does ("AMD ATOM inference engine", section 4: a decode step reserves
+ * num_new_tokens = mtp_k + 1 cache slots per sequence). The L new tokens are the last L of
+ * context_lens[b] (already written with pkv_kv_cache_write[_int8]); query token l attends
+ * causally to the first context_lens[b] - (L - 1 - l) tokens:
+ *     out[b][l][h][:] = sum_{t < n_b - L + 1 + l} softmax_t(scale * <q[b][l][h], K_t>) V_t
+ * q and out are [num_seqs][L][num_q_heads][head_dim]. kv_dtype PKV_F32 / PKV_BF16: q, out and the
+ * pools share it and the scale pointers must be NULL; PKV_I8: int8 pools with fp32 scales
+ * (as pkv_paged_decode_attention_int8), q and out bf16. Every (sequence, query token) row is
+ * split like a decode row, so the workspace is pkv_decode_workspace_bytes(num_seqs * L, ...).
+ * num_query_tokens = 1 is pkv_paged_decode_attention(_int8). A context_lens[b] < L is a caller
+ * error: it is flagged (PKV_FLAG_BAD_CONTEXT) and the rows with no visible token are zeros.
+ */
+pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void* k_pool,
+                                            const void* v_pool, const float* k_scales,
+                                            const float* v_scales, const int32_t* block_tables,
+                                            const int32_t* context_lens, int num_seqs,
+                                            int num_query_tokens, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int num_blocks, int max_blocks_per_seq,
+                                            int max_context_len, float scale, pkv_dtype kv_dtype,
+                                            int split_chunk_tokens, void* workspace,
+                                            size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * Bytes of device workspace pkv_paged_decode_attention[_int8] needs for the split-K partial
  * states (m, l, acc) of a batch: the split count per sequence follows "EchoLLMServing
  * inference framework notes", section 2 (split_num = max(1, context_len // chunk)), so the

@@ -30,6 +30,8 @@ SIGNATURES = {
                                     _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_decode_attention_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                          _I, _I, _F, _I, _P, _SZ, _P, _P], _I),
+    "pkv_paged_decode_attention_multi": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                          _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_decode_attention_static_ws": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                               _I, _F, _I, _I, _P, _P], _I),
 }
@@ -160,6 +162,22 @@ def paged_decode_attention_int8(out, q, k_pool, v_pool, k_scales, v_scales, bloc
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream))
     _check(rc, "paged_decode_attention_int8")
+
+
+def paged_decode_attention_multi(out, q, k_pool, v_pool, block_tables, context_lens,
+                                 max_context_len, scale, k_scales=None, v_scales=None,
+                                 split_chunk_tokens=0, workspace=None, status=None, stream=None):
+    """pkv_paged_decode_attention_multi: q/out [B, L, Hq, D]; query token l of sequence b sees its
+    first context_lens[b] - (L - 1 - l) tokens. INT8 pools take k_scales / v_scales."""
+    B, L, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_decode_attention_multi(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_tables), _ptr(context_lens), B, L, Hq, Hkv, D, BS, NB, block_tables.shape[1],
+        int(max_context_len), float(scale), _kv_code(k_pool), int(split_chunk_tokens),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "paged_decode_attention_multi")
 
 
 def paged_decode_attention_static_ws(out, q, k_pool, v_pool, block_tables, context_lens,

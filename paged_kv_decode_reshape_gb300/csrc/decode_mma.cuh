@@ -171,21 +171,19 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.head_chunks;
     const int hc = blockIdx.y - kvh * p.head_chunks;
-    const int b = blockIdx.z;
+    const int zb = blockIdx.z;          // row of q / out: query token lq of sequence b
+    const int b = zb / p.L, lq = zb - b * p.L;
     const int h0 = kvh * p.G + hc * kMmaHeads;
     const int nh = p.G - hc * kMmaHeads < kMmaHeads ? p.G - hc * kMmaHeads : kMmaHeads;
 
     grid_dependency_wait();  // inputs (new K/V rows, tables) may come from the previous kernel
 
-    int n = p.context_lens[b];
-    const int ncap = p.MBPS * kBlockSize;
-    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0;
-    if (n < 0 || n > ncap) {
-        if (reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
-        n = n < 0 ? 0 : ncap;
-    } else if (n > p.max_context_len && reporter) {
-        flag(p.status, PKV_FLAG_LONG_CONTEXT);
-    }
+    const int stored = p.context_lens[b];
+    bool bad;
+    const int n = query_context_len(stored, p.L, lq, p.MBPS * kBlockSize, &bad);
+    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && lq == 0;
+    if (bad && reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
+    else if (stored > p.max_context_len && reporter) flag(p.status, PKV_FLAG_LONG_CONTEXT);
     int per;
     const int ns = split_count(n, p.chunk, p.max_splits, &per);
     if (split >= ns) return;
@@ -269,7 +267,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
         float qsum = 0.f;  // INT8: sum of this lane's fp16 q' values of head r (as the MMA sees them)
         {
             const bool hv = r < nh;
-            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + h0 + (hv ? r : 0)) * kMmaD;
+            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)zb * p.Hq + h0 + (hv ? r : 0)) * kMmaD;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 if constexpr (kI8) {
@@ -534,7 +532,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                 A = fmaf(wt, sm_o[(w * kMmaHeads + hh) * kMmaD + d], A);
             }
         }
-        const size_t qh = (size_t)b * p.Hq + h0 + hh;
+        const size_t qh = (size_t)zb * p.Hq + h0 + hh;
         if (ns == 1) {
             store_out<__nv_bfloat16>(static_cast<__nv_bfloat16*>(p.out) + qh * kMmaD + d, L > 0.f ? A / L : 0.f);
         } else {

@@ -123,22 +123,20 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.head_chunks;
     const int hc = blockIdx.y - kvh * p.head_chunks;
-    const int b = blockIdx.z;
+    const int zb = blockIdx.z;          // row of q / out: query token lq of sequence b
+    const int b = zb / p.L, lq = zb - b * p.L;
     const int h0 = kvh * p.G + hc * HG;          // first query head of this CTA
     const int nh = cmin(HG, p.G - hc * HG);      // query heads this CTA produces
 
     grid_dependency_wait();  // inputs (new K/V rows, tables) may come from the previous kernel
 
-    // context length, clamped to what the block table can address
-    int n = p.context_lens[b];
-    const int ncap = p.MBPS * kBlockSize;
-    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0;
-    if (n < 0 || n > ncap) {
-        if (reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
-        n = n < 0 ? 0 : ncap;
-    } else if (n > p.max_context_len && reporter) {
-        flag(p.status, PKV_FLAG_LONG_CONTEXT);
-    }
+    // context length of this query token, clamped to what the block table can address
+    const int stored = p.context_lens[b];
+    bool bad;
+    const int n = query_context_len(stored, p.L, lq, p.MBPS * kBlockSize, &bad);
+    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && lq == 0;
+    if (bad && reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
+    else if (stored > p.max_context_len && reporter) flag(p.status, PKV_FLAG_LONG_CONTEXT);
     int per;
     const int ns = split_count(n, p.chunk, p.max_splits, &per);
     if (split >= ns) return;
@@ -155,7 +153,7 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh) {
         if (hh < nh) {
-            const QT* qp = static_cast<const QT*>(p.q) + ((size_t)b * p.Hq + h0 + hh) * D + slice * 8;
+            const QT* qp = static_cast<const QT*>(p.q) + ((size_t)zb * p.Hq + h0 + hh) * D + slice * 8;
             gload8_f32<QT>(qp, qf[hh]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[hh][e] *= p.scale_log2;
@@ -343,7 +341,7 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
                 A = fmaf(w, red_acc[(g * HG + hh) * D + d], A);
             }
         }
-        const size_t qh = (size_t)b * p.Hq + h0 + hh;
+        const size_t qh = (size_t)zb * p.Hq + h0 + hh;
         if (ns == 1) {
             store_out<QT>(static_cast<QT*>(p.out) + qh * D + d, L > 0.f ? A / L : 0.f);
         } else {
@@ -365,7 +363,7 @@ cudaError_t launch_split_t(const SplitParams& p, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.B), dim3(G::NT), G::SMEM, s, p);
+    return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.B * p.L), dim3(G::NT), G::SMEM, s, p);
 }
 
 template <typename KV, typename QT>

@@ -53,7 +53,7 @@ struct Decode {
     void* out; const void* q; const void* k_pool; const void* v_pool;
     const float* k_scales; const float* v_scales;
     const int32_t* block_tables; const int32_t* context_lens;
-    int B, Hq, Hkv, D, BS, NB, MBPS, max_ctx;
+    int B, L, Hq, Hkv, D, BS, NB, MBPS, max_ctx;  // L: query tokens per sequence
     float scale;
     pkv_dtype q_dtype, kv_dtype;
     int chunk_req;
@@ -63,7 +63,7 @@ struct Decode {
 };
 
 pkv_status run_decode(const Decode& a) {
-    if (a.B < 0 || a.Hq <= 0 || a.Hkv <= 0 || a.D <= 0 || a.NB <= 0 || a.MBPS <= 0)
+    if (a.B < 0 || a.L < 1 || a.Hq <= 0 || a.Hkv <= 0 || a.D <= 0 || a.NB <= 0 || a.MBPS <= 0)
         return PKV_ERR_INVALID_ARG;
     if (a.Hq % a.Hkv != 0) return PKV_ERR_INVALID_ARG;
     if (a.BS != kBlockSize || (a.D != 64 && a.D != 128)) return PKV_ERR_UNSUPPORTED;
@@ -79,7 +79,8 @@ pkv_status run_decode(const Decode& a) {
                             (const void*)a.v_scales})
         if (ptr && !aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
     if (!aligned(a.block_tables, 4) || !aligned(a.context_lens, 4)) return PKV_ERR_INVALID_ARG;
-    if (a.B > 65535) return PKV_ERR_UNSUPPORTED;  // grid.z
+    const int rows = a.B * a.L;  // (sequence, query token) rows of q and out
+    if ((long long)a.B * a.L > 65535) return PKV_ERR_UNSUPPORTED;  // grid.z
     const int g = a.Hq / a.Hkv;
     // head_dim 128 bf16 / INT8 pools run on the tensor-core kernel (8 heads per CTA); fp32 and
     // head_dim 64 on the CUDA-core kernel
@@ -89,10 +90,10 @@ pkv_status run_decode(const Decode& a) {
     if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
-    const int chunk = choose_chunk(a.B, a.Hkv, a.max_ctx, a.chunk_req);
+    const int chunk = choose_chunk(rows, a.Hkv, a.max_ctx, a.chunk_req);
     const int S = split_extent(a.max_ctx, chunk);
     if (S > kMaxSplits) return PKV_ERR_UNSUPPORTED;
-    const size_t need = workspace_bytes_for(a.B, a.Hq, a.D, S);
+    const size_t need = workspace_bytes_for(rows, a.Hq, a.D, S);
     if (need > 0) {
         if (!a.ws || a.ws_bytes < need) return PKV_ERR_WORKSPACE;
         if (!aligned(a.ws, 256)) return PKV_ERR_INVALID_ARG;
@@ -100,7 +101,7 @@ pkv_status run_decode(const Decode& a) {
 
     // out must not alias an input or the workspace
     const size_t qe = elem_bytes(a.q_dtype), ke = elem_bytes(a.kv_dtype);
-    const size_t out_b = (size_t)a.B * a.Hq * a.D * qe;
+    const size_t out_b = (size_t)rows * a.Hq * a.D * qe;
     const size_t pool_b = (size_t)a.NB * a.Hkv * kBlockSize * a.D * ke;
     const size_t sc_b = i8 ? (size_t)a.NB * a.Hkv * kBlockSize * 4 : 0;
     if (overlap(a.out, out_b, a.q, out_b) || overlap(a.out, out_b, a.k_pool, pool_b) ||
@@ -116,9 +117,9 @@ pkv_status run_decode(const Decode& a) {
     p.k_scales = a.k_scales; p.v_scales = a.v_scales;
     p.block_tables = a.block_tables; p.context_lens = a.context_lens;
     p.ws_acc = need ? static_cast<float*>(a.ws) : nullptr;
-    p.ws_ml = need ? static_cast<float*>(a.ws) + (size_t)a.B * a.Hq * S * a.D : nullptr;
+    p.ws_ml = need ? static_cast<float*>(a.ws) + (size_t)rows * a.Hq * S * a.D : nullptr;
     p.status = a.status;
-    p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = g; p.NB = a.NB; p.MBPS = a.MBPS;
+    p.B = a.B; p.L = a.L; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = g; p.NB = a.NB; p.MBPS = a.MBPS;
     p.chunk = chunk; p.max_splits = S; p.head_chunks = head_chunks;
     p.max_context_len = a.max_ctx;
     p.scale_log2 = a.scale * kLog2e;
@@ -138,7 +139,7 @@ pkv_status run_decode(const Decode& a) {
     if (S > 1) {
         MergeParams m{};
         m.out = a.out; m.ws_acc = p.ws_acc; m.ws_ml = p.ws_ml; m.context_lens = a.context_lens;
-        m.B = a.B; m.Hq = a.Hq; m.MBPS = a.MBPS; m.chunk = chunk; m.max_splits = S;
+        m.B = a.B; m.L = a.L; m.Hq = a.Hq; m.MBPS = a.MBPS; m.chunk = chunk; m.max_splits = S;
         if (launch_merge(m, a.q_dtype, a.D, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;
@@ -261,7 +262,7 @@ pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_po
                                       size_t workspace_bytes, int32_t* status, void* stream) {
     if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
     Decode a{out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens,
-             num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+             num_seqs, 1, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
              max_blocks_per_seq, max_context_len, scale, dtype, dtype, split_chunk_tokens,
              workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
     return run_decode(a);
@@ -278,9 +279,30 @@ pkv_status pkv_paged_decode_attention_int8(void* out, const void* q, const int8_
                                            size_t workspace_bytes, int32_t* status,
                                            void* stream) {
     Decode a{out, q, k_pool, v_pool, k_scales, v_scales, block_tables, context_lens,
-             num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+             num_seqs, 1, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
              max_blocks_per_seq, max_context_len, scale, PKV_BF16, PKV_I8, split_chunk_tokens,
              workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
+    return run_decode(a);
+}
+
+pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void* k_pool,
+                                            const void* v_pool, const float* k_scales,
+                                            const float* v_scales, const int32_t* block_tables,
+                                            const int32_t* context_lens, int num_seqs,
+                                            int num_query_tokens, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int num_blocks, int max_blocks_per_seq,
+                                            int max_context_len, float scale, pkv_dtype kv_dtype,
+                                            int split_chunk_tokens, void* workspace,
+                                            size_t workspace_bytes, int32_t* status,
+                                            void* stream) {
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8) return PKV_ERR_INVALID_ARG;
+    if (kv_dtype != PKV_I8 && (k_scales || v_scales)) return PKV_ERR_INVALID_ARG;
+    const pkv_dtype q_dtype = kv_dtype == PKV_I8 ? PKV_BF16 : kv_dtype;
+    Decode a{out, q, k_pool, v_pool, k_scales, v_scales, block_tables, context_lens,
+             num_seqs, num_query_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+             num_blocks, max_blocks_per_seq, max_context_len, scale, q_dtype, kv_dtype,
+             split_chunk_tokens, workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
     return run_decode(a);
 }
 

@@ -33,6 +33,17 @@ __host__ __device__ __forceinline__ int split_count(int n, int chunk, int max_sp
     return (n + p - 1) / p;
 }
 
+// Context length seen by query token lq (0 <= lq < L) of a sequence whose stored length is n
+// (multi-token decode: the L new tokens are the last L positions and attend causally, so token
+// lq sees the first n - (L - 1 - lq)). n is first clamped to [0, ncap]; *bad is set when n was
+// outside that range or shorter than L.
+__host__ __device__ __forceinline__ int query_context_len(int n, int L, int lq, int ncap, bool* bad) {
+    *bad = n < L || n > ncap;
+    n = n < 0 ? 0 : (n > ncap ? ncap : n);
+    n -= L - 1 - lq;
+    return n < 0 ? 0 : n;
+}
+
 struct SplitParams {
     void* out;                  // [B][Hq][D], element type of q
     const void* q;              // [B][Hq][D]
@@ -46,6 +57,7 @@ struct SplitParams {
     float* ws_ml;               // [B][Hq][S][2]  (m in log2 units, l)
     int32_t* status;
     int B, Hq, Hkv, G, NB, MBPS;
+    int L;                      // query tokens per sequence (1: decode); grid.z = B * L
     int chunk, max_splits;      // S = max_splits
     int head_chunks;            // CTAs per kv head along grid.y (ceil(G / heads per CTA))
     int max_context_len;
@@ -57,7 +69,7 @@ struct MergeParams {
     const float* ws_acc;
     const float* ws_ml;
     const int32_t* context_lens;
-    int B, Hq, MBPS, chunk, max_splits;
+    int B, Hq, MBPS, L, chunk, max_splits;  // B: sequences; rows are (sequence, query token)
 };
 
 struct WriteParams {

@@ -35,11 +35,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
 
     const int lane = threadIdx.x & 31;
     const int pair = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-    if (pair >= p.B * p.Hq) return;
-    const int b = pair / p.Hq;
-    int n = p.context_lens[b];
-    const int ncap = p.MBPS * kBlockSize;
-    n = n < 0 ? 0 : (n > ncap ? ncap : n);
+    if (pair >= p.B * p.L * p.Hq) return;
+    const int zb = pair / p.Hq;  // (sequence, query token) row
+    const int b = zb / p.L;
+    bool bad;
+    const int n = query_context_len(p.context_lens[b], p.L, zb - b * p.L, p.MBPS * kBlockSize, &bad);
     int per;
     const int ns = split_count(n, p.chunk, p.max_splits, &per);
     if (ns <= 1) return;
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
 
 template <typename OT, int D>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
-    const int pairs = p.B * p.Hq;
+    const int pairs = p.B * p.L * p.Hq;
     return launch_pdl(merge_kernel<OT, D>, dim3((pairs + kMergeWarps - 1) / kMergeWarps),
                       dim3(32 * kMergeWarps), 0, s, p);
 }

@@ -163,3 +163,24 @@ def test_quant_write_argument_checks(pkv, kw, expect):
                                           a["sm"], a["T"], a["Hkv"], a["D"], a["BS"], a["NB"],
                                           a["src"], None, None)
     assert rc == expect
+
+
+@fake_ptrs
+@pytest.mark.parametrize("kw,expect", [
+    (dict(L=0), P.ERR_INVALID_ARG),
+    (dict(ks=FAKE[8]), P.ERR_INVALID_ARG),                             # scales with bf16 pools
+    (dict(dtype=P.I8), P.ERR_INVALID_ARG),                             # INT8 without scales
+    (dict(B=20000, L=4), P.ERR_UNSUPPORTED),                           # B * L rows over grid.z
+    (dict(maxc=128, chunk=16), P.ERR_WORKSPACE),
+    (dict(B=0, out=None, q=None), P.OK),
+])
+def test_multi_token_argument_checks(pkv, kw, expect):
+    a = dict(out=FAKE[0], q=FAKE[1], k=FAKE[2], v=FAKE[3], ks=None, vs=None, bt=FAKE[4], cl=FAKE[5],
+             B=2, L=3, Hq=8, Hkv=2, D=128, BS=16, NB=64, MBPS=8, maxc=100, scale=0.1,
+             dtype=P.BF16, chunk=0, ws=None, wsb=0)
+    a.update(kw)
+    rc = P.load().pkv_paged_decode_attention_multi(
+        a["out"], a["q"], a["k"], a["v"], a["ks"], a["vs"], a["bt"], a["cl"], a["B"], a["L"],
+        a["Hq"], a["Hkv"], a["D"], a["BS"], a["NB"], a["MBPS"], a["maxc"], a["scale"], a["dtype"],
+        a["chunk"], a["ws"], a["wsb"], None, None)
+    assert rc == expect
