@@ -53,7 +53,8 @@ typedef enum {
     PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misalignment, aliasing */
     PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim not 64/128, block_size not 16 */
     PKV_ERR_WORKSPACE = 3,     /* workspace smaller than pkv_decode_workspace_bytes() */
-    PKV_ERR_CUDA = 4           /* the CUDA runtime rejected a launch */
+    PKV_ERR_CUDA = 4,          /* the CUDA runtime rejected a launch */
+    PKV_ERR_NO_BLOCKS = 5      /* block manager: not enough free blocks (nothing was changed) */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
@@ -228,6 +229,58 @@ pkv_status pkv_paged_decode_attention_static_ws(void* out, const void* q, const 
                                                 float scale, pkv_dtype dtype,
                                                 int split_chunk_tokens, int32_t* status,
                                                 void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Host block manager: the step before the decode path, producing block_tables, context_lens and
+ * slot_mapping. "AMD ATOM inference engine", section 5.1 (BlockManager: fixed 16-token blocks, a
+ * block_table per sequence, Block{block_id, ref_count, hash = -1, token_ids}, reset() sets
+ * ref_count to 1) and section 5.2 (prefix caching with xxhash64 chained over blocks);
+ * "LLM Primer VI, Chapter 8", section 8.1 (blocks shared by reference count).
+ *
+ * A pkv_block_manager is host memory owned by the caller (create / destroy); no device memory and
+ * no CUDA call is involved, and it is not thread-safe. Sequences are named by caller-chosen int64
+ * ids. Free blocks are handed out first-in first-out, initially 0, 1, 2, ...; freed blocks go to
+ * the back of the free list, tail block first. With prefix caching on, every full block carries
+ * the chained hash of its tokens; a prompt block whose hash (and tokens) match a cached block
+ * shares it (ref_count + 1) instead of taking a free block, even when that block sits freed but
+ * not yet reused in the free list. Partial blocks are never shared.
+ * --------------------------------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager over num_blocks blocks of block_size tokens; NULL on bad arguments / no memory. */
+pkv_block_manager* pkv_bm_create(int num_blocks, int block_size, int enable_prefix_cache);
+void pkv_bm_destroy(pkv_block_manager* bm);
+int pkv_bm_num_free_blocks(const pkv_block_manager* bm);
+int pkv_bm_ref_count(const pkv_block_manager* bm, int block_id);  /* -1 for a bad id */
+
+/* xxhash64 (the published XXH64 algorithm) of len bytes. */
+uint64_t pkv_xxh64(const void* data, size_t len, uint64_t seed);
+/* Chained block hash of section 5.2: XXH64, seed 0, over prefix_hash as 8 little-endian bytes
+ * (omitted when prefix_hash == -1) followed by the token ids as int64 little-endian. */
+uint64_t pkv_block_hash(const int64_t* token_ids, int num_tokens, int64_t prefix_hash);
+
+/* Prefill: enough free blocks for num_tokens (cache hits not counted)? */
+int pkv_bm_can_allocate(const pkv_block_manager* bm, int num_tokens);
+/* Prefill: give a new sequence blocks for its prompt, sharing cached full blocks of the same
+ * chained prefix; *num_cached_tokens (optional) gets the tokens found in the cache.
+ * PKV_ERR_NO_BLOCKS if pkv_bm_can_allocate is false; INVALID_ARG for a known seq_id. */
+pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq_id, const int64_t* token_ids,
+                           int num_tokens, int* num_cached_tokens);
+/* Decode: room for num_new_tokens more tokens (scheduler's can_append)? */
+int pkv_bm_can_append(const pkv_block_manager* bm, int64_t seq_id, int num_new_tokens);
+/* Decode (may_append): add the tokens, taking a new block at each block boundary; slot_mapping
+ * (optional, [num_new_tokens]) receives each token's slot block_id * block_size + offset, ready
+ * for pkv_kv_cache_write. A block that becomes full gets its chained hash. */
+pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int64_t* new_token_ids,
+                         int num_new_tokens, int64_t* slot_mapping);
+/* Finish or preempt a sequence: its blocks lose a reference; unreferenced ones become free. */
+pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
+int pkv_bm_context_len(const pkv_block_manager* bm, int64_t seq_id);  /* -1 if unknown */
+/* The decode inputs of a batch: block_tables [num_seqs][max_blocks_per_seq] (unused entries -1)
+ * and context_lens [num_seqs] in host memory, for upload to the device. */
+pkv_status pkv_bm_batch_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int num_seqs,
+                               int max_blocks_per_seq, int32_t* block_tables,
+                               int32_t* context_lens);
 
 #ifdef __cplusplus
 }

@@ -194,3 +194,105 @@ def paged_decode_attention_static_ws(out, q, k_pool, v_pool, block_tables, conte
         B, Hq, Hkv, D, BS, NB, block_tables.shape[1], int(max_context_len), float(scale),
         _kv_code(q), int(split_chunk_tokens), _ptr(status), _stream(stream))
     _check(rc, "paged_decode_attention_static_ws")
+
+
+# ---- host block manager (ctypes marshalling of the pkv_bm_* calls) ---------------------------
+ERR_NO_BLOCKS = 5
+_BM_SIGNATURES = {
+    "pkv_bm_create": ([_I, _I, _I], _P),
+    "pkv_bm_destroy": ([_P], None),
+    "pkv_bm_num_free_blocks": ([_P], _I),
+    "pkv_bm_ref_count": ([_P, _I], _I),
+    "pkv_xxh64": ([_P, _SZ, ctypes.c_uint64], ctypes.c_uint64),
+    "pkv_block_hash": ([_P, _I, ctypes.c_int64], ctypes.c_uint64),
+    "pkv_bm_can_allocate": ([_P, _I], _I),
+    "pkv_bm_allocate": ([_P, ctypes.c_int64, _P, _I, _P], _I),
+    "pkv_bm_can_append": ([_P, ctypes.c_int64, _I], _I),
+    "pkv_bm_append": ([_P, ctypes.c_int64, _P, _I, _P], _I),
+    "pkv_bm_free": ([_P, ctypes.c_int64], _I),
+    "pkv_bm_context_len": ([_P, ctypes.c_int64], _I),
+    "pkv_bm_batch_tables": ([_P, _P, _I, _I, _P, _P], _I),
+}
+SIGNATURES.update(_BM_SIGNATURES)
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def xxh64(data: bytes, seed: int = 0) -> int:
+    buf = ctypes.create_string_buffer(bytes(data), len(data))
+    return int(load().pkv_xxh64(buf, len(data), seed))
+
+
+def block_hash(token_ids, prefix_hash: int = -1) -> int:
+    import numpy as np
+    t = np.ascontiguousarray(token_ids, dtype=np.int64)
+    p = prefix_hash if prefix_hash < 2**63 else prefix_hash - 2**64  # int64 view of the uint64
+    return int(load().pkv_block_hash(_np_ptr(t), t.size, p))
+
+
+class BlockManager:
+    """Host block manager (include/pkv.h, pkv_bm_*): allocate prompts with prefix sharing, append
+    decode tokens (returning their slots), free sequences, and emit batch block tables."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE, prefix_cache: bool = True):
+        self._h = load().pkv_bm_create(num_blocks, block_size, int(prefix_cache))
+        if not self._h:
+            raise PkvError(ERR_INVALID_ARG, "pkv_bm_create")
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            load().pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free_blocks(self) -> int:
+        return load().pkv_bm_num_free_blocks(self._h)
+
+    def ref_count(self, block_id: int) -> int:
+        return load().pkv_bm_ref_count(self._h, block_id)
+
+    def can_allocate(self, num_tokens: int) -> bool:
+        return bool(load().pkv_bm_can_allocate(self._h, num_tokens))
+
+    def allocate(self, seq_id: int, token_ids) -> int:
+        import numpy as np
+        t = np.ascontiguousarray(token_ids, dtype=np.int64)
+        cached = ctypes.c_int(0)
+        _check(load().pkv_bm_allocate(self._h, seq_id, _np_ptr(t), t.size, ctypes.byref(cached)),
+               "pkv_bm_allocate")
+        return cached.value
+
+    def can_append(self, seq_id: int, num_new_tokens: int) -> bool:
+        return bool(load().pkv_bm_can_append(self._h, seq_id, num_new_tokens))
+
+    def append(self, seq_id: int, token_ids):
+        import numpy as np
+        t = np.ascontiguousarray(token_ids, dtype=np.int64)
+        slots = np.zeros(t.size, dtype=np.int64)
+        _check(load().pkv_bm_append(self._h, seq_id, _np_ptr(t), t.size, _np_ptr(slots)),
+               "pkv_bm_append")
+        return slots
+
+    def free(self, seq_id: int):
+        _check(load().pkv_bm_free(self._h, seq_id), "pkv_bm_free")
+
+    def context_len(self, seq_id: int) -> int:
+        return load().pkv_bm_context_len(self._h, seq_id)
+
+    def batch_tables(self, seq_ids, max_blocks_per_seq: int):
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        bt = np.zeros((ids.size, max_blocks_per_seq), dtype=np.int32)
+        cl = np.zeros(ids.size, dtype=np.int32)
+        _check(load().pkv_bm_batch_tables(self._h, _np_ptr(ids), ids.size, max_blocks_per_seq,
+                                          _np_ptr(bt), _np_ptr(cl)), "pkv_bm_batch_tables")
+        return bt, cl

@@ -15,7 +15,7 @@ BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libpkv.so")
 
 SOURCES = ["pkv_api.cu", "kv_write.cu", "decode_f32.cu", "decode_bf16.cu", "decode_i8.cu",
-           "decode_mma.cu", "splitk_merge.cu", "decode_static_ws.cu"]
+           "decode_mma.cu", "splitk_merge.cu", "decode_static_ws.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE]
@@ -49,7 +49,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(BUILD, src.replace(".", "_") + ".o")
         tune = os.environ.get("PKV_NVCC_FLAGS", "").split()  # build-time tuning defines
         cmd = [nvcc(), *ARCH, *FLAGS, *tune, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -156,6 +156,7 @@ const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
         case PKV_ERR_WORKSPACE: return "workspace too small";
         case PKV_ERR_CUDA: return "CUDA launch failed";
+        case PKV_ERR_NO_BLOCKS: return "not enough free KV blocks";
     }
     return "unknown status";
 }
