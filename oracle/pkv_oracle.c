@@ -371,6 +371,48 @@ int orc_paged_decode_attention_multi(double* out, const void* q, int q_dtype, co
     return rc;
 }
 
+/* Paged prefill (chunked prefill; "EchoLLMServing inference framework notes", section 2
+ * FlashAttention for prefill, section 3 chunked prefill and mixed batches): sequence b has
+ * L_b = query_start[b + 1] - query_start[b] query tokens, the last L_b of its context n_b, at
+ * rows query_start[b] .. of q / out [total][Hq][D]. Row i of sequence b attends causally to the
+ * first n_b - (L_b - 1 - i) tokens -- the multi-token rule with a per-sequence L. */
+int orc_paged_prefill_attention(double* out, const void* q, int q_dtype, const void* k_pool,
+                                const void* v_pool, int kv_dtype, const int32_t* block_tables,
+                                const int32_t* context_lens, const int32_t* query_start, int B,
+                                int Hq, int Hkv, int D, int BS, int NB, int MBPS, double scale) {
+    orc_problem P = {q, q_dtype, k_pool, v_pool, kv_dtype, NULL, NULL,
+                     block_tables, context_lens, B, Hq, Hkv, D, BS, NB, MBPS, scale};
+    int rc = check_problem(&P);
+    if (rc) return rc;
+    if (kv_dtype == ORC_I8) return ORC_BAD_ARG;
+    int maxn = 1;
+    for (int b = 0; b < B; ++b) {
+        int L = query_start[b + 1] - query_start[b];
+        if (L < 0 || context_lens[b] < L) return ORC_BAD_ARG;
+        if (context_lens[b] > maxn) maxn = context_lens[b];
+    }
+    double* s = (double*)malloc(sizeof(double) * (size_t)maxn);
+    double* row = (double*)malloc(sizeof(double) * (size_t)D);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!s || !row || !acc) { free(s); free(row); free(acc); return ORC_NO_MEMORY; }
+    for (int b = 0; b < B && rc == ORC_OK; ++b) {
+        int L = query_start[b + 1] - query_start[b];
+        for (int i = 0; i < L && rc == ORC_OK; ++i) {
+            int n_i = context_lens[b] - (L - 1 - i);
+            for (int h = 0; h < Hq; ++h) {
+                size_t r = (size_t)(query_start[b] + i) * Hq + h;
+                double m, lsum;
+                rc = partial_q(&P, r * D, b, h, 0, n_i, &m, &lsum, acc, s, row);
+                if (rc) break;
+                double* o = out + r * D;
+                for (int d = 0; d < D; ++d) o[d] = acc[d] / lsum;
+            }
+        }
+    }
+    free(s); free(row); free(acc);
+    return rc;
+}
+
 /* Split mode [ECHO2]: per (b, h, split j) the partial state (m_j, l_j, acc_j) of the tokens in
  * split j (orc_split_count's ranges). m/l are [B][Hq][max_splits], acc [B][Hq][max_splits][D];
  * unused split slots are left as m = -inf, l = 0, acc = 0. n_splits[b] receives the count. */

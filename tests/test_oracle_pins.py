@@ -392,3 +392,37 @@ def test_multi_token_needs_context_for_every_new_token(orc):
     q = np.zeros((2, 4, w.Hq, w.D), np.uint16)
     with pytest.raises(RuntimeError):
         orc.paged_decode_attention_multi(q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+
+
+# ---- paged prefill (varlen causal) --------------------------------------------------------------
+
+def test_prefill_with_uniform_lengths_is_multi_token_decode(orc):
+    w = W.make_prefill(name="p", query_lens=[3, 3, 3], cached_lens=[10, 0, 40], Hq=4, Hkv=2, D=64, seed=3)
+    a = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                    w.query_start, w.scale)
+    b = orc.paged_decode_attention_multi(w.q.reshape(3, 3, 4, 64), w.k_pool, w.v_pool,
+                                         w.block_tables, w.context_lens, w.scale)
+    assert np.array_equal(a.reshape(3, 3, 4, 64), b)
+
+
+def test_prefill_matches_library_causal_attention(orc):
+    """Whole-prompt prefill (nothing cached) is ordinary causal attention: torch SDPA with
+    is_causal on the gathered K/V, fp64 on CPU."""
+    torch = pytest.importorskip("torch")
+    w = W.make_prefill(name="p", query_lens=[37, 1, 20], cached_lens=[0, 0, 0], Hq=4, Hkv=2, D=64, seed=5)
+    out = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                      w.query_start, w.scale)
+    kf = W.bf16_bits_to_f32(w.k_pool).astype(np.float64)
+    vf = W.bf16_bits_to_f32(w.v_pool).astype(np.float64)
+    qf = W.bf16_bits_to_f32(w.q).astype(np.float64)
+    for b in range(w.B):
+        n = int(w.context_lens[b])
+        rows = [(w.block_tables[b, t // 16], t % 16) for t in range(n)]
+        K = np.stack([kf[blk, :, off] for blk, off in rows], 1)  # [Hkv, n, D]
+        V = np.stack([vf[blk, :, off] for blk, off in rows], 1)
+        Q = qf[w.query_start[b]:w.query_start[b + 1]].transpose(1, 0, 2)  # [Hq, n, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(Q), torch.from_numpy(K).repeat_interleave(2, 0),
+            torch.from_numpy(V).repeat_interleave(2, 0), is_causal=True, scale=w.scale)
+        np.testing.assert_allclose(out[w.query_start[b]:w.query_start[b + 1]],
+                                   ref.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)

@@ -336,3 +336,54 @@ def make_multi_token(w: DecodeWorkload, L: int, seed: int) -> DecodeWorkload:
         vn, _ = _draw_kv(rng, (B * L, Hkv, D), w.kv_dtype)
     return DecodeWorkload(**{**w.__dict__, "name": f"{w.name}_mtp{L}", "q": q,
                              "slot_mapping": slots, "k_new": kn, "v_new": vn, **extra})
+
+
+@dataclass
+class PrefillWorkload:
+    """A paged (chunked) prefill step: sequence b has context_lens[b] tokens in the pool, of
+    which its last L_b (query_start[b + 1] - query_start[b]) are this step's queries."""
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    BS: int
+    NB: int
+    q: np.ndarray             # bf16 bits [total, Hq, D]
+    k_pool: np.ndarray        # bf16 bits [NB, Hkv, BS, D]
+    v_pool: np.ndarray
+    block_tables: np.ndarray  # int32 [B, MBPS]
+    context_lens: np.ndarray  # int32 [B]
+    query_start: np.ndarray   # int32 [B + 1]
+    scale: float
+
+    @property
+    def B(self):
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_query_len(self):
+        return int(np.diff(self.query_start).max()) if self.B else 0
+
+
+def make_prefill(*, name, query_lens, cached_lens, Hq, Hkv, D, seed, pool_slack=0.10) -> PrefillWorkload:
+    """Sequences with cached_lens[b] tokens already in the cache and query_lens[b] new prompt
+    tokens (also in the cache, written before attention), blocks from a shuffled pool."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ql = np.asarray(query_lens, np.int64)
+    cl = ql + np.asarray(cached_lens, np.int64)
+    B = len(ql)
+    need = [-(-int(n) // BLOCK_SIZE) for n in cl]
+    NB = max(1, int(math.ceil(sum(need) * (1 + pool_slack))))
+    pool = BlockPool(NB, rng)
+    MBPS = max(1, max(need))
+    bt = np.full((B, MBPS), -1, np.int32)
+    for b in range(B):
+        if need[b]:
+            bt[b, :need[b]] = pool.allocate(need[b])
+    kp = _draw(rng, (NB, Hkv, BLOCK_SIZE, D), "bf16")
+    vp = _draw(rng, (NB, Hkv, BLOCK_SIZE, D), "bf16")
+    qs = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    q = _draw(rng, (int(qs[-1]), Hq, D), "bf16")
+    return PrefillWorkload(name=name, Hq=Hq, Hkv=Hkv, D=D, BS=BLOCK_SIZE, NB=NB, q=q, k_pool=kp,
+                           v_pool=vp, block_tables=bt, context_lens=cl.astype(np.int32),
+                           query_start=qs, scale=1.0 / math.sqrt(D))
