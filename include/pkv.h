@@ -110,6 +110,30 @@ pkv_status pkv_kv_cache_write_int8(const void* k_new, const void* v_new, int8_t*
                                    pkv_dtype src_dtype, int32_t* status, void* stream);
 
 /*
+ * Paged (chunked, variable-length) prefill attention on tcgen05 tensor cores ("EchoLLMServing
+ * inference framework notes", section 2: FlashAttention tiles the prefill queries; section 3:
+ * chunked prefill; "LLM Primer VI, Chapter 8", section 8.1: K/V through the block table).
+ * Sequence b owns query rows query_start[b] .. query_start[b + 1] - 1 of q and out
+ * ([total_query_tokens][num_q_heads][128], bf16): they are the last
+ * L_b = query_start[b + 1] - query_start[b] tokens of its context_lens[b] tokens, whose K/V are
+ * already in the pool (written with pkv_kv_cache_write). Row i of sequence b attends causally:
+ *     out[query_start[b] + i][h][:] = sum_{t < n_b - L_b + 1 + i} softmax_t(scale * <q, K_t>) V_t
+ * bf16 pools [num_blocks][num_kv_heads][16][128] only (head_dim 128; PKV_ERR_UNSUPPORTED
+ * otherwise). query_start is int32 [num_seqs + 1], non-decreasing, query_start[0] = 0;
+ * max_query_len >= every L_b (sizes the grid; a longer sequence's extra rows are not computed).
+ * A sequence with context_lens[b] < L_b or beyond the table is flagged (PKV_FLAG_BAD_CONTEXT) and
+ * its rows are not written. Needs no workspace. Accumulation fp32 in TMEM; the softmax weights
+ * enter the second product as bf16.
+ */
+pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_pool,
+                                       const void* v_pool, const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* query_start,
+                                       int num_seqs, int total_query_tokens, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int block_size,
+                                       int num_blocks, int max_blocks_per_seq, int max_query_len,
+                                       float scale, int32_t* status, void* stream);
+
+/*
  * Multi-token decode: L = num_query_tokens new tokens per sequence, verified in one pass, as MTP
  * speculative decoding does ("AMD ATOM inference engine", section 4: a decode step reserves
  * num_new_tokens = mtp_k + 1 cache slots per sequence). The L new tokens are the last L of

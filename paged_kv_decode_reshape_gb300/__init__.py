@@ -32,6 +32,8 @@ SIGNATURES = {
                                          _I, _I, _F, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_decode_attention_multi": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                           _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P], _I),
+    "pkv_paged_prefill_attention": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     _I, _F, _P, _P], _I),
     "pkv_paged_decode_attention_static_ws": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                               _I, _F, _I, _I, _P, _P], _I),
 }
@@ -178,6 +180,19 @@ def paged_decode_attention_multi(out, q, k_pool, v_pool, block_tables, context_l
         _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream))
     _check(rc, "paged_decode_attention_multi")
+
+
+def paged_prefill_attention(out, q, k_pool, v_pool, block_tables, context_lens, query_start,
+                            max_query_len, scale, status=None, stream=None):
+    """pkv_paged_prefill_attention: q/out [total, Hq, 128] bf16; sequence b's rows are
+    query_start[b] .. query_start[b + 1] - 1, its last tokens, attending causally."""
+    T, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_prefill_attention(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start), context_lens.shape[0], T, Hq, Hkv, D, BS, NB, block_tables.shape[1],
+        int(max_query_len), float(scale), _ptr(status), _stream(stream))
+    _check(rc, "paged_prefill_attention")
 
 
 def paged_decode_attention_static_ws(out, q, k_pool, v_pool, block_tables, context_lens,

@@ -122,16 +122,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
-// 2-D TMA tile load (box of the tensor map at coordinates (x, y)) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                           uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // int8 -> biased fp16, two values per instruction (the byte-permute / magic-number conversion
 // of Kim et al. 2022): placing the byte x + 128 (x XOR 0x80) in the low byte of the fp16 1024
 // gives exactly 1152 + x. For a word of four int8 [b0 b1 b2 b3], lo -> fp16x2(1152+b0, 1152+b2)

@@ -115,6 +115,17 @@ struct QuantWriteParams {
     int T, Hkv, NB;
 };
 
+struct PrefillParams {
+    void* out;                    // [total][Hq][128] bf16
+    const void* q;                // [total][Hq][128] bf16
+    const int32_t* block_tables;  // [B][MBPS]
+    const int32_t* context_lens;  // [B]
+    const int32_t* query_start;   // [B + 1]
+    int32_t* status;
+    int B, Hq, Hkv, G, NB, MBPS;
+    float scale_log2;
+};
+
 // Launchers (return the launch's error code).
 cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_kv_write_quant(const QuantWriteParams& p, pkv_dtype src, int D, cudaStream_t s);
@@ -126,6 +137,8 @@ cudaError_t launch_merge(const MergeParams& p, pkv_dtype out_dtype, int D, cudaS
 // Tensor-core split kernel for head_dim 128, bf16 or INT8 pools, 8 query heads per CTA; the K and
 // V pools are described by TMA tensor maps built with make_pool_tensor_map (false on failure).
 bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, bool i8);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int max_query_len, cudaStream_t s);
 cudaError_t launch_split_mma(const SplitParams& p, bool i8, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s);
 

@@ -184,3 +184,21 @@ def test_multi_token_argument_checks(pkv, kw, expect):
         a["Hq"], a["Hkv"], a["D"], a["BS"], a["NB"], a["MBPS"], a["maxc"], a["scale"], a["dtype"],
         a["chunk"], a["ws"], a["wsb"], None, None)
     assert rc == expect
+
+
+@fake_ptrs
+@pytest.mark.parametrize("kw,expect", [
+    (dict(D=64), P.ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=4), P.ERR_INVALID_ARG),
+    (dict(qs=None), P.ERR_INVALID_ARG),
+    (dict(out=FAKE[1]), P.ERR_INVALID_ARG),                             # out aliases q
+    (dict(T=0), P.OK),
+])
+def test_prefill_argument_checks(pkv, kw, expect):
+    a = dict(out=FAKE[0], q=FAKE[1], k=FAKE[2], v=FAKE[3], bt=FAKE[4], cl=FAKE[5], qs=FAKE[6],
+             B=2, T=10, Hq=8, Hkv=2, D=128, BS=16, NB=64, MBPS=8, maxq=8, scale=0.1)
+    a.update(kw)
+    rc = P.load().pkv_paged_prefill_attention(
+        a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["qs"], a["B"], a["T"], a["Hq"],
+        a["Hkv"], a["D"], a["BS"], a["NB"], a["MBPS"], a["maxq"], a["scale"], None, None)
+    assert rc == expect

@@ -1,0 +1,74 @@
+"""GPU parity of the tcgen05 paged prefill kernel against the fp64 oracle: variable query lengths
+(1 to several 128-row tiles, ragged), cached prefixes, GQA groups, and missing blocks."""
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_decode_reshape_gb300 as P
+import workloads as W
+from _gpu import assert_close, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(pkv):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_prefill(w, status=None, bt=None):
+    bt = w.block_tables if bt is None else bt
+    out = torch.zeros((w.q.shape[0], w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    P.paged_prefill_attention(out, to_dev(w.q), to_dev(w.k_pool), to_dev(w.v_pool), to_dev(bt),
+                              to_dev(w.context_lens), to_dev(w.query_start), w.max_query_len,
+                              w.scale, status)
+    return to_f64(out)
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2)])
+def test_prefill_matches_oracle(hq, hkv):
+    w = W.make_prefill(name="pf", query_lens=[1, 5, 127, 128, 129, 300],
+                       cached_lens=[0, 17, 64, 200, 5, 1000], Hq=hq, Hkv=hkv, D=128, seed=hq + hkv)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill(w, st)
+    ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                         w.query_start, w.scale)
+    assert_close(got, ref, "bf16", f"prefill Hq={hq} Hkv={hkv}")
+    assert int(st.item()) == 0
+
+
+def test_prefill_single_token_rows_equal_decode():
+    """A prefill chunk of one token per sequence is a decode step."""
+    w = W.make_prefill(name="pf1", query_lens=[1, 1, 1, 1], cached_lens=[0, 15, 16, 700], Hq=32,
+                       Hkv=8, D=128, seed=4)
+    got = run_prefill(w)
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale)
+    assert_close(got, ref, "bf16", "prefill L=1")
+
+
+def test_prefill_long_prompt():
+    w = W.make_prefill(name="pfl", query_lens=[1000, 37], cached_lens=[2048, 3000], Hq=32, Hkv=8,
+                       D=128, seed=8)
+    got = run_prefill(w)
+    rows = np.r_[0:64, 480:560, 936:1037]
+    sub_q = w.q[rows]
+    ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                         w.query_start, w.scale)
+    assert_close(got[rows], ref[rows], "bf16", "long prompt rows")
+    assert sub_q.shape[0] == rows.size
+
+
+def test_prefill_missing_block_is_skipped_and_flagged():
+    w = W.make_prefill(name="pfb", query_lens=[40, 70], cached_lens=[100, 30], Hq=8, Hkv=8, D=128, seed=9)
+    bt = w.block_tables.copy()
+    bt[0, 2] = w.NB + 5  # a block of sequence 0 outside the pool
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill(w, st, bt)
+    assert int(st.item()) & P.FLAG_BAD_BLOCK
+    assert np.all(np.isfinite(got))
+    ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                         w.query_start, w.scale)
+    s1 = slice(w.query_start[1], w.query_start[2])
+    assert_close(got[s1], ref[s1], "bf16", "untouched sequence")
