@@ -429,6 +429,78 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def prefill_flops(w) -> int:
+    """Algorithmic FLOPs of a causal paged prefill: per query head and row i of sequence b,
+    2 * D for each visible key in Q K^T and again in P V."""
+    vis = 0
+    for b in range(w.B):
+        L = int(w.query_start[b + 1] - w.query_start[b])
+        n = int(w.context_lens[b])
+        vis += sum(n - L + 1 + i for i in range(L))
+    return 4 * w.D * w.Hq * vis
+
+
+def run_prefill(args):
+    """Paged chunked prefill on tcgen05: 4 sequences x 4096 new prompt tokens after 2048 cached
+    tokens, Llama-3-8B heads (32 q / 8 kv, D = 128, bf16). Reports TFLOP/s against the measured
+    dense bf16 tensor peak."""
+    import torch
+
+    import paged_kv_decode_reshape_gb300 as pkv
+    pkv.load(build_if_missing=False)
+    w = W.make_prefill(name="prefill_llama3_8b", query_lens=[4096] * 4, cached_lens=[2048] * 4,
+                       Hq=32, Hkv=8, D=128, seed=7)
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(a).cuda()
+    q, kp, vp = up(w.q), up(w.k_pool), up(w.v_pool)
+    bt, cl, qs = up(w.block_tables), up(w.context_lens), up(w.query_start)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step():
+        pkv.paged_prefill_attention(out, q, kp, vp, bt, cl, qs, w.max_query_len, w.scale)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    for k in range(K):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record()
+        step()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    flops = prefill_flops(w)
+    tflops = flops / (ms / 1e3) / 1e12
+    peak = 1925.2
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            peak = float(json.load(f).get("bf16_tflops", peak))
+    line = {"metric": "paged prefill attention TFLOP/s (causal, tcgen05)", "value": round(tflops, 2),
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "sequences": w.B, "new_tokens": 4096, "cached_tokens": 2048,
+                       "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "flops_per_step": flops,
+                       "l2": "flushed before every step (untimed)"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "peak_kind": "of measured (cuBLAS bf16 burst)"},
+            "tokens_per_s": round(int(w.query_start[-1]) / (ms / 1e3), 1)}
+    if clk is not None:
+        line["clocks"] = clk
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,8 +510,12 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
     ap.add_argument("--chunk", type=int, default=0, help="split chunk in tokens (0 = auto)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the paged prefill kernel instead of the decode step")
     args = ap.parse_args(argv)
-    if args.impl == "reference":
+    if args.prefill:
+        run_prefill(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
