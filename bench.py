@@ -306,7 +306,8 @@ def run_ours(args):
     kns, vns = up(w.k_new_scales), up(w.v_new_scales)
     out = torch.empty_like(q)
     maxc = w.max_context_len
-    chunk = pkv.decode_split_chunk(w.B, w.Hkv, maxc, args.chunk)
+    chunk = pkv.decode_split_chunk(w.B, w.Hkv, w.D, maxc, args.chunk,
+                                   {"f32": pkv.F32, "bf16": pkv.BF16, "i8": pkv.I8}[w.kv_dtype])
     nws = pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, args.chunk)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -163,20 +163,25 @@ pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void
  * states (m, l, acc) of a batch: the split count per sequence follows "EchoLLMServing
  * inference framework notes", section 2 (split_num = max(1, context_len // chunk)), so the
  * bound uses max_context_len. split_chunk_tokens = 0 selects the library's chunk for this batch
- * shape (pkv_decode_split_chunk). Returns 0 for invalid arguments. Pure host arithmetic.
+ * shape. The auto chunk depends on the K/V dtype (pkv_decode_split_chunk); this bound takes the
+ * smallest chunk any dtype would get, so it covers them all. Returns 0 for invalid arguments.
+ * Pure host arithmetic.
  */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len, int split_chunk_tokens);
 
-/* The chunk (tokens per split before block rounding) used for a request of split_chunk_tokens
- * (0 = auto) and this batch shape; 0 for invalid arguments. The same notes call the chunk a
- * value calibrated from the GPU's SM count and cache size; the auto rule here aims at about
- * 4096 (sequence, kv head, split) units for the 152 SMs of a GB300 -- the power of two in
- * [256, 4096] nearest below num_seqs * num_kv_heads * max_context_len / 4096 -- and grows the
- * chunk until the split extent max(1, max_context_len / chunk) is at most 8192.
+/* The chunk (tokens per split before block rounding) that pkv_paged_decode_attention[_int8,
+ * _multi] use for a request of split_chunk_tokens (0 = auto), this batch shape and K/V dtype
+ * (num_seqs counts (sequence, query token) rows for the multi-token call); 0 for invalid
+ * arguments. The same notes call the chunk a value calibrated by profiling the GPU; the auto rule
+ * here is the power of two in [256, 4096] nearest below num_seqs * num_kv_heads *
+ * max_context_len / (2 * U), where U is the number of (sequence, kv head, split) units the kernel
+ * that serves the call does best with on a GB300 (152 SMs): 2048 for the bf16 head_dim-128
+ * tensor-core kernel, 4096 for the INT8 one and for the CUDA-core kernel (fp32, head_dim 64).
+ * The chunk then grows until the split extent max(1, max_context_len / chunk) is at most 8192.
  * Pure host arithmetic. */
-int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int max_context_len,
-                           int split_chunk_tokens);
+int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
+                           int split_chunk_tokens, pkv_dtype kv_dtype);
 
 /*
  * Paged decode attention ("LLM Primer VI, Chapter 8", section 8.1; "EchoLLMServing inference

@@ -25,7 +25,7 @@ SIGNATURES = {
     "pkv_kv_cache_write": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_kv_cache_write_int8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
-    "pkv_decode_split_chunk": ([_I, _I, _I, _I], _I),
+    "pkv_decode_split_chunk": ([_I, _I, _I, _I, _I, _I], _I),
     "pkv_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                     _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_decode_attention_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
@@ -129,9 +129,11 @@ def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_co
                                                  max_context_len, split_chunk_tokens))
 
 
-def decode_split_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens=0) -> int:
-    return int(load().pkv_decode_split_chunk(num_seqs, num_kv_heads, max_context_len,
-                                             split_chunk_tokens))
+def decode_split_chunk(num_seqs, num_kv_heads, head_dim, max_context_len, split_chunk_tokens=0,
+                       kv_dtype=BF16) -> int:
+    """The chunk a decode call uses; kv_dtype is F32, BF16 or I8 (the pool's element type)."""
+    return int(load().pkv_decode_split_chunk(num_seqs, num_kv_heads, head_dim, max_context_len,
+                                             split_chunk_tokens, kv_dtype))
 
 
 def paged_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, max_context_len,

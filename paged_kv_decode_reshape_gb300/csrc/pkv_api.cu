@@ -28,11 +28,20 @@ size_t elem_bytes(pkv_dtype t) { return t == PKV_F32 ? 4 : t == PKV_BF16 ? 2 : t
 // [kMinAutoChunk, kMaxAutoChunk] nearest below (work units of the batch) / kTargetUnits, so that
 // a batch yields about kTargetUnits units for the GPU's SMs to share; doubled further while the
 // split extent exceeds what the merge kernel supports.
-int choose_chunk(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
+// the tensor-core kernel serves head_dim 128 with bf16 or INT8 pools; the CUDA-core kernel the rest
+bool uses_mma(int head_dim, pkv_dtype kv_dtype) {
+    return head_dim == 128 && (kv_dtype == PKV_BF16 || kv_dtype == PKV_I8);
+}
+
+long long target_units(int head_dim, pkv_dtype kv_dtype) {
+    return uses_mma(head_dim, kv_dtype) && kv_dtype == PKV_BF16 ? kTargetUnitsBf16Mma : kTargetUnits;
+}
+
+int choose_chunk(int num_seqs, int num_kv_heads, int max_context_len, int requested, long long target) {
     if (requested > 0) return requested;
     const long long tokens = (long long)num_seqs * num_kv_heads * max_context_len;
     int c = kMinAutoChunk;
-    while (c < kMaxAutoChunk && tokens / (2LL * c) >= kTargetUnits) c *= 2;
+    while (c < kMaxAutoChunk && tokens / (2LL * c) >= target) c *= 2;
     while (max_context_len / c > kMaxSplits) c *= 2;
     return c;
 }
@@ -84,13 +93,13 @@ pkv_status run_decode(const Decode& a) {
     const int g = a.Hq / a.Hkv;
     // head_dim 128 bf16 / INT8 pools run on the tensor-core kernel (8 heads per CTA); fp32 and
     // head_dim 64 on the CUDA-core kernel
-    const bool mma = a.D == 128 && (a.kv_dtype == PKV_BF16 || a.kv_dtype == PKV_I8);
+    const bool mma = uses_mma(a.D, a.kv_dtype);
     const int hg = mma ? 8 : heads_per_cta(g);
     const int head_chunks = (g + hg - 1) / hg;
     if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
-    const int chunk = choose_chunk(rows, a.Hkv, a.max_ctx, a.chunk_req);
+    const int chunk = choose_chunk(rows, a.Hkv, a.max_ctx, a.chunk_req, target_units(a.D, a.kv_dtype));
     const int S = split_extent(a.max_ctx, chunk);
     if (S > kMaxSplits) return PKV_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes_for(rows, a.Hq, a.D, S);
@@ -236,12 +245,14 @@ pkv_status pkv_kv_cache_write_int8(const void* k_new, const void* v_new, int8_t*
                : PKV_ERR_CUDA;
 }
 
-int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int max_context_len,
-                           int split_chunk_tokens) {
-    if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0 || split_chunk_tokens < 0 ||
-        split_chunk_tokens % kBlockSize)
+int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
+                           int split_chunk_tokens, pkv_dtype kv_dtype) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize ||
+        (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8))
         return 0;
-    return choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens);
+    return choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens,
+                        target_units(head_dim, kv_dtype));
 }
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -249,7 +260,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_context_len < 0 || split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize)
         return 0;
-    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens);
+    // the largest target (smallest chunk, most splits) of any K/V dtype: an upper bound for all
+    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens, kTargetUnits);
     return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
 }
 

@@ -14,7 +14,12 @@ constexpr int kBlockSize = 16;      // tokens per KV block (the only size built)
 constexpr int kMaxSplits = 8192;    // split extent the merge kernel supports
 constexpr int kMinAutoChunk = 256;   // auto chunk range (tokens per split before block rounding)
 constexpr int kMaxAutoChunk = 4096;
-constexpr long long kTargetUnits = 4096;  // (sequence, kv head, split) units the auto chunk aims at
+// (sequence, kv head, split) units the auto chunk aims at, per kernel: measured on GB300 (152 SMs)
+// over chunks 256..4096 on the Llama-3-8B GQA, 131k-context, INT8 and shared-prefix batches. The
+// bf16 tensor-core kernel keeps 3 CTAs per SM and does best with fewer, longer splits; the INT8 one
+// keeps 5 per SM and, doing more arithmetic per byte, with more of them.
+constexpr long long kTargetUnitsBf16Mma = 2048;
+constexpr long long kTargetUnits = 4096;  // INT8 tensor-core and CUDA-core kernels
 
 // Split rule ("EchoLLMServing inference framework notes", section 2, FlashDecoding):
 // split_num = max(1, n // chunk), capped at max_splits; each split is a whole number of

@@ -53,21 +53,31 @@ def test_status_strings(pkv):
 
 def test_workspace_arithmetic(pkv):
     L = P.load()
-    # 8 seqs x 32 q / 8 kv heads, 131072 tokens: auto chunk 2048 -> 64 splits x (128 acc + m + l)
-    assert L.pkv_decode_split_chunk(8, 8, 131072, 0) == 2048
+    # 8 seqs x 32 q / 8 kv heads, 131072 tokens: the workspace bound takes the INT8 auto chunk,
+    # 2048 -> 64 splits x (128 acc + m + l)
+    assert L.pkv_decode_split_chunk(8, 8, 128, 131072, 0, P.I8) == 2048
+    assert L.pkv_decode_split_chunk(8, 8, 128, 131072, 0, P.BF16) == 4096
     assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 0) == 8 * 32 * 64 * 130 * 4
     assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 1024) == 8 * 32 * 128 * 130 * 4
     assert L.pkv_decode_workspace_bytes(4, 4, 4, 64, 100, 0) == 0    # one split: no workspace
     assert L.pkv_decode_workspace_bytes(4, 4, 4, 64, 100, 17) == 0   # chunk not a block multiple
-    # auto chunk: ~4096 units, powers of two in [256, 4096], more only to keep splits <= 8192
-    assert L.pkv_decode_split_chunk(64, 8, 4055, 0) == 256
-    assert L.pkv_decode_split_chunk(128, 8, 8083, 0) == 1024
-    assert L.pkv_decode_split_chunk(256, 8, 4090, 0) == 1024
-    assert L.pkv_decode_split_chunk(4, 4, 100, 0) == 256
-    assert L.pkv_decode_split_chunk(1024, 64, 1 << 20, 0) == 4096
-    assert L.pkv_decode_split_chunk(1, 1, 1 << 30, 0) >= 4096
-    assert (1 << 30) // L.pkv_decode_split_chunk(1, 1, 1 << 30, 0) <= 8192
-    assert L.pkv_decode_split_chunk(4, 4, 100, 48) == 48             # explicit request kept
+    # auto chunk: ~2048 units (bf16 tensor-core kernel) or ~4096 (INT8, CUDA-core), powers of
+    # two in [256, 4096], more only to keep splits <= 8192
+    BF, I8, F32 = P.BF16, P.I8, P.F32
+    assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, BF) == 512      # Llama-3-8B GQA batch
+    assert L.pkv_decode_split_chunk(8, 8, 128, 130882, 0, BF) == 2048    # 131k-context batch
+    assert L.pkv_decode_split_chunk(128, 8, 128, 8083, 0, I8) == 1024    # INT8 batch
+    assert L.pkv_decode_split_chunk(256, 8, 128, 4090, 0, BF) == 2048    # shared-prefix batch
+    assert L.pkv_decode_split_chunk(64, 8, 64, 4055, 0, BF) == 256       # head_dim 64: CUDA cores
+    assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, F32) == 256     # fp32: CUDA cores
+    assert L.pkv_decode_split_chunk(4, 4, 64, 100, 0, F32) == 256
+    assert L.pkv_decode_split_chunk(1024, 64, 128, 1 << 20, 0, BF) == 4096
+    assert L.pkv_decode_split_chunk(1, 1, 128, 1 << 30, 0, BF) >= 4096
+    assert (1 << 30) // L.pkv_decode_split_chunk(1, 1, 128, 1 << 30, 0, BF) <= 8192
+    assert L.pkv_decode_split_chunk(4, 4, 64, 100, 48, F32) == 48        # explicit request kept
+    assert L.pkv_decode_split_chunk(4, 4, 64, 100, 0, 7) == 0            # unknown dtype
+    # the workspace bound covers the bf16 call (fewer splits) too
+    assert L.pkv_decode_workspace_bytes(64, 32, 8, 128, 4055, 0) == 64 * 32 * (4055 // 256) * 130 * 4
 
 
 def _attn(L, **kw):
