@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+import paged_kv_decode_reshape_gb300 as P
 import workloads as W
 from _gpu import DevWorkload, assert_close, oracle_step, to_dev, to_f64, to_host_raw
 
@@ -132,6 +133,35 @@ def test_split_partials_match_oracle_partials():
         np.testing.assert_allclose(gm + np.log(gl), m[b, :, :k] + np.log(l[b, :, :k]), atol=2e-3)
         np.testing.assert_allclose(acc[b, :, :k] / gl[..., None],
                                    oacc[b, :, :k] / l[b, :, :k, None], atol=5e-3)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "i8", "f32"])
+def test_workspace_contents_on_entry_do_not_matter(kv):
+    """A workspace full of random bytes, one left by a call with other lengths (more splits per
+    sequence), and a repeat of the same call must all give the oracle's answer, the repeat bit for
+    bit: the merge reads only partial states the same call wrote."""
+    lens_a = [700, 33, 1500, 64, 1023, 257]
+    lens_b = [1500, 1400, 16, 900, 1024, 600]
+    mk = lambda lens, seed: W.make_decode(name="ws", B=6, Hq=16, Hkv=2, D=128, context_lens=lens,
+                                          kv_dtype=kv, q_dtype="f32" if kv == "f32" else "bf16",
+                                          seed=seed)
+    wa, wb = mk(lens_a, 51), mk(lens_b, 52)
+    chunk = 64
+    nbytes = max(P.decode_workspace_bytes(6, 16, 2, 128, max(l), chunk) for l in (lens_a, lens_b))
+    g = torch.Generator(device="cuda").manual_seed(5)
+    ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=g)
+
+    def ref(w):
+        return oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables,
+                                             w.context_lens, w.scale, w.k_scales, w.v_scales)
+    da, db = DevWorkload(wa), DevWorkload(wb)
+    first = da.attend(chunk=chunk, workspace=ws).clone()
+    assert_close(to_f64(first), ref(wa), kv, "random workspace")
+    got_b = db.attend(chunk=chunk, workspace=ws)
+    assert_close(to_f64(got_b), ref(wb), kv, "workspace left by another batch")
+    again = da.attend(chunk=chunk, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(again, first)
 
 
 @pytest.mark.parametrize("cfg", [2, 4])
