@@ -7,16 +7,23 @@
 // Sequence b's L_b query tokens are the last L_b of its context (written to the cache first);
 // query row i attends causally to the first n_b - (L_b - 1 - i) tokens.
 //
-// One CTA (4 warps) computes 128 query rows of one query head. The Q tile sits in shared memory
-// (K-major, 128-byte swizzle). K and V of 64-token key tiles -- four 16-token pool blocks -- come
-// in by TMA through the block table into a 2-stage ring. Per key tile:
-//   S[128 x 64]  = Q[128 x 128] . K^T     one thread issues 8 tcgen05.mma (k = 16), D in TMEM
-//   thread r reads row r of S from TMEM (tcgen05.ld), masks it (causal limit, context, missing
-//   blocks), keeps its own running max and sum (the max is raised lazily, by more than 2^8 only;
-//   O is rescaled in TMEM when it is), and writes its bf16 weights as row r of P in shared memory
-//   O[128 x 128] += P[128 x 64] . V      4 tcgen05.mma, V read MN-major from its natural layout
-// tcgen05.commit signals each product on an mbarrier; the next tile's copy starts as soon as the
-// product that read its stage is done. At the end thread r divides its O row by its sum.
+// One CTA computes the same 128 query rows for two query heads of one GQA group (tiles A and B):
+// both read every K/V tile once and have the same causal extent, so their work stays in step.
+// Warp roles (320 threads):
+//   warps 0-3  softmax of tile A: thread r owns query row r (TMEM lane r)
+//   warps 4-7  softmax of tile B
+//   warp 8     lane 0 issues every tcgen05.mma and commit; the warp owns the TMEM allocation
+//   warp 9     producer: block ids from the table, 2-D TMA copies of 64-key K/V tiles (four pool
+//              blocks) into a STAGES-deep ring
+// Per key tile t, the tensor core runs, in this order,
+//   PV_A(t-1 -> t): O_A += P_A . V_t ;  S_A(t+1) = Q_A . K_{t+1}^T ;  O_B += P_B . V_t ;
+//   S_B(t+1) = Q_B . K_{t+1}^T
+// so that while one tile's softmax warps turn S into P, the tensor core works on the other tile.
+// TMEM columns: O_A 0-127, O_B 128-255, S_A 256-319, S_B 320-383. A commit after S_X(t+1) also
+// covers PV_X(t) (commits track every earlier MMA of the issuing thread), so when softmax X sees
+// S_X(t+1) it may overwrite P_X and rescale O_X. The running max is raised lazily (only when a
+// tile exceeds it by more than 2^8), so O is rarely rescaled; at the end thread r divides its O
+// row by its sum.
 #include <cuda.h>
 
 #include "pkv_device.cuh"
@@ -25,20 +32,28 @@ namespace pkv {
 
 namespace {
 
-constexpr int kPfQ = 128;                      // query rows per CTA (MMA M)
+constexpr int kPfQ = 128;                      // query rows per tile (MMA M)
 constexpr int kPfK = 64;                       // keys per tile
 constexpr int kPfQBytes = 2 * kPfQ * 128;      // Q: two 64-dim halves of [128 rows x 128 B]
 constexpr int kPfPBytes = kPfQ * 128;          // P: [128 rows x 64 keys] bf16
 constexpr int kPfHalf = kPfK * 128;            // one 64-dim half of a K or V tile
 constexpr int kPfStage = 4 * kPfHalf;          // K half 0, K half 1, V half 0, V half 1
-constexpr int kPfStages = 2;
-constexpr int kPfOffP = kPfQBytes;
-constexpr int kPfOffKV = kPfQBytes + kPfPBytes;
+#ifndef PKV_PF_STAGES
+#define PKV_PF_STAGES 2
+#endif
+constexpr int kPfStages = PKV_PF_STAGES;
+constexpr int kPfOffP = 2 * kPfQBytes;         // Q_A, Q_B, then P_A, P_B
+constexpr int kPfOffKV = kPfOffP + 2 * kPfPBytes;
 constexpr int kPfOffBar = kPfOffKV + kPfStages * kPfStage;
-constexpr int kPfSmem = 1024 + kPfOffBar + 128;
-constexpr uint32_t kPfTmemCols = 256;          // O: columns 0..127, S: 128..191
-constexpr uint32_t kOCol = 0, kSCol = 128;
+// barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, drain; then the TMEM slot
+constexpr int kPfNumBars = 2 * kPfStages + 6;
+constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
+constexpr int kPfThreads = 320;
+constexpr int kPfMmaWarp = 8, kPfLoadWarp = 9;
+constexpr uint32_t kPfTmemCols = 512;
+constexpr uint32_t kOCol = 0, kSCol = 256;     // O_X at 128 X, S_X at 256 + 64 X
 constexpr float kPfRescale = 8.0f;             // log2 units
+static_assert(kPfSmem <= 227 * 1024, "shared memory");
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading / stride byte offsets,
 // descriptor version 1, 128-byte swizzle.
@@ -110,256 +125,327 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(128) prefill_kernel(const PrefillParams p,
-                                                      const __grid_constant__ CUtensorMap tmk,
-                                                      const __grid_constant__ CUtensorMap tmv) {
+__device__ __forceinline__ bool aborted(const volatile int* f) { return *f != 0; }
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillParams p,
+                                                                const __grid_constant__ CUtensorMap tmk,
+                                                                const __grid_constant__ CUtensorMap tmv) {
     grid_dependency_wait();
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    // heaviest query tiles (most keys under the causal mask) first
+    const int qt = gridDim.x - 1 - blockIdx.x, b = blockIdx.z;
+    const int HP = (p.G + 1) / 2;                       // head pairs per kv head
+    const int kvh = blockIdx.y / HP, hp = blockIdx.y - kvh * HP;
+    const bool two = 2 * hp + 1 < p.G;                  // tile B exists
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q0 = p.query_start[b];
     const int L = p.query_start[b + 1] - q0;
     if (qt * kPfQ >= L) return;
     const int n = p.context_lens[b];
     if (n < L || n > p.MBPS * kBlockSize) {
-        if (tid == 0 && qt == 0 && h == 0) flag(p.status, PKV_FLAG_BAD_CONTEXT);
+        if (tid == 0 && qt == 0 && blockIdx.y == 0) flag(p.status, PKV_FLAG_BAD_CONTEXT);
         return;
     }
-    const int first_visible = n - L + 1;                       // keys visible to query row 0
+    const int first_visible = n - L + 1;                          // keys visible to query row 0
     const int rows = min(kPfQ, L - qt * kPfQ);
     const int n_tile_max = first_visible + qt * kPfQ + rows - 1;  // keys visible to the last row
     const int ntiles = (n_tile_max + kPfK - 1) / kPfK;
-    const int kvh = h / p.G;
+    const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const uint32_t sq = smem_addr(smem), sp = sq + kPfOffP, skv = sq + kPfOffKV;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPfOffBar);  // full[2], s, o
-    const uint32_t full0 = smem_addr(bars), bar_s = full0 + 16, bar_o = full0 + 24;
-    int32_t* tile_mask = reinterpret_cast<int32_t*>(smem + kPfOffBar + 32);  // [2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + 48);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t skv = sbase + kPfOffKV;
+    const uint32_t bar0 = sbase + kPfOffBar;
+    auto kv_full = [&](int s) { return bar0 + 8 * s; };
+    auto kv_empty = [&](int s) { return bar0 + 8 * (kPfStages + s); };
+    auto s_full = [&](int x) { return bar0 + 8 * (2 * kPfStages + x); };
+    auto p_full = [&](int x) { return bar0 + 8 * (2 * kPfStages + 2 + x); };
+    const uint32_t o_done = bar0 + 8 * (2 * kPfStages + 4);
+    const uint32_t drain = bar0 + 8 * (2 * kPfStages + 5);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + kPfNumBars * 8);
     __shared__ int abort_flag;
 
     if (tid == 0) {
-        mbar_init(full0, 1);
-        mbar_init(full0 + 8, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
+        for (int s = 0; s < kPfStages; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), kPfQ);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
         abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 0) {
+    if (warp == kPfMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                      "r"(kPfTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+
+    // ---- Q tiles: softmax thread r of tile X writes query row r (zeros past the sequence's queries) ----
+    const int gx = warp >> 2;              // softmax group (tile) of warps 0-7
+    const int r = tid & 127;               // its row / TMEM lane
+    const int i = qt * kPfQ + r;
+    const bool row_valid = i < L;
+    if (warp < 8 && (gx == 0 || two)) {
+        const int h = kvh * p.G + 2 * hp + gx;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                          ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128);
+        unsigned char* qs = smem + gx * kPfQBytes;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = dims 8c .. 8c+7
+            const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t off = (c >> 3) * (kPfQ * 128) + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+            *reinterpret_cast<uint4*>(qs + off) = v;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quadrant
 
-    // ---- Q tile: row tid is query i of the sequence (zeros past its queries) ----
-    const int i = qt * kPfQ + tid;
-    const bool row_valid = i < L;
-    const int n_row = row_valid ? first_visible + i : 0;
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = dims 8c .. 8c+7
-            const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t off = (c >> 3) * (kPfQ * 128) + tid * 128 + ((((c & 7) ^ (tid & 7))) << 4);
-            *reinterpret_cast<uint4*>(smem + off) = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-
-    // ---- producer (thread 0): key tile kt -> stage kt % 2 ----
-    const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS;
-    auto issue = [&](int kt) {
-        const int st = kt & 1;
-        const uint32_t bar = full0 + 8 * st;
-        const uint32_t dst = skv + st * kPfStage;
-        int mask = 0, nvalid = 0, ids[4];
-        for (int jj = 0; jj < 4; ++jj) {
-            const int j = kt * 4 + jj;
-            ids[jj] = -1;
-            if (j * kBlockSize < n_tile_max) {
-                const int id = bt_row[j];
-                if (id >= 0 && id < p.NB) {
-                    ids[jj] = id;
-                    mask |= 1 << jj;
-                    ++nvalid;
-                } else {
-                    flag(p.status, PKV_FLAG_BAD_BLOCK);
+    if (warp == kPfLoadWarp) {
+        // ---------------- producer ----------------
+        int issued = 0;
+        for (int t = 0; t < ntiles; ++t) {
+            const int st = t % kPfStages;
+            if (t >= kPfStages && !mbar_wait_bounded(kv_empty(st), ((t / kPfStages) - 1) & 1, 200)) {
+                if (lane == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
+                break;
+            }
+            if (aborted(&abort_flag)) break;
+            // lane jj < 4: the pool block of keys 64t + 16jj .. (-1 when not needed or invalid)
+            int id = -1;
+            if (lane < 4) {
+                const int j = 4 * t + lane;
+                if (j * kBlockSize < n_tile_max) {
+                    const int v = bt_row[j];
+                    if (v >= 0 && v < p.NB) id = v;
+                    else flag(p.status, PKV_FLAG_BAD_BLOCK);
                 }
             }
+            const unsigned valid = __ballot_sync(0xffffffffu, id >= 0);
+            if (lane == 0) {
+                const uint32_t bar = kv_full(st);
+                if (valid == 0) {
+                    mbar_arrive(bar);
+                } else {
+                    mbar_arrive_expect_tx(bar, __popc(valid) * 4 * (kBlockSize * 128));
+                }
+            }
+            __syncwarp();
+            if (lane < 4 && id >= 0) {
+                const uint32_t bar = kv_full(st), dst = skv + st * kPfStage;
+                const int row = (id * p.Hkv + kvh) * kBlockSize;
+                const uint32_t o = lane * (kBlockSize * 128);
+                tma_load_2d(dst + o, &tmk, 0, row, bar);
+                tma_load_2d(dst + kPfHalf + o, &tmk, 64, row, bar);
+                tma_load_2d(dst + 2 * kPfHalf + o, &tmv, 0, row, bar);
+                tma_load_2d(dst + 3 * kPfHalf + o, &tmv, 64, row, bar);
+            }
+            issued = t + 1;
         }
-        tile_mask[st] = mask;
-        if (nvalid == 0) {
-            mbar_arrive(bar);
-            return;
+        if (aborted(&abort_flag) && lane == 0) {
+            // let this CTA's own copies land before shared memory goes away
+            for (int t = issued - kPfStages < 0 ? 0 : issued - kPfStages; t < issued; ++t)
+                mbar_wait_bounded(kv_full(t % kPfStages), (t / kPfStages) & 1);
         }
-        mbar_arrive_expect_tx(bar, nvalid * 4 * (kBlockSize * 128));
-        for (int jj = 0; jj < 4; ++jj) {
-            if (ids[jj] < 0) continue;
-            const int row = (ids[jj] * p.Hkv + kvh) * kBlockSize;
-            const uint32_t o = jj * (kBlockSize * 128);
-            tma_load_2d(dst + o, &tmk, 0, row, bar);
-            tma_load_2d(dst + kPfHalf + o, &tmk, 64, row, bar);
-            tma_load_2d(dst + 2 * kPfHalf + o, &tmv, 0, row, bar);
-            tma_load_2d(dst + 3 * kPfHalf + o, &tmv, 64, row, bar);
-        }
-    };
-    if (tid == 0) {
-        issue(0);
-        if (ntiles > 1) issue(1);
-    }
-
-    constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
-    constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
-    float m = -INFINITY, l = 0.f;
-    int issued_s = 0, issued_o = 0;  // products issued (for the drain on abort)
-    bool failed = false;
-
-    for (int kt = 0; kt < ntiles; ++kt) {
-        const int st = kt & 1;
-        const uint32_t kvs = skv + st * kPfStage;
-        if (!mbar_wait_bounded(full0 + 8 * st, (kt >> 1) & 1)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        const int mask = tile_mask[st];
-        // V rows of keys no row may see (past the context or in a missing block) must be finite:
-        // their weights are 0, and 0 * NaN would poison O. Zero them.
-        {
-            const int r = tid >> 1, half = tid & 1;
-            const int k = kt * kPfK + r;
-            if (k >= n_tile_max || !((mask >> (r >> 4)) & 1)) {
-                uint4* z = reinterpret_cast<uint4*>(smem + kPfOffKV + st * kPfStage + (2 + half) * kPfHalf + r * 128);
+    } else if (warp == kPfMmaWarp) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
+            constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
+            auto issue_s = [&](int x, int t) {  // S_X = Q_X . K_t^T
+                const uint32_t kvs = skv + (t % kPfStages) * kPfStage;
+                const uint32_t qs = sbase + x * kPfQBytes;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t a = sdesc(qs + (ks >> 2) * (kPfQ * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc(kvs + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
+                    umma(tmem + kSCol + 64 * x, a, bd, kIdescS, ks > 0);
+                }
+                umma_commit(s_full(x));
+            };
+            auto issue_pv = [&](int x, int t) {  // O_X += P_X . V_t
+                const uint32_t kvs = skv + (t % kPfStages) * kPfStage;
+                const uint32_t ps = sbase + kPfOffP + x * kPfPBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = sdesc(ps + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc(kvs + 2 * kPfHalf + kk * (16 * 128), kPfHalf, 1024);
+                    umma(tmem + kOCol + 128 * x, a, bd, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = true;
+            auto wait = [&](uint32_t bar, uint32_t par) {
+                if (ok && !mbar_wait_bounded(bar, par)) {
+                    ok = false;
+                    atomicExch(&abort_flag, 1);
+                    flag(p.status, PKV_FLAG_TIMEOUT);
+                }
+                if (ok && aborted(&abort_flag)) ok = false;
+                tc_fence_after();
+                return ok;
+            };
+            if (wait(kv_full(0), 0)) {
+                issue_s(0, 0);
+                if (two) issue_s(1, 0);
+            }
+            for (int t = 0; t < ntiles && ok; ++t) {
+                if (!wait(p_full(0), t & 1)) break;
+                issue_pv(0, t);
+                const bool more = t + 1 < ntiles;
+                if (more) {
+                    if (!wait(kv_full((t + 1) % kPfStages), ((t + 1) / kPfStages) & 1)) break;
+                    issue_s(0, t + 1);
+                }
+                if (two) {
+                    if (!wait(p_full(1), t & 1)) break;
+                    issue_pv(1, t);
+                }
+                umma_commit(kv_empty(t % kPfStages));  // every product that reads stage t is issued
+                if (two && more) issue_s(1, t + 1);
+            }
+            umma_commit(o_done);
+            umma_commit(drain);
+            mbar_wait_bounded(drain, 0);  // every issued product is done before TMEM may go away
+        }
+        __syncwarp();
+    } else if (gx == 0 || two) {
+        // ---------------- softmax of tile gx ----------------
+        const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
+        const uint32_t s_col = tmem + tl + kSCol + 64 * gx, o_col = tmem + tl + kOCol + 128 * gx;
+        unsigned char* ps = smem + kPfOffP + gx * kPfPBytes;
+        const int n_row = row_valid ? first_visible + i : 0;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            // which of the tile's four blocks are present (same test as the producer)
+            int mask = 0;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * t + jj;
+                if (j * kBlockSize < n_tile_max) {
+                    const int v = bt_row[j];
+                    if (v >= 0 && v < p.NB) mask |= 1 << jj;
+                }
+            }
+            if (!mbar_wait_bounded(s_full(gx), t & 1)) {
+                atomicExch(&abort_flag, 1);
+                flag(p.status, PKV_FLAG_TIMEOUT);
+                ok = false;
+            }
+            if (!ok || aborted(&abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            if (gx == 0) {
+                // V rows of keys no row may see (past the context or in a missing block) must be
+                // finite: their weights are 0, and 0 * NaN would poison O. Zero them. (The copy of
+                // tile t has landed: S_A(t) was issued after it.)
+                const int kr = r >> 1, half = r & 1;
+                const int k = t * kPfK + kr;
+                if (k >= n_tile_max || !((mask >> (kr >> 4)) & 1)) {
+                    uint4* z = reinterpret_cast<uint4*>(smem + kPfOffKV + (t % kPfStages) * kPfStage +
+                                                        (2 + half) * kPfHalf + kr * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            float s[64];
+            {
+                float t0[32], t1[32];
+                tmem_ld32(s_col, t0);
+                tmem_ld32(s_col + 32, t1);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) { s[c] = t0[c]; s[32 + c] = t1[c]; }
+            }
+            float mx = -INFINITY;
+            const int kbase = t * kPfK;
+            if (kbase + kPfK <= n_row && mask == 0xF) {  // whole tile visible to this row
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    s[c] *= p.scale_log2;
+                    mx = fmaxf(mx, s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const bool vis = kbase + c < n_row && ((mask >> (c >> 4)) & 1);
+                    s[c] = vis ? s[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[c]);
+                }
+            }
+            const bool up = mx > m + kPfRescale;
+            float alpha = 1.f;
+            if (up) {
+                alpha = ex2(m - mx);  // m == -inf: 0
+                m = mx;
+                l *= alpha;
+            }
+            const float ms = m == -INFINITY ? 0.f : m;
+            if (t > 0 && __any_sync(0xffffffffu, up)) {  // rescale this warp's O rows (rare)
+#pragma unroll 1
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(o_col + c0, o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                    tmem_st32(o_col + c0, o);
+                }
+            }
+            uint32_t pw[32];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float a0 = ex2(s[2 * c] - ms), a1 = ex2(s[2 * c + 1] - ms);
+                lsum += a0 + a1;
+                pw[c] = pack2_bf16(a0, a1);
+            }
+            l += lsum;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = keys 8j .. 8j+7 of row r
+                const uint32_t off = r * 128 + ((j ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4*>(ps + off) = make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(p_full(gx));
         }
-        tc_fence_before();
-        __syncthreads();
+        if (ok && !mbar_wait_bounded(o_done, 0)) {
+            atomicExch(&abort_flag, 1);
+            flag(p.status, PKV_FLAG_TIMEOUT);
+            ok = false;
+        }
         tc_fence_after();
-        if (tid == 0) {  // S = Q . K^T
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = sdesc(sq + (ks >> 2) * (kPfQ * 128) + (ks & 3) * 32, 16, 1024);
-                const uint64_t bd = sdesc(kvs + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
-                umma(tmem + kSCol, a, bd, kIdescS, ks > 0);
-            }
-            umma_commit(bar_s);
-        }
-        ++issued_s;
-        if (!mbar_wait_bounded(bar_s, kt & 1)) failed = true;
-        tc_fence_after();
-        float s[64];
-        {
-            float t0[32], t1[32];
-            tmem_ld32(tmem + tlane + kSCol, t0);
-            tmem_ld32(tmem + tlane + kSCol + 32, t1);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) { s[c] = t0[c]; s[32 + c] = t1[c]; }
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const int k = kt * kPfK + c;
-            const bool ok = k < n_row && ((mask >> (c >> 4)) & 1);
-            s[c] = ok ? s[c] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, s[c]);
-        }
-        const bool up = mx > m + kPfRescale;
-        float alpha = 1.f;
-        if (up) {
-            alpha = ex2(m - mx);  // m == -inf: 0
-            m = mx;
-            l *= alpha;
-        }
-        const float ms = m == -INFINITY ? 0.f : m;
-        // the previous P . V must be done before P, O or its stage are touched again
-        if (kt > 0) {
-            if (!mbar_wait_bounded(bar_o, (kt - 1) & 1)) failed = true;
-            tc_fence_after();
-            if (tid == 0 && kt + 1 < ntiles && !failed) issue(kt + 1);
-        }
-        uint32_t pw[32];
-        float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float a0 = ex2(s[2 * c] - ms), a1 = ex2(s[2 * c + 1] - ms);
-            lsum += a0 + a1;
-            pw[c] = pack2_bf16(a0, a1);
-        }
-        l += lsum;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = keys 8j .. 8j+7 of row tid
-            const uint32_t off = kPfOffP + tid * 128 + ((j ^ (tid & 7)) << 4);
-            *reinterpret_cast<uint4*>(smem + off) = make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-        }
-        if (kt > 0 && __any_sync(0xffffffffu, up)) {  // rescale this warp's O rows (rare)
+        if (ok && !aborted(&abort_flag)) {
+            // ---- epilogue: row r of O / l -> out ----
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int h = kvh * p.G + 2 * hp + gx;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                  ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128);
 #pragma unroll 1
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 float o[32];
-                tmem_ld32(tmem + tlane + kOCol + c0, o);
+                tmem_ld32(o_col + c0, o);
+                if (row_valid) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] *= alpha;
-                tmem_st32(tmem + tlane + kOCol + c0, o);
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        if (__syncthreads_or(failed)) break;
-        tc_fence_after();
-        if (tid == 0) {  // O += P . V
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = sdesc(sp + kk * 32, 16, 1024);
-                const uint64_t bd = sdesc(kvs + 2 * kPfHalf + kk * (16 * 128), kPfHalf, 1024);
-                umma(tmem + kOCol, a, bd, kIdescO, (kt > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(bar_o);
-        }
-        ++issued_o;
-    }
-
-    if (!failed && issued_o > 0 && !mbar_wait_bounded(bar_o, (issued_o - 1) & 1)) failed = true;
-    tc_fence_after();
-    if (__syncthreads_or(failed)) {
-        if (tid == 0) {
-            atomicExch(&abort_flag, 1);
-            flag(p.status, PKV_FLAG_TIMEOUT);
-            // let in-flight products and copies finish before TMEM and shared memory go away
-            if (issued_s > 0) mbar_wait_bounded(bar_s, (issued_s - 1) & 1);
-            if (issued_o > 0) mbar_wait_bounded(bar_o, (issued_o - 1) & 1);
-            for (int kt = 0; kt < ntiles && kt < 2 + issued_o; ++kt) mbar_wait_bounded(full0 + 8 * (kt & 1), (kt >> 1) & 1);
-        }
-    } else {
-        // ---- epilogue: row tid of O / l -> out ----
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                              ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128);
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-            float o[32];
-            tmem_ld32(tmem + tlane + kOCol + c0, o);
-            if (row_valid) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    dst[c0 / 8 + c] = make_uint4(pack2_bf16(o[8 * c] * inv, o[8 * c + 1] * inv),
-                                                 pack2_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                                 pack2_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                                                 pack2_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                    for (int c = 0; c < 4; ++c)
+                        dst[c0 / 8 + c] = make_uint4(pack2_bf16(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                                     pack2_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                                     pack2_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                                     pack2_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kPfMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPfTmemCols)
                      : "memory");
@@ -372,8 +458,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const 
                            int max_query_len, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hq, p.B);
-    return launch_pdl(prefill_kernel, grid, dim3(128), kPfSmem, s, p, tk, tv);
+    const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hkv * ((p.G + 1) / 2), p.B);
+    return launch_pdl(prefill_kernel, grid, dim3(kPfThreads), kPfSmem, s, p, tk, tv);
 }
 
 }  // namespace pkv

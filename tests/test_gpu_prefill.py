@@ -27,7 +27,7 @@ def run_prefill(w, status=None, bt=None):
     return to_f64(out)
 
 
-@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2)])
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2), (6, 2), (4, 2)])
 def test_prefill_matches_oracle(hq, hkv):
     w = W.make_prefill(name="pf", query_lens=[1, 5, 127, 128, 129, 300],
                        cached_lens=[0, 17, 64, 200, 5, 1000], Hq=hq, Hkv=hkv, D=128, seed=hq + hkv)
