@@ -39,21 +39,23 @@ constexpr int kPfPBytes = kPfQ * 128;          // P: [128 rows x 64 keys] bf16
 constexpr int kPfHalf = kPfK * 128;            // one 64-dim half of a K or V tile
 constexpr int kPfStage = 4 * kPfHalf;          // K half 0, K half 1, V half 0, V half 1
 #ifndef PKV_PF_STAGES
-#define PKV_PF_STAGES 2
+#define PKV_PF_STAGES 4
 #endif
 constexpr int kPfStages = PKV_PF_STAGES;
 constexpr int kPfOffP = 2 * kPfQBytes;         // Q_A, Q_B, then P_A, P_B
 constexpr int kPfOffKV = kPfOffP + 2 * kPfPBytes;
 constexpr int kPfOffBar = kPfOffKV + kPfStages * kPfStage;
-// barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, drain; then the TMEM slot
-constexpr int kPfNumBars = 2 * kPfStages + 6;
+// barriers: kv_full[S], kv_empty[S], s_full[2 tiles][2 buffers], p_full[2], pv_done[2], o_done,
+// drain; then the TMEM slot
+constexpr int kPfNumBars = 2 * kPfStages + 10;
 constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
 constexpr int kPfThreads = 320;
 constexpr int kPfMmaWarp = 8, kPfLoadWarp = 9;
 constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kOCol = 0, kSCol = 256;     // O_X at 128 X, S_X at 256 + 64 X
+constexpr uint32_t kOCol = 0, kSCol = 256;     // O_X at 128 X, S_X buffer u at 256 + 128 X + 64 u
 constexpr float kPfRescale = 8.0f;             // log2 units
 static_assert(kPfSmem <= 227 * 1024, "shared memory");
+static_assert(kPfStages >= 3, "S of tile t + 2 is computed while tile t still holds its stage");
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading / stride byte offsets,
 // descriptor version 1, 128-byte swizzle.
@@ -127,6 +129,8 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 
 __device__ __forceinline__ bool aborted(const volatile int* f) { return *f != 0; }
 
+__device__ __forceinline__ int lane_of() { return threadIdx.x & 31; }
+
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillParams p,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
@@ -150,6 +154,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     const int n_tile_max = first_visible + qt * kPfQ + rows - 1;  // keys visible to the last row
     const int ntiles = (n_tile_max + kPfK - 1) / kPfK;
     const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS;
+    // Block ids come in windows of 32 (8 key tiles), lane j holding block 32 w + j (-1: not needed
+    // or invalid), the next window loaded while the current one is used.
+    auto load_window = [&](int w, bool report) {
+        const int j = 32 * w + lane_of();
+        int id = -1;
+        if (j * kBlockSize < n_tile_max) {
+            const int v = bt_row[j];
+            if (v >= 0 && v < p.NB) id = v;
+            else if (report) flag(p.status, PKV_FLAG_BAD_BLOCK);
+        }
+        return id;
+    };
+    auto has_window = [&](int w) { return 32 * w * kBlockSize < n_tile_max; };
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -159,10 +176,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     const uint32_t bar0 = sbase + kPfOffBar;
     auto kv_full = [&](int s) { return bar0 + 8 * s; };
     auto kv_empty = [&](int s) { return bar0 + 8 * (kPfStages + s); };
-    auto s_full = [&](int x) { return bar0 + 8 * (2 * kPfStages + x); };
-    auto p_full = [&](int x) { return bar0 + 8 * (2 * kPfStages + 2 + x); };
-    const uint32_t o_done = bar0 + 8 * (2 * kPfStages + 4);
-    const uint32_t drain = bar0 + 8 * (2 * kPfStages + 5);
+    auto s_full = [&](int x, int u) { return bar0 + 8 * (2 * kPfStages + 2 * x + u); };
+    auto p_full = [&](int x) { return bar0 + 8 * (2 * kPfStages + 4 + x); };
+    auto pv_done = [&](int x) { return bar0 + 8 * (2 * kPfStages + 6 + x); };
+    const uint32_t o_done = bar0 + 8 * (2 * kPfStages + 8);
+    const uint32_t drain = bar0 + 8 * (2 * kPfStages + 9);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + kPfNumBars * 8);
     __shared__ int abort_flag;
 
@@ -172,8 +190,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             mbar_init(kv_empty(s), 1);
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(s_full(x), 1);
+            mbar_init(s_full(x, 0), 1);
+            mbar_init(s_full(x, 1), 1);
             mbar_init(p_full(x), kPfQ);
+            mbar_init(pv_done(x), 1);
         }
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
@@ -213,23 +233,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     if (warp == kPfLoadWarp) {
         // ---------------- producer ----------------
         int issued = 0;
+        int ids_cur = load_window(0, true), ids_next = has_window(1) ? load_window(1, true) : -1;
         for (int t = 0; t < ntiles; ++t) {
             const int st = t % kPfStages;
-            if (t >= kPfStages && !mbar_wait_bounded(kv_empty(st), ((t / kPfStages) - 1) & 1, 200)) {
+            if (t > 0 && (t & 7) == 0) {
+                ids_cur = ids_next;
+                ids_next = has_window((t >> 3) + 1) ? load_window((t >> 3) + 1, true) : -1;
+            }
+            const bool got = t < kPfStages || mbar_wait_bounded(kv_empty(st), ((t / kPfStages) - 1) & 1, 200);
+            if (!__all_sync(0xffffffffu, got)) {  // warp-uniform exit
                 if (lane == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
                 break;
             }
-            if (aborted(&abort_flag)) break;
+            if (__any_sync(0xffffffffu, aborted(&abort_flag))) break;
             // lane jj < 4: the pool block of keys 64t + 16jj .. (-1 when not needed or invalid)
-            int id = -1;
-            if (lane < 4) {
-                const int j = 4 * t + lane;
-                if (j * kBlockSize < n_tile_max) {
-                    const int v = bt_row[j];
-                    if (v >= 0 && v < p.NB) id = v;
-                    else flag(p.status, PKV_FLAG_BAD_BLOCK);
-                }
-            }
+            int id = __shfl_sync(0xffffffffu, ids_cur, 4 * (t & 7) + (lane & 3));
+            if (lane >= 4) id = -1;
             const unsigned valid = __ballot_sync(0xffffffffu, id >= 0);
             if (lane == 0) {
                 const uint32_t bar = kv_full(st);
@@ -261,16 +280,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
             constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
-            auto issue_s = [&](int x, int t) {  // S_X = Q_X . K_t^T
+            auto issue_s = [&](int x, int t) {  // S_X(t) = Q_X . K_t^T into buffer t % 2
                 const uint32_t kvs = skv + (t % kPfStages) * kPfStage;
                 const uint32_t qs = sbase + x * kPfQBytes;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t a = sdesc(qs + (ks >> 2) * (kPfQ * 128) + (ks & 3) * 32, 16, 1024);
                     const uint64_t bd = sdesc(kvs + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
-                    umma(tmem + kSCol + 64 * x, a, bd, kIdescS, ks > 0);
+                    umma(tmem + kSCol + 128 * x + 64 * (t & 1), a, bd, kIdescS, ks > 0);
                 }
-                umma_commit(s_full(x));
+                umma_commit(s_full(x, t & 1));
             };
             auto issue_pv = [&](int x, int t) {  // O_X += P_X . V_t
                 const uint32_t kvs = skv + (t % kPfStages) * kPfStage;
@@ -293,24 +312,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 tc_fence_after();
                 return ok;
             };
-            if (wait(kv_full(0), 0)) {
-                issue_s(0, 0);
-                if (two) issue_s(1, 0);
+            // S of the first two tiles, then per tile t: the products of t once its P is ready, and
+            // S of tile t + 2 into the buffer tile t has just released
+            for (int t = 0; t < 2 && t < ntiles && ok; ++t) {
+                if (!wait(kv_full(t % kPfStages), (t / kPfStages) & 1)) break;
+                issue_s(0, t);
+                if (two) issue_s(1, t);
             }
             for (int t = 0; t < ntiles && ok; ++t) {
                 if (!wait(p_full(0), t & 1)) break;
                 issue_pv(0, t);
-                const bool more = t + 1 < ntiles;
-                if (more) {
-                    if (!wait(kv_full((t + 1) % kPfStages), ((t + 1) / kPfStages) & 1)) break;
-                    issue_s(0, t + 1);
-                }
+                umma_commit(pv_done(0));
                 if (two) {
                     if (!wait(p_full(1), t & 1)) break;
                     issue_pv(1, t);
+                    umma_commit(pv_done(1));
                 }
                 umma_commit(kv_empty(t % kPfStages));  // every product that reads stage t is issued
-                if (two && more) issue_s(1, t + 1);
+                if (t + 2 < ntiles) {  // the S buffers tile t used are free (its P is written)
+                    if (!wait(kv_full((t + 2) % kPfStages), ((t + 2) / kPfStages) & 1)) break;
+                    issue_s(0, t + 2);
+                    if (two) issue_s(1, t + 2);
+                }
             }
             umma_commit(o_done);
             umma_commit(drain);
@@ -320,28 +343,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     } else if (gx == 0 || two) {
         // ---------------- softmax of tile gx ----------------
         const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
-        const uint32_t s_col = tmem + tl + kSCol + 64 * gx, o_col = tmem + tl + kOCol + 128 * gx;
+        const uint32_t s_col = tmem + tl + kSCol + 128 * gx, o_col = tmem + tl + kOCol + 128 * gx;
         unsigned char* ps = smem + kPfOffP + gx * kPfPBytes;
         const int n_row = row_valid ? first_visible + i : 0;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        // bit j of `present`: block 32 w + j of the current window is present (the producer's test)
+        unsigned present = __ballot_sync(0xffffffffu, load_window(0, false) >= 0);
+        int ids_next = has_window(1) ? load_window(1, false) : -1;
         for (int t = 0; t < ntiles; ++t) {
-            // which of the tile's four blocks are present (same test as the producer)
-            int mask = 0;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = 4 * t + jj;
-                if (j * kBlockSize < n_tile_max) {
-                    const int v = bt_row[j];
-                    if (v >= 0 && v < p.NB) mask |= 1 << jj;
-                }
+            if (t > 0 && (t & 7) == 0) {
+                present = __ballot_sync(0xffffffffu, ids_next >= 0);
+                ids_next = has_window((t >> 3) + 1) ? load_window((t >> 3) + 1, false) : -1;
             }
-            if (!mbar_wait_bounded(s_full(gx), t & 1)) {
+            const int mask = (present >> (4 * (t & 7))) & 0xF;
+            const bool got = mbar_wait_bounded(s_full(gx, t & 1), (t >> 1) & 1);
+            if (!__all_sync(0xffffffffu, got)) {  // warp-uniform exit
                 atomicExch(&abort_flag, 1);
                 flag(p.status, PKV_FLAG_TIMEOUT);
                 ok = false;
+                break;
             }
-            if (!ok || aborted(&abort_flag)) { ok = false; break; }
+            if (__any_sync(0xffffffffu, aborted(&abort_flag))) { ok = false; break; }
             tc_fence_after();
             if (gx == 0) {
                 // V rows of keys no row may see (past the context or in a missing block) must be
@@ -359,27 +382,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             float s[64];
             {
                 float t0[32], t1[32];
-                tmem_ld32(s_col, t0);
-                tmem_ld32(s_col + 32, t1);
+                tmem_ld32(s_col + 64 * (t & 1), t0);
+                tmem_ld32(s_col + 64 * (t & 1) + 32, t1);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) { s[c] = t0[c]; s[32 + c] = t1[c]; }
             }
-            float mx = -INFINITY;
             const int kbase = t * kPfK;
             if (kbase + kPfK <= n_row && mask == 0xF) {  // whole tile visible to this row
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    s[c] *= p.scale_log2;
-                    mx = fmaxf(mx, s[c]);
-                }
+                for (int c = 0; c < 64; ++c) s[c] *= p.scale_log2;
             } else {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const bool vis = kbase + c < n_row && ((mask >> (c >> 4)) & 1);
                     s[c] = vis ? s[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[c]);
                 }
             }
+            float mx8[8];  // tree maximum: 8 independent chains, then 3 levels
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int e = 0; e < w; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w]);
+            const float mx = mx8[0];
             const bool up = mx > m + kPfRescale;
             float alpha = 1.f;
             if (up) {
@@ -388,7 +416,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 l *= alpha;
             }
             const float ms = m == -INFINITY ? 0.f : m;
+            // P_X and O_X may be touched once the previous tile's product is done
+            bool pv_ready = t == 0;
+            auto wait_pv = [&]() {
+                if (!pv_ready) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done(gx), (t - 1) & 1))) {
+                        atomicExch(&abort_flag, 1);
+                        flag(p.status, PKV_FLAG_TIMEOUT);
+                        ok = false;
+                    }
+                    tc_fence_after();
+                    pv_ready = true;
+                }
+            };
             if (t > 0 && __any_sync(0xffffffffu, up)) {  // rescale this warp's O rows (rare)
+                wait_pv();
+                if (!ok) break;
 #pragma unroll 1
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     float o[32];
@@ -399,14 +442,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 }
             }
             uint32_t pw[32];
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float a0 = ex2(s[2 * c] - ms), a1 = ex2(s[2 * c + 1] - ms);
-                lsum += a0 + a1;
+                ls[c & 3] += a0 + a1;
                 pw[c] = pack2_bf16(a0, a1);
             }
-            l += lsum;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            wait_pv();
+            if (!ok) break;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = keys 8j .. 8j+7 of row r
                 const uint32_t off = r * 128 + ((j ^ (r & 7)) << 4);
@@ -416,13 +461,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             tc_fence_before();
             mbar_arrive(p_full(gx));
         }
-        if (ok && !mbar_wait_bounded(o_done, 0)) {
+        if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(o_done, 0))) {
             atomicExch(&abort_flag, 1);
             flag(p.status, PKV_FLAG_TIMEOUT);
             ok = false;
         }
         tc_fence_after();
-        if (ok && !aborted(&abort_flag)) {
+        if (ok && !__any_sync(0xffffffffu, aborted(&abort_flag))) {
             // ---- epilogue: row r of O / l -> out ----
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int h = kvh * p.G + 2 * hp + gx;
