@@ -7,23 +7,28 @@
 // Sequence b's L_b query tokens are the last L_b of its context (written to the cache first);
 // query row i attends causally to the first n_b - (L_b - 1 - i) tokens.
 //
-// One CTA computes the same 128 query rows for two query heads of one GQA group (tiles A and B):
-// both read every K/V tile once and have the same causal extent, so their work stays in step.
+// One CTA computes 128 query rows of one query head against 128-key tiles. Both products read
+// their A operand from tensor memory: measured on GB300, a tcgen05.mma (M = 128, K = 16) with A in
+// TMEM takes ~82 cycles at N = 128 (the tensor peak), while with A in shared memory it takes
+// ~142 cycles at N = 64 or 128 and reaches the peak only at N = 256. TMEM columns:
+//   O   0-127     fp32 accumulator, row r in lane r
+//   Q   128-191   the CTA's 128 query rows, two bf16 dims per column (written once)
+//   S   256-383 (buffer 0), 384-511 (buffer 1): S = Q . K^T of one key tile, fp32; the softmax
+//       writes that tile's bf16 weights P over the first 32 columns of each 64-column half
 // Warp roles (320 threads):
-//   warps 0-3  softmax of tile A: thread r owns query row r (TMEM lane r)
-//   warps 4-7  softmax of tile B
+//   warps 0-7  softmax. Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows); warps 0-3 take
+//              keys 0-63 of every tile, warps 4-7 keys 64-127. The two threads of a row swap
+//              their maxima through shared memory each tile and their sums at the end.
 //   warp 8     lane 0 issues every tcgen05.mma and commit; the warp owns the TMEM allocation
-//   warp 9     producer: block ids from the table, 2-D TMA copies of 64-key K/V tiles (four pool
-//              blocks) into a STAGES-deep ring
-// Per key tile t, the tensor core runs, in this order,
-//   PV_A(t-1 -> t): O_A += P_A . V_t ;  S_A(t+1) = Q_A . K_{t+1}^T ;  O_B += P_B . V_t ;
-//   S_B(t+1) = Q_B . K_{t+1}^T
-// so that while one tile's softmax warps turn S into P, the tensor core works on the other tile.
-// TMEM columns: O_A 0-127, O_B 128-255, S_A 256-319, S_B 320-383. A commit after S_X(t+1) also
-// covers PV_X(t) (commits track every earlier MMA of the issuing thread), so when softmax X sees
-// S_X(t+1) it may overwrite P_X and rescale O_X. The running max is raised lazily (only when a
-// tile exceeds it by more than 2^8), so O is rarely rescaled; at the end thread r divides its O
-// row by its sum.
+//   warps 9-10 producers: block ids from the table, 2-D TMA copies of the 8 pool blocks of a key
+//              tile (128-byte swizzle), K by warp 9 into one ring, V by warp 10 into another. A
+//              K slot is free once S of its tile is done, so K runs well ahead of V.
+// Per key tile t the tensor core runs O += P(t) . V(t) once P(t) is written, then
+// S(t+2) = Q . K(t+2)^T into the buffer tile t used, so the softmax of tile t+1 overlaps both.
+// S and P are double-buffered with one barrier per buffer, so no barrier completes a phase its
+// waiter has not yet seen (a parity wait would miss it). The running max is raised lazily (only
+// when a tile exceeds it by more than 2^8), so O is rarely rescaled; at the end each row is
+// divided by its sum.
 #include <cuda.h>
 
 #include "pkv_device.cuh"
@@ -32,27 +37,29 @@ namespace pkv {
 
 namespace {
 
-constexpr int kPfQ = 128;                      // query rows per tile (MMA M)
-constexpr int kPfK = 64;                       // keys per tile
-constexpr int kPfQBytes = 2 * kPfQ * 128;      // Q: two 64-dim halves of [128 rows x 128 B]
-constexpr int kPfPBytes = kPfQ * 128;          // P: [128 rows x 64 keys] bf16
-constexpr int kPfHalf = kPfK * 128;            // one 64-dim half of a K or V tile
-constexpr int kPfStage = 4 * kPfHalf;          // K half 0, K half 1, V half 0, V half 1
+constexpr int kPfQ = 128;                      // query rows per CTA (MMA M)
+constexpr int kPfK = 128;                      // keys per tile (MMA N of S, K of PV)
+constexpr int kPfHalf = kPfK * 128;            // one 64-dim half of a K or V tile: [128 keys x 128 B]
+constexpr int kPfStage = 2 * kPfHalf;          // one K (or V) tile: dims 0-63, then dims 64-127
 #ifndef PKV_PF_STAGES
-#define PKV_PF_STAGES 4
+#define PKV_PF_STAGES 3                        // slots per ring (K and V each)
+#endif
+#ifndef PKV_PF_WAR_GUARD
+#define PKV_PF_WAR_GUARD 0
 #endif
 constexpr int kPfStages = PKV_PF_STAGES;
-constexpr int kPfOffP = 2 * kPfQBytes;         // Q_A, Q_B, then P_A, P_B
-constexpr int kPfOffKV = kPfOffP + 2 * kPfPBytes;
-constexpr int kPfOffBar = kPfOffKV + kPfStages * kPfStage;
-// barriers: kv_full[S], kv_empty[S], s_full[2 tiles][2 buffers], p_full[2], pv_done[2], o_done,
-// drain; then the TMEM slot
-constexpr int kPfNumBars = 2 * kPfStages + 10;
+constexpr int kPfOffK = 0;
+constexpr int kPfOffV = kPfStages * kPfStage;
+constexpr int kPfOffX = 2 * kPfStages * kPfStage;  // row maxima [2][2][128] and sums [2][128], fp32
+constexpr int kPfOffBar = kPfOffX + 6 * kPfQ * 4;
+// barriers: full[2 rings][S], empty[2 rings][S], s_full[2], p_full[2], pv_done, o_done, drain;
+// then the TMEM slot
+constexpr int kPfNumBars = 4 * kPfStages + 7;
 constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
-constexpr int kPfThreads = 320;
-constexpr int kPfMmaWarp = 8, kPfLoadWarp = 9;
+constexpr int kPfThreads = 352;
+constexpr int kPfMmaWarp = 8, kPfLoadWarpK = 9, kPfLoadWarpV = 10;
 constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kOCol = 0, kSCol = 256;     // O_X at 128 X, S_X buffer u at 256 + 128 X + 64 u
+constexpr uint32_t kOCol = 0, kQCol = 128, kSCol = 256;
 constexpr float kPfRescale = 8.0f;             // log2 units
 static_assert(kPfSmem <= 227 * 1024, "shared memory");
 static_assert(kPfStages >= 3, "S of tile t + 2 is computed while tile t still holds its stage");
@@ -71,11 +78,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// tcgen05.mma with A read from tensor memory (128 lanes = rows, two 16-bit K elements per
+// 32-bit column in order, K = 16 in 8 columns).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -122,6 +131,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -131,22 +152,37 @@ __device__ __forceinline__ bool aborted(const volatile int* f) { return *f != 0;
 
 __device__ __forceinline__ int lane_of() { return threadIdx.x & 31; }
 
+// bar.sync on named barrier `id` for `count` threads (whole warps)
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// OR of `pred` over the `count` threads (whole warps) of named barrier `id`
+__device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
+    int res;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(res)
+        : "r"((int)pred), "r"(id), "r"(count)
+        : "memory");
+    return res != 0;
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillParams p,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
     grid_dependency_wait();
     // heaviest query tiles (most keys under the causal mask) first
-    const int qt = gridDim.x - 1 - blockIdx.x, b = blockIdx.z;
-    const int HP = (p.G + 1) / 2;                       // head pairs per kv head
-    const int kvh = blockIdx.y / HP, hp = blockIdx.y - kvh * HP;
-    const bool two = 2 * hp + 1 < p.G;                  // tile B exists
+    const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int kvh = h / p.G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q0 = p.query_start[b];
     const int L = p.query_start[b + 1] - q0;
     if (qt * kPfQ >= L) return;
     const int n = p.context_lens[b];
     if (n < L || n > p.MBPS * kBlockSize) {
-        if (tid == 0 && qt == 0 && blockIdx.y == 0) flag(p.status, PKV_FLAG_BAD_CONTEXT);
+        if (tid == 0 && qt == 0 && h == 0) flag(p.status, PKV_FLAG_BAD_CONTEXT);
         return;
     }
     const int first_visible = n - L + 1;                          // keys visible to query row 0
@@ -154,7 +190,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     const int n_tile_max = first_visible + qt * kPfQ + rows - 1;  // keys visible to the last row
     const int ntiles = (n_tile_max + kPfK - 1) / kPfK;
     const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS;
-    // Block ids come in windows of 32 (8 key tiles), lane j holding block 32 w + j (-1: not needed
+    // Block ids come in windows of 32 (4 key tiles), lane j holding block 32 w + j (-1: not needed
     // or invalid), the next window loaded while the current one is used.
     auto load_window = [&](int w, bool report) {
         const int j = 32 * w + lane_of();
@@ -172,29 +208,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t skv = sbase + kPfOffKV;
+    float* xmax = reinterpret_cast<float*>(smem + kPfOffX);  // [2 buffers][2 halves][128 rows]
+    float* xsum = xmax + 4 * kPfQ;                           // [2 halves][128 rows]
     const uint32_t bar0 = sbase + kPfOffBar;
-    auto kv_full = [&](int s) { return bar0 + 8 * s; };
-    auto kv_empty = [&](int s) { return bar0 + 8 * (kPfStages + s); };
-    auto s_full = [&](int x, int u) { return bar0 + 8 * (2 * kPfStages + 2 * x + u); };
-    auto p_full = [&](int x) { return bar0 + 8 * (2 * kPfStages + 4 + x); };
-    auto pv_done = [&](int x) { return bar0 + 8 * (2 * kPfStages + 6 + x); };
-    const uint32_t o_done = bar0 + 8 * (2 * kPfStages + 8);
-    const uint32_t drain = bar0 + 8 * (2 * kPfStages + 9);
+    // ring g (0: K, 1: V): slot s of tile t is t % S
+    auto full = [&](int g, int s) { return bar0 + 8 * (g * kPfStages + s); };
+    auto empty = [&](int g, int s) { return bar0 + 8 * (2 * kPfStages + g * kPfStages + s); };
+    auto slot = [&](int g, int t) { return sbase + (g ? kPfOffV : kPfOffK) + (t % kPfStages) * kPfStage; };
+    auto s_full = [&](int u) { return bar0 + 8 * (4 * kPfStages + u); };
+    auto p_full = [&](int u) { return bar0 + 8 * (4 * kPfStages + 2 + u); };
+    const uint32_t pv_done = bar0 + 8 * (4 * kPfStages + 4);
+    const uint32_t o_done = bar0 + 8 * (4 * kPfStages + 5);
+    const uint32_t drain = bar0 + 8 * (4 * kPfStages + 6);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + kPfNumBars * 8);
     __shared__ int abort_flag;
 
     if (tid == 0) {
-        for (int s = 0; s < kPfStages; ++s) {
-            mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+        for (int g = 0; g < 2; ++g)
+            for (int s = 0; s < kPfStages; ++s) {
+                mbar_init(full(g, s), 1);
+                mbar_init(empty(g, s), 1);
+            }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(s_full(u), 1);
+            mbar_init(p_full(u), 2 * kPfQ);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(s_full(x, 0), 1);
-            mbar_init(s_full(x, 1), 1);
-            mbar_init(p_full(x), kPfQ);
-            mbar_init(pv_done(x), 1);
-        }
+        mbar_init(pv_done, 1);
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
         abort_flag = 0;
@@ -206,100 +245,100 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-
-    // ---- Q tiles: softmax thread r of tile X writes query row r (zeros past the sequence's queries) ----
-    const int gx = warp >> 2;              // softmax group (tile) of warps 0-7
-    const int r = tid & 127;               // its row / TMEM lane
-    const int i = qt * kPfQ + r;
-    const bool row_valid = i < L;
-    if (warp < 8 && (gx == 0 || two)) {
-        const int h = kvh * p.G + 2 * hp + gx;
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128);
-        unsigned char* qs = smem + gx * kPfQBytes;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = dims 8c .. 8c+7
-            const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t off = (c >> 3) * (kPfQ * 128) + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
-            *reinterpret_cast<uint4*>(qs + off) = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kPfLoadWarp) {
-        // ---------------- producer ----------------
+    // softmax thread (hf, r): row r, keys 64 hf .. 64 hf + 63 of each tile
+    const int hf = (warp >> 2) & 1;
+    const int r = tid & 127;
+    const int i = qt * kPfQ + r;
+    const bool row_valid = i < L;
+    const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
+    if (warp < 8) {
+        // Q row r, dims 64 hf .. 64 hf + 63, into TMEM columns 128 + 32 hf .. (zeros past the queries)
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                          ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128 + 64 * hf);
+        uint32_t qw[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+            qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
+        }
+        tmem_st32u(tmem + tl + kQCol + 32 * hf, qw);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp == kPfLoadWarpK || warp == kPfLoadWarpV) {
+        // ---------------- producers: ring g = K (warp 9) or V (warp 10) ----------------
+        const int g = warp - kPfLoadWarpK;
+        const CUtensorMap* map = g ? &tmv : &tmk;
         int issued = 0;
         int ids_cur = load_window(0, true), ids_next = has_window(1) ? load_window(1, true) : -1;
         for (int t = 0; t < ntiles; ++t) {
             const int st = t % kPfStages;
-            if (t > 0 && (t & 7) == 0) {
+            if (t > 0 && (t & 3) == 0) {
                 ids_cur = ids_next;
-                ids_next = has_window((t >> 3) + 1) ? load_window((t >> 3) + 1, true) : -1;
+                ids_next = has_window((t >> 2) + 1) ? load_window((t >> 2) + 1, true) : -1;
             }
-            const bool got = t < kPfStages || mbar_wait_bounded(kv_empty(st), ((t / kPfStages) - 1) & 1, 200);
+            const bool got = t < kPfStages || mbar_wait_bounded(empty(g, st), ((t / kPfStages) - 1) & 1);
             if (!__all_sync(0xffffffffu, got)) {  // warp-uniform exit
                 if (lane == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
                 break;
             }
             if (__any_sync(0xffffffffu, aborted(&abort_flag))) break;
-            // lane jj < 4: the pool block of keys 64t + 16jj .. (-1 when not needed or invalid)
-            int id = __shfl_sync(0xffffffffu, ids_cur, 4 * (t & 7) + (lane & 3));
-            if (lane >= 4) id = -1;
+            // lane jj < 8: the pool block of keys 128 t + 16 jj .. (-1 when not needed or invalid)
+            int id = __shfl_sync(0xffffffffu, ids_cur, 8 * (t & 3) + (lane & 7));
+            if (lane >= 8) id = -1;
             const unsigned valid = __ballot_sync(0xffffffffu, id >= 0);
             if (lane == 0) {
-                const uint32_t bar = kv_full(st);
-                if (valid == 0) {
-                    mbar_arrive(bar);
-                } else {
-                    mbar_arrive_expect_tx(bar, __popc(valid) * 4 * (kBlockSize * 128));
-                }
+                if (valid == 0) mbar_arrive(full(g, st));
+                else mbar_arrive_expect_tx(full(g, st), __popc(valid) * 2 * (kBlockSize * 128));
             }
             __syncwarp();
-            if (lane < 4 && id >= 0) {
-                const uint32_t bar = kv_full(st), dst = skv + st * kPfStage;
+            if (id >= 0) {
+                const uint32_t bar = full(g, st), dst = slot(g, t);
                 const int row = (id * p.Hkv + kvh) * kBlockSize;
                 const uint32_t o = lane * (kBlockSize * 128);
-                tma_load_2d(dst + o, &tmk, 0, row, bar);
-                tma_load_2d(dst + kPfHalf + o, &tmk, 64, row, bar);
-                tma_load_2d(dst + 2 * kPfHalf + o, &tmv, 0, row, bar);
-                tma_load_2d(dst + 3 * kPfHalf + o, &tmv, 64, row, bar);
+                tma_load_2d(dst + o, map, 0, row, bar);
+                tma_load_2d(dst + kPfHalf + o, map, 64, row, bar);
             }
             issued = t + 1;
         }
         if (aborted(&abort_flag) && lane == 0) {
             // let this CTA's own copies land before shared memory goes away
             for (int t = issued - kPfStages < 0 ? 0 : issued - kPfStages; t < issued; ++t)
-                mbar_wait_bounded(kv_full(t % kPfStages), (t / kPfStages) & 1);
+                mbar_wait_bounded(full(g, t % kPfStages), (t / kPfStages) & 1);
         }
     } else if (warp == kPfMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
             constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
-            auto issue_s = [&](int x, int t) {  // S_X(t) = Q_X . K_t^T into buffer t % 2
-                const uint32_t kvs = skv + (t % kPfStages) * kPfStage;
-                const uint32_t qs = sbase + x * kPfQBytes;
+            auto issue_s = [&](int t) {  // S(t) = Q . K(t)^T into buffer t % 2
+                const uint32_t kbase = slot(0, t);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t a = sdesc(qs + (ks >> 2) * (kPfQ * 128) + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc(kvs + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
-                    umma(tmem + kSCol + 128 * x + 64 * (t & 1), a, bd, kIdescS, ks > 0);
+                    const uint64_t bd = sdesc(kbase + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
+                    umma_ts(tmem + kSCol + 128 * (t & 1), tmem + kQCol + 8 * ks, bd, kIdescS, ks > 0);
                 }
-                umma_commit(s_full(x, t & 1));
+                umma_commit(s_full(t & 1));
+                umma_commit(empty(0, t % kPfStages));  // the K slot is free once S(t) is done
             };
-            auto issue_pv = [&](int x, int t) {  // O_X += P_X . V_t
-                const uint32_t kvs = skv + (t % kPfStages) * kPfStage;
-                const uint32_t ps = sbase + kPfOffP + x * kPfPBytes;
+            auto issue_pv = [&](int t) {  // O += P(t) . V(t); P over the first 32 columns of each S half
+                const uint32_t vbase = slot(1, t);
+                const uint32_t pt = tmem + kSCol + 128 * (t & 1);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc(ps + kk * 32, 16, 1024);
-                    const uint64_t bd = sdesc(kvs + 2 * kPfHalf + kk * (16 * 128), kPfHalf, 1024);
-                    umma(tmem + kOCol + 128 * x, a, bd, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bd = sdesc(vbase + kk * (16 * 128), kPfHalf, 1024);
+                    umma_ts(tmem + kOCol, pt + 64 * (kk >> 2) + 8 * (kk & 3), bd, kIdescO,
+                            (t > 0 || kk > 0) ? 1u : 0u);
                 }
+                umma_commit(pv_done);
+                umma_commit(empty(1, t % kPfStages));  // the V slot is free once PV(t) is done
             };
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t par) {
@@ -312,27 +351,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 tc_fence_after();
                 return ok;
             };
-            // S of the first two tiles, then per tile t: the products of t once its P is ready, and
-            // S of tile t + 2 into the buffer tile t has just released
             for (int t = 0; t < 2 && t < ntiles && ok; ++t) {
-                if (!wait(kv_full(t % kPfStages), (t / kPfStages) & 1)) break;
-                issue_s(0, t);
-                if (two) issue_s(1, t);
+                if (!wait(full(0, t % kPfStages), (t / kPfStages) & 1)) break;
+                issue_s(t);
             }
             for (int t = 0; t < ntiles && ok; ++t) {
-                if (!wait(p_full(0), t & 1)) break;
-                issue_pv(0, t);
-                umma_commit(pv_done(0));
-                if (two) {
-                    if (!wait(p_full(1), t & 1)) break;
-                    issue_pv(1, t);
-                    umma_commit(pv_done(1));
-                }
-                umma_commit(kv_empty(t % kPfStages));  // every product that reads stage t is issued
-                if (t + 2 < ntiles) {  // the S buffers tile t used are free (its P is written)
-                    if (!wait(kv_full((t + 2) % kPfStages), ((t + 2) / kPfStages) & 1)) break;
-                    issue_s(0, t + 2);
-                    if (two) issue_s(1, t + 2);
+                if (!wait(p_full(t & 1), (t >> 1) & 1)) break;
+                if (!wait(full(1, t % kPfStages), (t / kPfStages) & 1)) break;
+                issue_pv(t);
+                if (t + 2 < ntiles) {
+#if PKV_PF_WAR_GUARD
+                    if (!wait(pv_done, t & 1)) break;
+#endif
+                    if (!wait(full(0, (t + 2) % kPfStages), ((t + 2) / kPfStages) & 1)) break;
+                    issue_s(t + 2);
                 }
             }
             umma_commit(o_done);
@@ -340,62 +372,69 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             mbar_wait_bounded(drain, 0);  // every issued product is done before TMEM may go away
         }
         __syncwarp();
-    } else if (gx == 0 || two) {
-        // ---------------- softmax of tile gx ----------------
-        const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
-        const uint32_t s_col = tmem + tl + kSCol + 128 * gx, o_col = tmem + tl + kOCol + 128 * gx;
-        unsigned char* ps = smem + kPfOffP + gx * kPfPBytes;
+    } else {
+        // ---------------- softmax: row r, key half hf ----------------
+        const uint32_t s_col = tmem + tl + kSCol + 64 * hf, o_col = tmem + tl + kOCol + 64 * hf;
         const int n_row = row_valid ? first_visible + i : 0;
+        const int pair_bar = 1 + (warp & 3);  // named barrier of warps w and w + 4 (64 threads)
+        // scores are scaled inside the exponents by |scale| * log2 e; a negative scale flips their
+        // sign. |scale| is at least FLT_MIN so a masked score (-inf) never meets a zero factor: a
+        // zero scale still gives weights of exactly 1 (every visible score times FLT_MIN is ~0).
+        const bool neg = p.scale_log2 < 0.f;
+        const float csc = fmaxf(fabsf(p.scale_log2), 1.17549435e-38f);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // bit j of `present`: block 32 w + j of the current window is present (the producer's test)
         unsigned present = __ballot_sync(0xffffffffu, load_window(0, false) >= 0);
         int ids_next = has_window(1) ? load_window(1, false) : -1;
         for (int t = 0; t < ntiles; ++t) {
-            if (t > 0 && (t & 7) == 0) {
+            if (t > 0 && (t & 3) == 0) {
                 present = __ballot_sync(0xffffffffu, ids_next >= 0);
-                ids_next = has_window((t >> 3) + 1) ? load_window((t >> 3) + 1, false) : -1;
+                ids_next = has_window((t >> 2) + 1) ? load_window((t >> 2) + 1, false) : -1;
             }
-            const int mask = (present >> (4 * (t & 7))) & 0xF;
-            const bool got = mbar_wait_bounded(s_full(gx, t & 1), (t >> 1) & 1);
-            if (!__all_sync(0xffffffffu, got)) {  // warp-uniform exit
+            const int mask8 = (present >> (8 * (t & 3))) & 0xFF;
+            const int mask = (mask8 >> (4 * hf)) & 0xF;  // this half's four blocks
+            const int u = t & 1;
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u), (t >> 1) & 1));
+            if (!got) {
                 atomicExch(&abort_flag, 1);
                 flag(p.status, PKV_FLAG_TIMEOUT);
-                ok = false;
-                break;
             }
-            if (__any_sync(0xffffffffu, aborted(&abort_flag))) { ok = false; break; }
+            // both threads of a row take the same exit
+            if (barrier_or(pair_bar, 64, !got || aborted(&abort_flag))) { ok = false; break; }
             tc_fence_after();
-            if (gx == 0) {
+            if ((t + 1) * kPfK > n_tile_max || mask8 != 0xFF) {
                 // V rows of keys no row may see (past the context or in a missing block) must be
-                // finite: their weights are 0, and 0 * NaN would poison O. Zero them. (The copy of
-                // tile t has landed: S_A(t) was issued after it.)
-                const int kr = r >> 1, half = r & 1;
-                const int k = t * kPfK + kr;
-                if (k >= n_tile_max || !((mask >> (kr >> 4)) & 1)) {
-                    uint4* z = reinterpret_cast<uint4*>(smem + kPfOffKV + (t % kPfStages) * kPfStage +
-                                                        (2 + half) * kPfHalf + kr * 128);
+                // finite: their weights are 0, and 0 * NaN would poison O. Zero them once the V
+                // copy of tile t has landed (PV(t) waits for this thread's P, so it reads them
+                // zeroed; the next copy into the slot waits for PV(t)).
+                const int k = tid >> 1, half = tid & 1;  // 256 threads: key k, 64-dim half
+                if (!mbar_wait_bounded(full(1, t % kPfStages), (t / kPfStages) & 1)) {
+                    atomicExch(&abort_flag, 1);
+                    flag(p.status, PKV_FLAG_TIMEOUT);
+                } else if (t * kPfK + k >= n_tile_max || !((mask8 >> (k >> 4)) & 1)) {
+                    uint4* z = reinterpret_cast<uint4*>(smem + kPfOffV + (t % kPfStages) * kPfStage +
+                                                        half * kPfHalf + k * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
             }
             float s[64];
             {
                 float t0[32], t1[32];
-                tmem_ld32(s_col + 64 * (t & 1), t0);
-                tmem_ld32(s_col + 64 * (t & 1) + 32, t1);
+                tmem_ld32(s_col + 128 * u, t0);
+                tmem_ld32(s_col + 128 * u + 32, t1);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) { s[c] = t0[c]; s[32 + c] = t1[c]; }
             }
-            const int kbase = t * kPfK;
-            if (kbase + kPfK <= n_row && mask == 0xF) {  // whole tile visible to this row
-#pragma unroll
-                for (int c = 0; c < 64; ++c) s[c] *= p.scale_log2;
-            } else {
+            // raw scores here; the scale (with log2 e) is applied inside each exponent below
+            const int kbase = t * kPfK + 64 * hf;
+            if (neg || !(kbase + 64 <= n_row && mask == 0xF)) {  // not the whole half visible to this row
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const bool vis = kbase + c < n_row && ((mask >> (c >> 4)) & 1);
-                    s[c] = vis ? s[c] * p.scale_log2 : -INFINITY;
+                    s[c] = vis ? (neg ? -s[c] : s[c]) : -INFINITY;
                 }
             }
             float mx8[8];  // tree maximum: 8 independent chains, then 3 levels
@@ -404,10 +443,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
 #pragma unroll
             for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
 #pragma unroll
-            for (int w = 4; w >= 1; w >>= 1)
+            for (int w2 = 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
-                for (int e = 0; e < w; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w]);
-            const float mx = mx8[0];
+                for (int e = 0; e < w2; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w2]);
+            // the row's maximum over both halves (the same value in both threads), in log2 units
+            xmax[(u * 2 + hf) * kPfQ + r] = mx8[0];
+            named_barrier_sync(pair_bar, 64);
+            const float mx = fmaxf(mx8[0], xmax[(u * 2 + (hf ^ 1)) * kPfQ + r]) * csc;
             const bool up = mx > m + kPfRescale;
             float alpha = 1.f;
             if (up) {
@@ -416,24 +458,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 l *= alpha;
             }
             const float ms = m == -INFINITY ? 0.f : m;
-            // P_X and O_X may be touched once the previous tile's product is done
-            bool pv_ready = t == 0;
-            auto wait_pv = [&]() {
-                if (!pv_ready) {
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done(gx), (t - 1) & 1))) {
-                        atomicExch(&abort_flag, 1);
-                        flag(p.status, PKV_FLAG_TIMEOUT);
-                        ok = false;
-                    }
-                    tc_fence_after();
-                    pv_ready = true;
+            if (t > 0 && __any_sync(0xffffffffu, up)) {
+                // rescale this thread's half of its O row (rare), once PV of tile t - 1 is done
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done, (t - 1) & 1))) {
+                    atomicExch(&abort_flag, 1);
+                    flag(p.status, PKV_FLAG_TIMEOUT);
                 }
-            };
-            if (t > 0 && __any_sync(0xffffffffu, up)) {  // rescale this warp's O rows (rare)
-                wait_pv();
-                if (!ok) break;
+                tc_fence_after();
 #pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
+                for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
                     tmem_ld32(o_col + c0, o);
 #pragma unroll
@@ -445,36 +478,33 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float a0 = ex2(s[2 * c] - ms), a1 = ex2(s[2 * c + 1] - ms);
+                const float a0 = ex2(fmaf(s[2 * c], csc, -ms)), a1 = ex2(fmaf(s[2 * c + 1], csc, -ms));
                 ls[c & 3] += a0 + a1;
                 pw[c] = pack2_bf16(a0, a1);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            wait_pv();
-            if (!ok) break;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = keys 8j .. 8j+7 of row r
-                const uint32_t off = r * 128 + ((j ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(ps + off) = make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // P over the first 32 columns of this half of the S buffer just read (the product
+            // that last read those columns, PV of tile t - 2, finished before S(t) was written)
+            tmem_st32u(s_col + 128 * u, pw);
             tc_fence_before();
-            mbar_arrive(p_full(gx));
+            mbar_arrive(p_full(u));
         }
         if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(o_done, 0))) {
             atomicExch(&abort_flag, 1);
             flag(p.status, PKV_FLAG_TIMEOUT);
-            ok = false;
         }
         tc_fence_after();
-        if (ok && !__any_sync(0xffffffffu, aborted(&abort_flag))) {
-            // ---- epilogue: row r of O / l -> out ----
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int h = kvh * p.G + 2 * hp + gx;
+        // the row's sum over both halves; both threads of the row decide together
+        xsum[hf * kPfQ + r] = l;
+        const bool fail = barrier_or(pair_bar, 64, !ok || aborted(&abort_flag));
+        const float lt = l + xsum[(hf ^ 1) * kPfQ + r];
+        if (!fail) {
+            // ---- epilogue: dims 64 hf .. 64 hf + 63 of row r of O / l -> out ----
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                  ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128);
+                                                  ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128 + 64 * hf);
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 float o[32];
                 tmem_ld32(o_col + c0, o);
                 if (row_valid) {
@@ -503,7 +533,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const 
                            int max_query_len, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hkv * ((p.G + 1) / 2), p.B);
+    const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hq, p.B);
     return launch_pdl(prefill_kernel, grid, dim3(kPfThreads), kPfSmem, s, p, tk, tv);
 }
 

@@ -72,3 +72,19 @@ def test_prefill_missing_block_is_skipped_and_flagged():
                                          w.query_start, w.scale)
     s1 = slice(w.query_start[1], w.query_start[2])
     assert_close(got[s1], ref[s1], "bf16", "untouched sequence")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 2.0, 0.0])
+def test_prefill_scale_sign_and_running_max_rescale(scale):
+    """A negative scale flips which key dominates; a large one makes the running maximum jump by
+    far more than the kernel's lazy-rescale margin across key tiles (the O rescale path); zero
+    gives uniform weights over the visible keys."""
+    w = W.make_prefill(name="pfs", query_lens=[300, 129], cached_lens=[700, 0], Hq=8, Hkv=2,
+                       D=128, seed=17)
+    w.scale = scale
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill(w, st)
+    ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                         w.query_start, w.scale)
+    assert_close(got, ref, "bf16", f"prefill scale={scale}")
+    assert int(st.item()) == 0
