@@ -13,20 +13,25 @@
 // ~142 cycles at N = 64 or 128 and reaches the peak only at N = 256. TMEM columns:
 //   O   0-127     fp32 accumulator, row r in lane r
 //   Q   128-191   the CTA's 128 query rows, two bf16 dims per column (written once)
-//   S   256-383 (buffer 0), 384-511 (buffer 1): S = Q . K^T of one key tile, fp32; the softmax
-//       writes that tile's bf16 weights P over the first 32 columns of each 64-column half
+//   P   192-255 (buffer 0), 256-319 (buffer 1): bf16 weights of a key tile, two keys per column
+//   S   320-447   S = Q . K^T of one key tile, fp32
 // Warp roles (320 threads):
 //   warps 0-7  softmax. Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows); warps 0-3 take
 //              keys 0-63 of every tile, warps 4-7 keys 64-127. The two threads of a row swap
 //              their maxima through shared memory each tile and their sums at the end.
-//   warp 8     lane 0 issues every tcgen05.mma and commit; the warp owns the TMEM allocation
+//   warp 8     lane 0 issues the S products (and their commits); the warp owns the TMEM allocation
+//   warp 11    lane 0 issues the PV products. Two issuers, because a thread that has just issued a
+//              batch of products takes several hundred cycles to notice its next barrier, and
+//              the S and PV streams depend on each other only through the softmax.
 //   warps 9-10 producers: block ids from the table, 2-D TMA copies of the 8 pool blocks of a key
 //              tile (128-byte swizzle), K by warp 9 into one ring, V by warp 10 into another. A
 //              K slot is free once S of its tile is done, so K runs well ahead of V.
-// Per key tile t the tensor core runs O += P(t) . V(t) once P(t) is written, then
-// S(t+2) = Q . K(t+2)^T into the buffer tile t used, so the softmax of tile t+1 overlaps both.
-// S and P are double-buffered with one barrier per buffer, so no barrier completes a phase its
-// waiter has not yet seen (a parity wait would miss it). The running max is raised lazily (only
+// Per key tile t the MMA thread issues S(t+1) = Q . K(t+1)^T as soon as the softmax has read S(t)
+// (s_free), and O += P(t) . V(t) once P(t) is written into P buffer t % 2 (p_full). The softmax
+// writes P(t) once the product that last read that buffer, PV(t-2), is done (pv_done). So S(t+1)
+// is computed while the softmax works on tile t, and the softmax never waits for a PV unless it
+// must rescale O. P has one barrier per buffer, so no barrier completes a phase its waiter has
+// not yet seen (a parity wait would miss it). The running max is raised lazily (only
 // when a tile exceeds it by more than 2^8), so O is rarely rescaled; at the end each row is
 // divided by its sum.
 #include <cuda.h>
@@ -44,22 +49,19 @@ constexpr int kPfStage = 2 * kPfHalf;          // one K (or V) tile: dims 0-63, 
 #ifndef PKV_PF_STAGES
 #define PKV_PF_STAGES 3                        // slots per ring (K and V each)
 #endif
-#ifndef PKV_PF_WAR_GUARD
-#define PKV_PF_WAR_GUARD 0
-#endif
 constexpr int kPfStages = PKV_PF_STAGES;
 constexpr int kPfOffK = 0;
 constexpr int kPfOffV = kPfStages * kPfStage;
 constexpr int kPfOffX = 2 * kPfStages * kPfStage;  // row maxima [2][2][128] and sums [2][128], fp32
 constexpr int kPfOffBar = kPfOffX + 6 * kPfQ * 4;
-// barriers: full[2 rings][S], empty[2 rings][S], s_full[2], p_full[2], pv_done, o_done, drain;
-// then the TMEM slot
-constexpr int kPfNumBars = 4 * kPfStages + 7;
+// barriers: full[2 rings][S], empty[2 rings][S], s_full, s_free, p_full[2], pv_done[2], o_done,
+// drain[2]; then the TMEM slot
+constexpr int kPfNumBars = 4 * kPfStages + 9;
 constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
-constexpr int kPfThreads = 352;
-constexpr int kPfMmaWarp = 8, kPfLoadWarpK = 9, kPfLoadWarpV = 10;
+constexpr int kPfThreads = 384;
+constexpr int kPfMmaWarp = 8, kPfLoadWarpK = 9, kPfLoadWarpV = 10, kPfMmaWarpPV = 11;
 constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kOCol = 0, kQCol = 128, kSCol = 256;
+constexpr uint32_t kOCol = 0, kQCol = 128, kPCol = 192, kSCol = 320;
 constexpr float kPfRescale = 8.0f;             // log2 units
 static_assert(kPfSmem <= 227 * 1024, "shared memory");
 static_assert(kPfStages >= 3, "S of tile t + 2 is computed while tile t still holds its stage");
@@ -215,11 +217,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     auto full = [&](int g, int s) { return bar0 + 8 * (g * kPfStages + s); };
     auto empty = [&](int g, int s) { return bar0 + 8 * (2 * kPfStages + g * kPfStages + s); };
     auto slot = [&](int g, int t) { return sbase + (g ? kPfOffV : kPfOffK) + (t % kPfStages) * kPfStage; };
-    auto s_full = [&](int u) { return bar0 + 8 * (4 * kPfStages + u); };
+    const uint32_t s_full = bar0 + 8 * (4 * kPfStages);
+    const uint32_t s_free = bar0 + 8 * (4 * kPfStages + 1);
     auto p_full = [&](int u) { return bar0 + 8 * (4 * kPfStages + 2 + u); };
-    const uint32_t pv_done = bar0 + 8 * (4 * kPfStages + 4);
-    const uint32_t o_done = bar0 + 8 * (4 * kPfStages + 5);
-    const uint32_t drain = bar0 + 8 * (4 * kPfStages + 6);
+    auto pv_done = [&](int u) { return bar0 + 8 * (4 * kPfStages + 4 + u); };
+    const uint32_t o_done = bar0 + 8 * (4 * kPfStages + 6);
+    auto drain = [&](int x) { return bar0 + 8 * (4 * kPfStages + 7 + x); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + kPfNumBars * 8);
     __shared__ int abort_flag;
 
@@ -229,13 +232,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 mbar_init(full(g, s), 1);
                 mbar_init(empty(g, s), 1);
             }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 2 * kPfQ);
         for (int u = 0; u < 2; ++u) {
-            mbar_init(s_full(u), 1);
             mbar_init(p_full(u), 2 * kPfQ);
+            mbar_init(pv_done(u), 1);
         }
-        mbar_init(pv_done, 1);
         mbar_init(o_done, 1);
-        mbar_init(drain, 1);
+        mbar_init(drain(0), 1);
+        mbar_init(drain(1), 1);
         abort_flag = 0;
         mbar_init_fence();
     }
@@ -313,31 +318,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             for (int t = issued - kPfStages < 0 ? 0 : issued - kPfStages; t < issued; ++t)
                 mbar_wait_bounded(full(g, t % kPfStages), (t / kPfStages) & 1);
         }
-    } else if (warp == kPfMmaWarp) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == kPfMmaWarp || warp == kPfMmaWarpPV) {
+        // ---------------- MMA issuers: S (warp 8) and PV (warp 11) ----------------
         if (lane == 0) {
+            const bool is_s = warp == kPfMmaWarp;
             constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
             constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
-            auto issue_s = [&](int t) {  // S(t) = Q . K(t)^T into buffer t % 2
+            auto issue_s = [&](int t) {  // S(t) = Q . K(t)^T
                 const uint32_t kbase = slot(0, t);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t bd = sdesc(kbase + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
-                    umma_ts(tmem + kSCol + 128 * (t & 1), tmem + kQCol + 8 * ks, bd, kIdescS, ks > 0);
+                    umma_ts(tmem + kSCol, tmem + kQCol + 8 * ks, bd, kIdescS, ks > 0);
                 }
-                umma_commit(s_full(t & 1));
+                umma_commit(s_full);
                 umma_commit(empty(0, t % kPfStages));  // the K slot is free once S(t) is done
             };
-            auto issue_pv = [&](int t) {  // O += P(t) . V(t); P over the first 32 columns of each S half
+            auto issue_pv = [&](int t) {  // O += P(t) . V(t), P(t) in buffer t % 2
                 const uint32_t vbase = slot(1, t);
-                const uint32_t pt = tmem + kSCol + 128 * (t & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bd = sdesc(vbase + kk * (16 * 128), kPfHalf, 1024);
-                    umma_ts(tmem + kOCol, pt + 64 * (kk >> 2) + 8 * (kk & 3), bd, kIdescO,
+                    umma_ts(tmem + kOCol, tmem + kPCol + 64 * (t & 1) + 8 * kk, bd, kIdescO,
                             (t > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(pv_done);
+                umma_commit(pv_done(t & 1));
                 umma_commit(empty(1, t % kPfStages));  // the V slot is free once PV(t) is done
             };
             bool ok = true;
@@ -351,30 +356,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 tc_fence_after();
                 return ok;
             };
-            for (int t = 0; t < 2 && t < ntiles && ok; ++t) {
-                if (!wait(full(0, t % kPfStages), (t / kPfStages) & 1)) break;
-                issue_s(t);
-            }
-            for (int t = 0; t < ntiles && ok; ++t) {
-                if (!wait(p_full(t & 1), (t >> 1) & 1)) break;
-                if (!wait(full(1, t % kPfStages), (t / kPfStages) & 1)) break;
-                issue_pv(t);
-                if (t + 2 < ntiles) {
-#if PKV_PF_WAR_GUARD
-                    if (!wait(pv_done, t & 1)) break;
-#endif
-                    if (!wait(full(0, (t + 2) % kPfStages), ((t + 2) / kPfStages) & 1)) break;
-                    issue_s(t + 2);
+            if (is_s) {
+                if (wait(full(0, 0), 0)) issue_s(0);
+                for (int t = 0; t + 1 < ntiles && ok; ++t) {  // S is free once the softmax has read S(t)
+                    if (!wait(s_free, t & 1)) break;
+                    if (!wait(full(0, (t + 1) % kPfStages), ((t + 1) / kPfStages) & 1)) break;
+                    issue_s(t + 1);
                 }
+            } else {
+                for (int t = 0; t < ntiles && ok; ++t) {
+                    if (!wait(p_full(t & 1), (t >> 1) & 1)) break;
+                    if (!wait(full(1, t % kPfStages), (t / kPfStages) & 1)) break;
+                    issue_pv(t);
+                }
+                umma_commit(o_done);
             }
-            umma_commit(o_done);
-            umma_commit(drain);
-            mbar_wait_bounded(drain, 0);  // every issued product is done before TMEM may go away
+            // every product this thread issued is done before TMEM may go away
+            umma_commit(drain(is_s ? 0 : 1));
+            mbar_wait_bounded(drain(is_s ? 0 : 1), 0);
         }
         __syncwarp();
     } else {
         // ---------------- softmax: row r, key half hf ----------------
         const uint32_t s_col = tmem + tl + kSCol + 64 * hf, o_col = tmem + tl + kOCol + 64 * hf;
+        const uint32_t p_col = tmem + tl + kPCol + 32 * hf;  // + 64 (t % 2)
         const int n_row = row_valid ? first_visible + i : 0;
         const int pair_bar = 1 + (warp & 3);  // named barrier of warps w and w + 4 (64 threads)
         // scores are scaled inside the exponents by |scale| * log2 e; a negative scale flips their
@@ -395,7 +400,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             const int mask8 = (present >> (8 * (t & 3))) & 0xFF;
             const int mask = (mask8 >> (4 * hf)) & 0xF;  // this half's four blocks
             const int u = t & 1;
-            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u), (t >> 1) & 1));
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(s_full, t & 1));
             if (!got) {
                 atomicExch(&abort_flag, 1);
                 flag(p.status, PKV_FLAG_TIMEOUT);
@@ -423,11 +428,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             float s[64];
             {
                 float t0[32], t1[32];
-                tmem_ld32(s_col + 128 * u, t0);
-                tmem_ld32(s_col + 128 * u + 32, t1);
+                tmem_ld32(s_col, t0);
+                tmem_ld32(s_col + 32, t1);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) { s[c] = t0[c]; s[32 + c] = t1[c]; }
             }
+            tc_fence_before();
+            mbar_arrive(s_free);  // S(t + 1) may now be written
             // raw scores here; the scale (with log2 e) is applied inside each exponent below
             const int kbase = t * kPfK + 64 * hf;
             if (neg || !(kbase + 64 <= n_row && mask == 0xF)) {  // not the whole half visible to this row
@@ -458,22 +465,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 l *= alpha;
             }
             const float ms = m == -INFINITY ? 0.f : m;
-            if (t > 0 && __any_sync(0xffffffffu, up)) {
-                // rescale this thread's half of its O row (rare), once PV of tile t - 1 is done
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done, (t - 1) & 1))) {
-                    atomicExch(&abort_flag, 1);
-                    flag(p.status, PKV_FLAG_TIMEOUT);
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    float o[32];
-                    tmem_ld32(o_col + c0, o);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] *= alpha;
-                    tmem_st32(o_col + c0, o);
-                }
-            }
             uint32_t pw[32];
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -483,9 +474,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
                 pw[c] = pack2_bf16(a0, a1);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // P over the first 32 columns of this half of the S buffer just read (the product
-            // that last read those columns, PV of tile t - 2, finished before S(t) was written)
-            tmem_st32u(s_col + 128 * u, pw);
+            // P buffer u is free once PV(t - 2) is done; O may be rescaled once PV(t - 1) is done
+            const bool resc = t > 0 && __any_sync(0xffffffffu, up);
+            const int wt = resc ? t - 1 : t - 2;  // the tile whose product must be complete
+            if (wt >= 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done(wt & 1), (wt >> 1) & 1))) {
+                    atomicExch(&abort_flag, 1);
+                    flag(p.status, PKV_FLAG_TIMEOUT);
+                }
+                tc_fence_after();
+            }
+            if (resc) {  // rescale this thread's half of its O row (rare)
+#pragma unroll 1
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(o_col + c0, o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                    tmem_st32(o_col + c0, o);
+                }
+            }
+            tmem_st32u(p_col + 64 * u, pw);
             tc_fence_before();
             mbar_arrive(p_full(u));
         }
