@@ -177,8 +177,11 @@ def parse_clock_rows(rows):
             "samples": len(sm)}
 
 
-def cuda_launches_per_step(w: W.DecodeWorkload, chunk_used: int) -> int:
-    """Kernels of this library one step launches: write, split, and merge when any split."""
+def cuda_launches_per_step(w: W.DecodeWorkload, chunk_used: int, cascade: bool = False) -> int:
+    """Kernels of this library one step launches: write, split, and merge when any split; a
+    shared-prefix (cascade) step adds the prefix kernel and always merges."""
+    if cascade:
+        return 4
     splits = max(1, w.max_context_len // chunk_used)
     return 2 + (1 if splits > 1 else 0)
 
@@ -306,9 +309,13 @@ def run_ours(args):
     kns, vns = up(w.k_new_scales), up(w.v_new_scales)
     out = torch.empty_like(q)
     maxc = w.max_context_len
-    chunk = pkv.decode_split_chunk(w.B, w.Hkv, w.D, maxc, args.chunk,
+    # a batch whose sequences share a prefix runs through the shared-prefix (cascade) call
+    prefix = w.shared_prefix_blocks * w.BS
+    cascade = prefix > 0 and not getattr(args, "no_cascade", False)
+    chunk = pkv.decode_split_chunk(w.B, w.Hkv, w.D, maxc - (prefix if cascade else 0), args.chunk,
                                    {"f32": pkv.F32, "bf16": pkv.BF16, "i8": pkv.I8}[w.kv_dtype])
-    nws = pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, args.chunk)
+    nws = (pkv.decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, prefix, args.chunk)
+           if cascade else pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, args.chunk))
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -325,7 +332,10 @@ def run_ours(args):
         pkv.kv_cache_write(kn, vn, kp, vp, sm, kns, vns, ks, vs, status=status, stream=stream)
 
     def attend():
-        if w.kv_dtype == "i8":
+        if cascade:
+            pkv.paged_decode_attention_shared_prefix(out, q, kp, vp, bt, cl, maxc, w.scale, prefix,
+                                                     args.chunk, ws, status, stream)
+        elif w.kv_dtype == "i8":
             pkv.paged_decode_attention_int8(out, q, kp, vp, ks, vs, bt, cl, maxc, w.scale,
                                             args.chunk, ws, status, stream)
         else:
@@ -423,6 +433,7 @@ def run_ours(args):
                    "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
                    "block_size": w.BS, "mean_context": float(w.context_lens.mean()),
                    "max_context": maxc, "split_chunk": chunk,
+                   "shared_prefix_call": bool(cascade),
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write, then a "
                          f"{L2_FLUSH_BYTES >> 21} MB read so no dirty line is left; untimed)",
                    "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
@@ -430,14 +441,16 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_kind": f"of {peak_kind}",
-                     "kernel": "paged decode attention call: split kernel + merge kernel (CUDA "
-                               "events around the call); traffic: split kernel (ncu)",
+                     "kernel": ("paged decode attention call: " +
+                                ("prefix (tcgen05) + split + merge kernels" if cascade
+                                 else "split kernel + merge kernel") +
+                                " (CUDA events around the call); traffic: split kernel (ncu)"),
                      "traffic": profiled_traffic(w.name),
                      "algorithmic_bytes_per_launch": attn_bytes,
                      "avg_launch_us": round(attn_avg_s * 1e6, 3)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": KE},
-        "gpu_launches": cuda_launches_per_step(w, chunk) * K,
+        "gpu_launches": cuda_launches_per_step(w, chunk, cascade) * K,
         "wall_s": round(wall_s, 3),
     }
     if clk is not None:
@@ -532,6 +545,9 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
     ap.add_argument("--chunk", type=int, default=0, help="split chunk in tokens (0 = auto)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="run a shared-prefix workload through the plain decode call instead of "
+                         "the shared-prefix (cascade) call")
     ap.add_argument("--prefill", action="store_true",
                     help="time the paged prefill kernel instead of the decode step")
     args = ap.parse_args(argv)

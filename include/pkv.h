@@ -68,6 +68,9 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
                                          sequence's splits were made longer (informational) */
 #define PKV_FLAG_TIMEOUT 0x10         /* a wait for a staged copy exceeded 1 s: that unit was
                                          abandoned and its output rows are undefined */
+#define PKV_FLAG_BAD_PREFIX 0x20      /* shared-prefix call: a sequence's table does not start with
+                                         the shared blocks, or its context is shorter than the
+                                         prefix; that sequence's output is undefined */
 
 /* Static text for a status code. Never NULL. */
 const char* pkv_status_string(pkv_status s);
@@ -157,6 +160,38 @@ pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void
                                             int max_context_len, float scale, pkv_dtype kv_dtype,
                                             int split_chunk_tokens, void* workspace,
                                             size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Decode attention for a batch whose sequences all begin with the same shared_prefix_tokens
+ * tokens stored in the same blocks -- the refcounted prefix sharing of "LLM Primer VI, Chapter 8",
+ * section 8.1 (one system prompt, or the samples of one request). The result is that of
+ * pkv_paged_decode_attention with the same arguments (the same softmax, summed in another
+ * order). The pages run each sequence over the whole context; here the prefix is read once per
+ * kv head and multiplied against every sequence's query heads at once on the tensor cores
+ * (tcgen05, the prefill kernel's machinery, split into key ranges), each sequence's own suffix
+ * [shared_prefix_tokens, context_len) goes through the split-K decode kernel, and the merge
+ * kernel combines both sets of (m, l, acc) states ("EchoLLMServing inference framework notes",
+ * section 2).
+ * bf16 q / out / pools, head_dim 128, one query token per sequence. shared_prefix_tokens is a
+ * positive multiple of block_size, <= max_context_len. The shared blocks are read from
+ * block_tables row 0; a sequence whose table does not start with them, or whose context_len is
+ * below shared_prefix_tokens, is flagged PKV_FLAG_BAD_PREFIX and its output is undefined.
+ * workspace: at least pkv_decode_shared_prefix_workspace_bytes(...) bytes, 256-byte aligned,
+ * contents on entry irrelevant. Other arguments and errors as pkv_paged_decode_attention.
+ */
+pkv_status pkv_paged_decode_attention_shared_prefix(
+    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+    int shared_prefix_tokens, int split_chunk_tokens, void* workspace, size_t workspace_bytes,
+    int32_t* status, void* stream);
+
+/* Workspace bytes pkv_paged_decode_attention_shared_prefix needs (0 for invalid arguments):
+ * num_seqs * num_q_heads * (suffix splits + prefix key splits) * (head_dim + 2) * 4. Pure host
+ * arithmetic. */
+size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int max_context_len,
+                                                int shared_prefix_tokens, int split_chunk_tokens);
 
 /*
  * Bytes of device workspace pkv_paged_decode_attention[_int8] needs for the split-K partial

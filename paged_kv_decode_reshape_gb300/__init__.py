@@ -15,6 +15,7 @@ from . import _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 F32, BF16, I8 = 0, 1, 2
 FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_CONTEXT, FLAG_LONG_CONTEXT, FLAG_TIMEOUT = 1, 2, 4, 8, 16
+FLAG_BAD_PREFIX = 32
 BLOCK_SIZE = 16
 
 # every exported symbol, with its ctypes signature (mirrors include/pkv.h)
@@ -36,6 +37,9 @@ SIGNATURES = {
                                      _I, _F, _P, _P], _I),
     "pkv_paged_decode_attention_static_ws": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                               _I, _F, _I, _I, _P, _P], _I),
+    "pkv_paged_decode_attention_shared_prefix": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                  _I, _I, _F, _I, _I, _P, _SZ, _P, _P], _I),
+    "pkv_decode_shared_prefix_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
 }
 STATIC_WORKSPACE_BYTES = 32 << 20  # PKV_STATIC_WORKSPACE_BYTES
 
@@ -151,6 +155,31 @@ def paged_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, m
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream))
     _check(rc, "paged_decode_attention")
+
+
+def decode_shared_prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                         max_context_len, shared_prefix_tokens,
+                                         split_chunk_tokens=0) -> int:
+    return int(load().pkv_decode_shared_prefix_workspace_bytes(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, shared_prefix_tokens,
+        split_chunk_tokens))
+
+
+def paged_decode_attention_shared_prefix(out, q, k_pool, v_pool, block_tables, context_lens,
+                                         max_context_len, scale, shared_prefix_tokens,
+                                         split_chunk_tokens=0, workspace=None, status=None,
+                                         stream=None):
+    """pkv_paged_decode_attention_shared_prefix: bf16 q/out [B, Hq, 128], bf16 pools; the first
+    shared_prefix_tokens tokens of every sequence are the blocks of block_tables row 0."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_decode_attention_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
+        B, Hq, Hkv, D, BS, NB, block_tables.shape[1], int(max_context_len), float(scale),
+        int(shared_prefix_tokens), int(split_chunk_tokens), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _check(rc, "paged_decode_attention_shared_prefix")
 
 
 def paged_decode_attention_int8(out, q, k_pool, v_pool, k_scales, v_scales, block_tables,

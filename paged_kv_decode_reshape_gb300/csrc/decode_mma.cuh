@@ -174,12 +174,20 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && lq == 0;
     if (bad && reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
     else if (stored > p.max_context_len && reporter) flag(p.status, PKV_FLAG_LONG_CONTEXT);
+    // tokens [kv_start, n) are this kernel's (kv_start > 0: a shared prefix is handled elsewhere)
+    if (p.kv_start > 0 && split == 0 && blockIdx.y == 0 && lq == 0) {
+        bool badp = n < p.kv_start;
+        const int nb = p.kv_start / kBlockSize;
+        for (int j = tid; j < nb && !badp; j += G::THREADS)
+            badp = p.block_tables[(size_t)b * p.MBPS + j] != p.block_tables[j];
+        if (badp) flag(p.status, PKV_FLAG_BAD_PREFIX);
+    }
     int per;
-    const int ns = split_count(n, p.chunk, p.max_splits, &per);
+    const int ns = split_count(n > p.kv_start ? n - p.kv_start : 0, p.chunk, p.max_splits, &per);
     if (split >= ns) return;
-    const int t0 = split * per;
+    const int t0 = p.kv_start + split * per;
     const int t1 = n < t0 + per ? n : t0 + per;
-    const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
+    const int nblk = t1 > t0 ? (t1 - t0 + kBlockSize - 1) / kBlockSize : 0;
     const int blk0 = t0 / kBlockSize;
 
     const uint32_t ring = smem_addr(smem);
@@ -523,10 +531,10 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
             }
         }
         const size_t qh = (size_t)zb * p.Hq + h0 + hh;
-        if (ns == 1) {
+        if (ns == 1 && !p.always_partial) {
             store_out<__nv_bfloat16>(static_cast<__nv_bfloat16*>(p.out) + qh * kMmaD + d, L > 0.f ? A / L : 0.f);
         } else {
-            const size_t u = qh * p.max_splits + split;
+            const size_t u = qh * p.ws_stride + split;
             p.ws_acc[u * kMmaD + d] = A;
             if (d == 0) {
                 p.ws_ml[2 * u] = M;

@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
         if (ns == 1) {
             store_out<QT>(static_cast<QT*>(p.out) + qh * D + d, L > 0.f ? A / L : 0.f);
         } else {
-            const size_t u = qh * p.max_splits + split;
+            const size_t u = qh * p.ws_stride + split;
             p.ws_acc[u * D + d] = A;
             if (d == 0) {
                 p.ws_ml[2 * u] = M;

@@ -56,6 +56,24 @@ size_t workspace_bytes_for(int B, int Hq, int D, int S) {
     return (size_t)B * Hq * S * ((size_t)D + 2) * sizeof(float);
 }
 
+// Key splits of a shared prefix (cascade decode): enough (row tile, kv head, split) CTAs for about
+// kPrefixTargetCtas, each split a whole number of 128-key tiles. Measured on the 256-sequence,
+// 2048-token-prefix batch: 64 CTAs (no key split) beat 148, 296 and 600 -- a CTA's set-up (TMEM,
+// Q, pipeline fill) outweighs the parallelism splitting the prefix adds.
+#ifndef PKV_PREFIX_TARGET_CTAS
+#define PKV_PREFIX_TARGET_CTAS 64
+#endif
+constexpr long long kPrefixTargetCtas = PKV_PREFIX_TARGET_CTAS;
+void prefix_splits(int rows, int g, int Hkv, int prefix, int* splits, int* split_tokens) {
+    const long long base = (long long)((rows * (long long)g + 127) / 128) * Hkv;
+    const int tiles = (prefix + 127) / 128;
+    long long s = (kPrefixTargetCtas + base - 1) / base;
+    s = s < 1 ? 1 : (s > tiles ? tiles : s);
+    const int per = (int)((tiles + s - 1) / s) * 128;
+    *split_tokens = per;
+    *splits = (prefix + per - 1) / per;
+}
+
 int heads_per_cta(int g) { return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8; }
 
 struct Decode {
@@ -69,6 +87,7 @@ struct Decode {
     void* ws; size_t ws_bytes;
     int32_t* status;
     cudaStream_t stream;
+    int prefix;  // shared-prefix tokens (cascade decode), else 0
 };
 
 pkv_status run_decode(const Decode& a) {
@@ -99,10 +118,23 @@ pkv_status run_decode(const Decode& a) {
     if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
-    const int chunk = choose_chunk(rows, a.Hkv, a.max_ctx, a.chunk_req, target_units(a.D, a.kv_dtype));
-    const int S = split_extent(a.max_ctx, chunk);
+    // shared prefix (cascade): tokens [0, prefix) of every sequence are the same blocks; they go to
+    // the tcgen05 prefix kernel as P key splits, the split kernel covers [prefix, n)
+    const int prefix = a.prefix;
+    if (prefix < 0) return PKV_ERR_INVALID_ARG;
+    if (prefix > 0) {
+        if (a.kv_dtype != PKV_BF16 || a.D != 128 || a.L != 1) return PKV_ERR_UNSUPPORTED;
+        if (prefix % kBlockSize || prefix > a.max_ctx) return PKV_ERR_INVALID_ARG;
+    }
+    const int suffix_max = a.max_ctx - prefix;
+    const int chunk = choose_chunk(rows, a.Hkv, suffix_max, a.chunk_req, target_units(a.D, a.kv_dtype));
+    const int S = split_extent(suffix_max, chunk);
     if (S > kMaxSplits) return PKV_ERR_UNSUPPORTED;
-    const size_t need = workspace_bytes_for(rows, a.Hq, a.D, S);
+    int P = 0, split_tokens = 0;
+    if (prefix > 0) prefix_splits(rows, g, a.Hkv, prefix, &P, &split_tokens);
+    const int Sw = S + P;  // partial slots per (row, query head)
+    const size_t need = P > 0 ? (size_t)rows * a.Hq * Sw * ((size_t)a.D + 2) * sizeof(float)
+                              : workspace_bytes_for(rows, a.Hq, a.D, S);
     if (need > 0) {
         if (!a.ws || a.ws_bytes < need) return PKV_ERR_WORKSPACE;
         if (!aligned(a.ws, 256)) return PKV_ERR_INVALID_ARG;
@@ -126,12 +158,15 @@ pkv_status run_decode(const Decode& a) {
     p.k_scales = a.k_scales; p.v_scales = a.v_scales;
     p.block_tables = a.block_tables; p.context_lens = a.context_lens;
     p.ws_acc = need ? static_cast<float*>(a.ws) : nullptr;
-    p.ws_ml = need ? static_cast<float*>(a.ws) + (size_t)rows * a.Hq * S * a.D : nullptr;
+    p.ws_ml = need ? static_cast<float*>(a.ws) + (size_t)rows * a.Hq * Sw * a.D : nullptr;
     p.status = a.status;
     p.B = a.B; p.L = a.L; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = g; p.NB = a.NB; p.MBPS = a.MBPS;
     p.chunk = chunk; p.max_splits = S; p.head_chunks = head_chunks;
     p.max_context_len = a.max_ctx;
     p.scale_log2 = a.scale * kLog2e;
+    p.kv_start = prefix;
+    p.always_partial = P > 0;
+    p.ws_stride = Sw;
 
     cudaError_t e;
     if (mma) {
@@ -140,15 +175,24 @@ pkv_status run_decode(const Decode& a) {
         if (!make_pool_tensor_map(&tk, a.k_pool, a.NB, a.Hkv, i8m) ||
             !make_pool_tensor_map(&tv, a.v_pool, a.NB, a.Hkv, i8m))
             return PKV_ERR_CUDA;
+        if (P > 0) {
+            PrefixParams x{};
+            x.q = a.q; x.block_tables = a.block_tables; x.ws_acc = p.ws_acc; x.ws_ml = p.ws_ml;
+            x.status = a.status; x.B = a.B; x.Hq = a.Hq; x.Hkv = a.Hkv; x.G = g; x.NB = a.NB;
+            x.MBPS = a.MBPS; x.S = Sw; x.slot0 = S; x.prefix_tokens = prefix;
+            x.split_tokens = split_tokens; x.scale_log2 = p.scale_log2;
+            if (launch_prefix(x, tk, tv, P, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
+        }
         e = launch_split_mma(p, i8m, tk, tv, a.stream);
     } else if (a.kv_dtype == PKV_F32) e = launch_split_f32(p, a.D, hg, a.stream);
     else if (a.kv_dtype == PKV_BF16) e = launch_split_bf16(p, a.D, hg, a.stream);
     else e = launch_split_i8(p, a.D, hg, a.stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
-    if (S > 1) {
+    if (S > 1 || P > 0) {
         MergeParams m{};
         m.out = a.out; m.ws_acc = p.ws_acc; m.ws_ml = p.ws_ml; m.context_lens = a.context_lens;
         m.B = a.B; m.L = a.L; m.Hq = a.Hq; m.MBPS = a.MBPS; m.chunk = chunk; m.max_splits = S;
+        m.kv_start = prefix; m.extra0 = S; m.extra = P; m.ws_stride = Sw;
         if (launch_merge(m, a.q_dtype, a.D, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;
@@ -358,6 +402,39 @@ pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void
              num_seqs, num_query_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
              num_blocks, max_blocks_per_seq, max_context_len, scale, q_dtype, kv_dtype,
              split_chunk_tokens, workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
+    return run_decode(a);
+}
+
+size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int max_context_len,
+                                                int shared_prefix_tokens, int split_chunk_tokens) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+        head_dim != 128 || max_context_len < 0 || split_chunk_tokens < 0 ||
+        split_chunk_tokens % kBlockSize || shared_prefix_tokens <= 0 ||
+        shared_prefix_tokens % kBlockSize || shared_prefix_tokens > max_context_len)
+        return 0;
+    const int suffix_max = max_context_len - shared_prefix_tokens;
+    const int chunk = choose_chunk(num_seqs, num_kv_heads, suffix_max, split_chunk_tokens,
+                                   target_units(head_dim, PKV_BF16));
+    const int S = split_extent(suffix_max, chunk);
+    int P = 0, split_tokens = 0;
+    prefix_splits(num_seqs, num_q_heads / num_kv_heads, num_kv_heads, shared_prefix_tokens, &P,
+                  &split_tokens);
+    return (size_t)num_seqs * num_q_heads * (S + P) * ((size_t)head_dim + 2) * sizeof(float);
+}
+
+pkv_status pkv_paged_decode_attention_shared_prefix(
+    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+    int shared_prefix_tokens, int split_chunk_tokens, void* workspace, size_t workspace_bytes,
+    int32_t* status, void* stream) {
+    if (shared_prefix_tokens <= 0) return PKV_ERR_INVALID_ARG;
+    Decode a{out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens,
+             num_seqs, 1, num_q_heads, num_kv_heads, head_dim, block_size,
+             num_blocks, max_blocks_per_seq, max_context_len, scale, PKV_BF16, PKV_BF16,
+             split_chunk_tokens, workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
+    a.prefix = shared_prefix_tokens;
     return run_decode(a);
 }
 

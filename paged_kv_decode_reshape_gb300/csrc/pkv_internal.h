@@ -67,6 +67,9 @@ struct SplitParams {
     int head_chunks;            // CTAs per kv head along grid.y (ceil(G / heads per CTA))
     int max_context_len;
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units
+    int kv_start;               // tokens [0, kv_start) are handled elsewhere (shared prefix), else 0
+    int always_partial;         // write (m, l, acc) even for single-split rows (merged later)
+    int ws_stride;              // partial slots per (row, query head) in the workspace (>= max_splits)
 };
 
 struct MergeParams {
@@ -75,6 +78,9 @@ struct MergeParams {
     const float* ws_ml;
     const int32_t* context_lens;
     int B, Hq, MBPS, L, chunk, max_splits;  // B: sequences; rows are (sequence, query token)
+    int kv_start;          // the split kernel's kv_start (its splits cover [kv_start, n))
+    int extra0, extra;     // extra partial slots [extra0, extra0 + extra) per row (shared prefix)
+    int ws_stride;         // partial slots per (row, query head) in the workspace
 };
 
 struct WriteParams {
@@ -131,6 +137,21 @@ struct PrefillParams {
     float scale_log2;
 };
 
+// Shared-prefix (cascade) decode, prefix part: every (sequence, query head) row of one kv head
+// against the first prefix_tokens tokens of block_tables[0], split into key ranges; each range
+// writes a partial state (m, l, acc) into partial slot slot0 + split of the decode workspace.
+struct PrefixParams {
+    const void* q;                // [B][Hq][128] bf16
+    const int32_t* block_tables;  // [B][MBPS]; row 0's first prefix blocks are the shared ones
+    float* ws_acc;                // [B][Hq][S][128]
+    float* ws_ml;                 // [B][Hq][S][2]
+    int32_t* status;
+    int B, Hq, Hkv, G, NB, MBPS;
+    int S, slot0;                 // partial slots per (row, head); first prefix slot
+    int prefix_tokens, split_tokens;  // both multiples of 128
+    float scale_log2;
+};
+
 // Launchers (return the launch's error code).
 cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_kv_write_quant(const QuantWriteParams& p, pkv_dtype src, int D, cudaStream_t s);
@@ -142,6 +163,8 @@ cudaError_t launch_merge(const MergeParams& p, pkv_dtype out_dtype, int D, cudaS
 // Tensor-core split kernel for head_dim 128, bf16 or INT8 pools, 8 query heads per CTA; the K and
 // V pools are described by TMA tensor maps built with make_pool_tensor_map (false on failure).
 bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, bool i8);
+cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int splits,
+                          cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                            int max_query_len, cudaStream_t s);
 cudaError_t launch_split_mma(const SplitParams& p, bool i8, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -7,6 +7,10 @@
 // Sequence b's L_b query tokens are the last L_b of its context (written to the cache first);
 // query row i attends causally to the first n_b - (L_b - 1 - i) tokens.
 //
+// The same kernel (kPrefix) also runs the shared-prefix part of a cascade decode: there a CTA's 128
+// rows are (sequence, query head) pairs of one kv head, all attending to one key range of the
+// prefix every sequence shares, and it writes partial states (m, l, acc) for the merge kernel.
+//
 // One CTA computes 128 query rows of one query head against 128-key tiles. Both products read
 // their A operand from tensor memory: measured on GB300, a tcgen05.mma (M = 128, K = 16) with A in
 // TMEM takes ~82 cycles at N = 128 (the tensor peak), while with A in shared memory it takes
@@ -171,27 +175,58 @@ __device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
     return res != 0;
 }
 
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillParams p,
+// What one launch computes, filled by launch_prefill (kPrefix false) or launch_prefix (true).
+struct PfWork {
+    const void* q;
+    const int32_t* block_tables;
+    int32_t* status;
+    int Hq, Hkv, G, NB, MBPS;
+    float scale_log2;
+    // prefill: rows are query tokens of sequence blockIdx.z, one query head (blockIdx.y) per CTA
+    void* out;
+    const int32_t* context_lens;
+    const int32_t* query_start;
+    // shared prefix: rows are the (sequence, head-in-group) pairs of kv head blockIdx.y; keys are
+    // split blockIdx.z of the prefix (block_tables row 0); output is a partial state per row
+    float* ws_acc;
+    float* ws_ml;
+    int B, S, slot0, prefix_tokens, split_tokens;
+};
+
+template <bool kPrefix>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
     grid_dependency_wait();
-    // heaviest query tiles (most keys under the causal mask) first
-    const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int kvh = h / p.G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q0 = p.query_start[b];
-    const int L = p.query_start[b + 1] - q0;
-    if (qt * kPfQ >= L) return;
-    const int n = p.context_lens[b];
-    if (n < L || n > p.MBPS * kBlockSize) {
-        if (tid == 0 && qt == 0 && h == 0) flag(p.status, PKV_FLAG_BAD_CONTEXT);
-        return;
+    int qt, h, kvh, b, L, q0, first_visible, n_tile_max, split;
+    const int32_t* bt_row;
+    if constexpr (!kPrefix) {
+        // heaviest query tiles (most keys under the causal mask) first
+        qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+        kvh = h / p.G;
+        split = 0;
+        q0 = p.query_start[b];
+        L = p.query_start[b + 1] - q0;
+        if (qt * kPfQ >= L) return;
+        const int n = p.context_lens[b];
+        if (n < L || n > p.MBPS * kBlockSize) {
+            if (tid == 0 && qt == 0 && h == 0) flag(p.status, PKV_FLAG_BAD_CONTEXT);
+            return;
+        }
+        first_visible = n - L + 1;                          // keys visible to query row 0
+        const int rows = min(kPfQ, L - qt * kPfQ);
+        n_tile_max = first_visible + qt * kPfQ + rows - 1;  // keys visible to the last row
+        bt_row = p.block_tables + (size_t)b * p.MBPS;
+    } else {
+        qt = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
+        h = 0, b = 0, q0 = 0, first_visible = 0;
+        L = p.B * p.G;                                      // rows of this kv head
+        const int key0 = split * p.split_tokens;            // keys [key0, key0 + n_tile_max)
+        n_tile_max = min(p.split_tokens, p.prefix_tokens - key0);
+        bt_row = p.block_tables + key0 / kBlockSize;
     }
-    const int first_visible = n - L + 1;                          // keys visible to query row 0
-    const int rows = min(kPfQ, L - qt * kPfQ);
-    const int n_tile_max = first_visible + qt * kPfQ + rows - 1;  // keys visible to the last row
     const int ntiles = (n_tile_max + kPfK - 1) / kPfK;
-    const int32_t* bt_row = p.block_tables + (size_t)b * p.MBPS;
     // Block ids come in windows of 32 (4 key tiles), lane j holding block 32 w + j (-1: not needed
     // or invalid), the next window loaded while the current one is used.
     auto load_window = [&](int w, bool report) {
@@ -260,11 +295,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
     const int r = tid & 127;
     const int i = qt * kPfQ + r;
     const bool row_valid = i < L;
+    // the (token, head) row of q / out: prefill query token q0 + i of head h; shared prefix: the
+    // (sequence i / G, head kvh * G + i % G) pair
+    const size_t qrow = !kPrefix ? (size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h
+                                 : (row_valid ? (size_t)(i / p.G) * p.Hq + kvh * p.G + i % p.G : 0);
     const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
     if (warp < 8) {
-        // Q row r, dims 64 hf .. 64 hf + 63, into TMEM columns 128 + 32 hf .. (zeros past the queries)
+        // Q row r, dims 64 hf .. 64 hf + 63, into TMEM columns 128 + 32 hf .. (zeros past the rows)
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128 + 64 * hf);
+                                                          qrow * 128 + 64 * hf);
         uint32_t qw[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -380,7 +419,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
         // ---------------- softmax: row r, key half hf ----------------
         const uint32_t s_col = tmem + tl + kSCol + 64 * hf, o_col = tmem + tl + kOCol + 64 * hf;
         const uint32_t p_col = tmem + tl + kPCol + 32 * hf;  // + 64 (t % 2)
-        const int n_row = row_valid ? first_visible + i : 0;
+        // keys (relative to the CTA's first key) this row sees
+        const int n_row = !row_valid ? 0 : (kPrefix ? n_tile_max : first_visible + i);
         const int pair_bar = 1 + (warp & 3);  // named barrier of warps w and w + 4 (64 threads)
         // scores are scaled inside the exponents by |scale| * log2 e; a negative scale flips their
         // sign. |scale| is at least FLT_MIN so a masked score (-inf) never meets a zero factor: a
@@ -507,11 +547,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
         xsum[hf * kPfQ + r] = l;
         const bool fail = barrier_or(pair_bar, 64, !ok || aborted(&abort_flag));
         const float lt = l + xsum[(hf ^ 1) * kPfQ + r];
-        if (!fail) {
+        if (!fail && kPrefix) {
+            // ---- epilogue: the partial state (m in log2 units, l, acc = O unnormalised) ----
+            const size_t u = qrow * p.S + p.slot0 + split;
+            float* acc = p.ws_acc + u * 128 + 64 * hf;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float o[32];
+                tmem_ld32(o_col + c0, o);
+                if (row_valid) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        reinterpret_cast<float4*>(acc + c0)[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                }
+            }
+            if (row_valid && hf == 0) {
+                p.ws_ml[2 * u] = m;
+                p.ws_ml[2 * u + 1] = lt;
+            }
+        } else if (!fail) {
             // ---- epilogue: dims 64 hf .. 64 hf + 63 of row r of O / l -> out ----
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                  ((size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h) * 128 + 64 * hf);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + qrow * 128 + 64 * hf);
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 float o[32];
@@ -540,10 +597,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                            int max_query_len, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return e;
+    PfWork w{};
+    w.q = p.q; w.block_tables = p.block_tables; w.status = p.status;
+    w.Hq = p.Hq; w.Hkv = p.Hkv; w.G = p.G; w.NB = p.NB; w.MBPS = p.MBPS; w.scale_log2 = p.scale_log2;
+    w.out = p.out; w.context_lens = p.context_lens; w.query_start = p.query_start; w.B = p.B;
     const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hq, p.B);
-    return launch_pdl(prefill_kernel, grid, dim3(kPfThreads), kPfSmem, s, p, tk, tv);
+    return launch_pdl(prefill_kernel<false>, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
+}
+
+cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int splits,
+                          cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return e;
+    PfWork w{};
+    w.q = p.q; w.block_tables = p.block_tables; w.status = p.status;
+    w.Hq = p.Hq; w.Hkv = p.Hkv; w.G = p.G; w.NB = p.NB; w.MBPS = p.MBPS; w.scale_log2 = p.scale_log2;
+    w.ws_acc = p.ws_acc; w.ws_ml = p.ws_ml; w.B = p.B; w.S = p.S; w.slot0 = p.slot0;
+    w.prefix_tokens = p.prefix_tokens; w.split_tokens = p.split_tokens;
+    const dim3 grid((p.B * p.G + kPfQ - 1) / kPfQ, p.Hkv, splits);
+    return launch_pdl(prefill_kernel<true>, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
 }
 
 }  // namespace pkv

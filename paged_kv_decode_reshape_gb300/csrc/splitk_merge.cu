@@ -4,7 +4,8 @@
 // (m, l, acc) and a second reduce kernel combines them. For one (sequence, query head) with
 // splits j < ns (scores in base-2 units):
 //     M = max_j m_j,   w_j = 2^(m_j - M),   L = sum_j w_j l_j,   out = sum_j w_j acc_j / L
-// Sequences with a single split were finished by kernel 1 and are skipped here.
+// Sequences with a single split were finished by kernel 1 and are skipped here. In a shared-prefix
+// call every row also has extra slots (the prefix partials) and is always merged.
 //
 // One warp per (sequence, query head), eight per CTA, so the whole batch is one wave of CTAs.
 // Lane i owns D/32 consecutive columns. The warp loads its split rows eight at a time as
@@ -41,28 +42,32 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     bool bad;
     const int n = query_context_len(p.context_lens[b], p.L, zb - b * p.L, p.MBPS * kBlockSize, &bad);
     int per;
-    const int ns = split_count(n, p.chunk, p.max_splits, &per);
-    if (ns <= 1) return;
+    const int ns = split_count(n > p.kv_start ? n - p.kv_start : 0, p.chunk, p.max_splits, &per);
+    if (ns <= 1 && p.extra == 0) return;
+    // slots: the row's ns splits, then the extra (shared-prefix) slots
+    const int total = ns + p.extra;
+    auto slot = [&](int k) { return k < ns ? k : p.extra0 + (k - ns); };
 
-    const size_t base = (size_t)pair * p.max_splits;
+    const size_t base = (size_t)pair * p.ws_stride;
     const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + base;
     const VT* acc = reinterpret_cast<const VT*>(p.ws_acc + base * D) + lane;
     float m = -INFINITY, l = 0.f, a[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) a[e] = 0.f;
-    for (int j0 = 0; j0 < ns; j0 += kMergeBatch) {
+    for (int j0 = 0; j0 < total; j0 += kMergeBatch) {
         float2 st[kMergeBatch];
         VT v[kMergeBatch];
 #pragma unroll
         for (int u = 0; u < kMergeBatch; ++u) {
-            if (j0 + u < ns) {
-                st[u] = ml[j0 + u];
-                v[u] = acc[(size_t)(j0 + u) * (D / V)];
+            if (j0 + u < total) {
+                const int sl = slot(j0 + u);
+                st[u] = ml[sl];
+                v[u] = acc[(size_t)sl * (D / V)];
             }
         }
 #pragma unroll
         for (int u = 0; u < kMergeBatch; ++u) {
-            if (j0 + u >= ns || st[u].x == -INFINITY) continue;  // empty split: no contribution
+            if (j0 + u >= total || st[u].x == -INFINITY) continue;  // empty split: no contribution
             const float mn = fmaxf(m, st[u].x);
             const float s0 = ex2(m - mn), s1 = ex2(st[u].x - mn);  // m == -inf: s0 = 0
             l = l * s0 + st[u].y * s1;

@@ -76,6 +76,17 @@ def test_workspace_arithmetic(pkv):
     assert (1 << 30) // L.pkv_decode_split_chunk(1, 1, 128, 1 << 30, 0, BF) <= 8192
     assert L.pkv_decode_split_chunk(4, 4, 64, 100, 48, F32) == 48        # explicit request kept
     assert L.pkv_decode_split_chunk(4, 4, 64, 100, 0, 7) == 0            # unknown dtype
+    # shared-prefix decode: suffix splits (auto chunk over the longest suffix) + prefix key splits
+    # (about 64 CTAs over (row tile of 128, kv head, split); whole 128-key tiles).
+    # 256 seqs x 32/8 heads, prefix 2048 of max 4090: suffix chunk 1024 -> 1 split; 8 row tiles
+    # x 8 kv heads = 64 -> 1 prefix split; 2 slots x 130 floats
+    assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 128, 4090, 2048, 0) == 256 * 32 * 2 * 130 * 4
+    # 8 seqs: suffix chunk 256 -> 2042 // 256 = 7 splits; 1 row tile x 8 kv heads -> 8 prefix
+    # splits of 256 tokens; 15 slots
+    assert L.pkv_decode_shared_prefix_workspace_bytes(8, 32, 8, 128, 4090, 2048, 0) == 8 * 32 * 15 * 130 * 4
+    assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 128, 4090, 40, 0) == 0    # not a block multiple
+    assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 64, 4090, 2048, 0) == 0   # head_dim 128 only
+    assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 128, 1000, 2048, 0) == 0  # prefix > context
     # the workspace bound covers the bf16 call (fewer splits) too
     assert L.pkv_decode_workspace_bytes(64, 32, 8, 128, 4055, 0) == 64 * 32 * (4055 // 256) * 130 * 4
 
