@@ -166,7 +166,12 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int h0 = kvh * p.G + hc * kMmaHeads;
     const int nh = p.G - hc * kMmaHeads < kMmaHeads ? p.G - hc * kMmaHeads : kMmaHeads;
 
-    grid_dependency_wait();  // inputs (new K/V rows, tables) may come from the previous kernel
+    // Inputs (new K/V rows, tables) may come from the previous kernel: wait for it. In a
+    // shared-prefix call the previous kernel is the prefix kernel, which releases this one only
+    // after its own wait (so the inputs are complete) and writes nothing this kernel reads; this
+    // kernel then runs alongside it and waits for it only at exit, which keeps the merge kernel
+    // (waiting for this grid) behind both.
+    if (p.kv_start == 0) grid_dependency_wait();
 
     const int stored = p.context_lens[b];
     bool bad;
@@ -184,7 +189,10 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     }
     int per;
     const int ns = split_count(n > p.kv_start ? n - p.kv_start : 0, p.chunk, p.max_splits, &per);
-    if (split >= ns) return;
+    if (split >= ns) {
+        if (p.kv_start > 0) grid_dependency_wait();
+        return;
+    }
     const int t0 = p.kv_start + split * per;
     const int t1 = n < t0 + per ? n : t0 + per;
     const int nblk = t1 > t0 ? (t1 - t0 + kBlockSize - 1) / kBlockSize : 0;
@@ -490,7 +498,10 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     }
 
     __syncthreads();  // every warp is done with the ring (its copies all consumed or drained)
-    if (abort_flag) return;
+    if (abort_flag) {
+        if (p.kv_start > 0) grid_dependency_wait();
+        return;
+    }
     grid_dependents_launch();  // the merge kernel may start launching
     // ---- merge the consumer warps' states (ring memory reused) ----
     float* sm_m = reinterpret_cast<float*>(smem);               // [NC][8]
@@ -542,6 +553,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
             }
         }
     }
+    if (p.kv_start > 0) grid_dependency_wait();
 }
 
 }  // namespace pkv

@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
     grid_dependency_wait();
+    // shared prefix: the suffix kernel after this one reads nothing this one writes, so it may
+    // start now and run on the SMs this grid leaves free (it waits for this grid before it exits)
+    if constexpr (kPrefix) grid_dependents_launch();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int qt, h, kvh, b, L, q0, first_visible, n_tile_max, split;
     const int32_t* bt_row;
