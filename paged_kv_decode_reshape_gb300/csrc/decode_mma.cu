@@ -31,7 +31,7 @@ cudaError_t launch_t(const SplitParams& p, const CUtensorMap& tk, const CUtensor
     auto kern = mma_split_kernel<kI8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.B * p.L), dim3(G::THREADS), G::SMEM, s,
+    return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.packed ? p.B : p.B * p.L), dim3(G::THREADS), G::SMEM, s,
                       p, tk, tv);
 }
 

@@ -161,10 +161,17 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.head_chunks;
     const int hc = blockIdx.y - kvh * p.head_chunks;
-    const int zb = blockIdx.z;          // row of q / out: query token lq of sequence b
-    const int b = zb / p.L, lq = zb - b * p.L;
-    const int h0 = kvh * p.G + hc * kMmaHeads;
-    const int nh = p.G - hc * kMmaHeads < kMmaHeads ? p.G - hc * kMmaHeads : kMmaHeads;
+    // MMA columns: query heads of one (sequence, query token) row, or -- packed multi-token
+    // decode -- the (query token, head) pairs of one sequence's kv head, so that the L tokens
+    // being verified read each K/V tile once. The splits follow the longest context (the last
+    // token's); each column masks the keys past its own context n - (L - 1 - l).
+    const int b = p.packed ? blockIdx.z : blockIdx.z / p.L;
+    const int lq = p.packed ? p.L - 1 : blockIdx.z - b * p.L;  // the token the splits follow
+    const int c0 = hc * kMmaHeads;                               // first column of this CTA
+    const int ncols = p.packed ? p.L * p.G : p.G;
+    const int nh = ncols - c0 < kMmaHeads ? ncols - c0 : kMmaHeads;  // columns in use
+    auto col_zb = [&](int j) { return p.packed ? b * p.L + (c0 + j) / p.G : (int)blockIdx.z; };
+    auto col_head = [&](int j) { return kvh * p.G + (p.packed ? (c0 + j) % p.G : c0 + j); };
 
     // Inputs (new K/V rows, tables) may come from the previous kernel: wait for it. In a
     // shared-prefix call the previous kernel is the prefix kernel, which releases this one only
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int stored = p.context_lens[b];
     bool bad;
     const int n = query_context_len(stored, p.L, lq, p.MBPS * kBlockSize, &bad);
-    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && lq == 0;
+    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && (p.packed || lq == 0);
     if (bad && reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
     else if (stored > p.max_context_len && reporter) flag(p.status, PKV_FLAG_LONG_CONTEXT);
     // tokens [kv_start, n) are this kernel's (kv_start > 0: a shared prefix is handled elsewhere)
@@ -210,6 +217,9 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     // per-lane MMA coordinates
     const int r = lane >> 2;  // fragment row group: token (QK) / head (B operand)
     const int c = lane & 3;   // thread in group: head pair 2c, 2c+1 of the C fragments
+    // context of columns 2c and 2c + 1 (packed: token (c0 + col) / G sees n - (L - 1 - l) keys)
+    auto col_ctx = [&](int j) { return p.packed ? n - (p.L - 1 - (c0 + j) / p.G) : n; };
+    const int ncol_lim0 = col_ctx(2 * c), ncol_lim1 = col_ctx(2 * c + 1);
 
     float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
     float o[8][4];
@@ -273,7 +283,8 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
         float qsum = 0.f;  // INT8: sum of this lane's fp16 q' values of head r (as the MMA sees them)
         {
             const bool hv = r < nh;
-            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)zb * p.Hq + h0 + (hv ? r : 0)) * kMmaD;
+            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                        ((size_t)col_zb(hv ? r : 0) * p.Hq + col_head(hv ? r : 0)) * kMmaD;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 if constexpr (kI8) {
@@ -360,7 +371,9 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                 }
                 // s[0] = (tok r, head 2c), s[1] = (tok r, 2c+1), s[2] = (tok r+8, 2c), s[3] = (tok r+8, 2c+1)
                 const int nvalid = t1 - (t0 + j * kBlockSize);  // >= 1; >= 16 for full blocks
-                const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+                // keys of this block visible to this lane's columns 2c and 2c + 1
+                const int lim0 = min(nvalid, ncol_lim0 - (t0 + j * kBlockSize));
+                const int lim1 = min(nvalid, ncol_lim1 - (t0 + j * kBlockSize));
                 float vs0 = 1.f, vs1 = 1.f;
                 if constexpr (kI8) {
                     const float* sc = scl + st * 2 * kBlockSize;
@@ -373,10 +386,10 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[e] *= p.scale_log2;
                 }
-                s[0] = v0 ? s[0] : kNegInf;
-                s[1] = v0 ? s[1] : kNegInf;
-                s[2] = v1 ? s[2] : kNegInf;
-                s[3] = v1 ? s[3] : kNegInf;
+                s[0] = r < lim0 ? s[0] : kNegInf;
+                s[1] = r < lim1 ? s[1] : kNegInf;
+                s[2] = r + 8 < lim0 ? s[2] : kNegInf;
+                s[3] = r + 8 < lim1 ? s[3] : kNegInf;
                 float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
                 for (int off = 4; off <= 16; off <<= 1) {
@@ -529,6 +542,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     for (int e = tid; e < kMmaHeads * kMmaD; e += G::THREADS) {
         const int hh = e / kMmaD, d = e % kMmaD;
         if (hh >= nh) continue;
+        const int zb = col_zb(hh);
         float M = kNegInf;
 #pragma unroll
         for (int w = 0; w < G::NC; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
@@ -541,7 +555,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                 A = fmaf(wt, sm_o[(w * kMmaHeads + hh) * kMmaD + d], A);
             }
         }
-        const size_t qh = (size_t)zb * p.Hq + h0 + hh;
+        const size_t qh = (size_t)zb * p.Hq + col_head(hh);
         if (ns == 1 && !p.always_partial) {
             store_out<__nv_bfloat16>(static_cast<__nv_bfloat16*>(p.out) + qh * kMmaD + d, L > 0.f ? A / L : 0.f);
         } else {

@@ -114,7 +114,12 @@ pkv_status run_decode(const Decode& a) {
     // head_dim 64 on the CUDA-core kernel
     const bool mma = uses_mma(a.D, a.kv_dtype);
     const int hg = mma ? 8 : heads_per_cta(g);
-    const int head_chunks = (g + hg - 1) / hg;
+    // multi-token decode on the tensor-core kernel: pack the (token, head) pairs of a sequence's
+    // kv head into the kernel's 8 columns when that takes fewer passes over K/V than one row
+    // (query token) at a time
+    const bool packed = mma && a.L > 1 && a.prefix == 0 &&
+                        (long long)(a.L * g + 7) / 8 < (long long)a.L * ((g + 7) / 8);
+    const int head_chunks = packed ? (a.L * g + 7) / 8 : (g + hg - 1) / hg;
     if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
@@ -167,6 +172,7 @@ pkv_status run_decode(const Decode& a) {
     p.kv_start = prefix;
     p.always_partial = P > 0;
     p.ws_stride = Sw;
+    p.packed = packed;
 
     cudaError_t e;
     if (mma) {
@@ -192,7 +198,7 @@ pkv_status run_decode(const Decode& a) {
         MergeParams m{};
         m.out = a.out; m.ws_acc = p.ws_acc; m.ws_ml = p.ws_ml; m.context_lens = a.context_lens;
         m.B = a.B; m.L = a.L; m.Hq = a.Hq; m.MBPS = a.MBPS; m.chunk = chunk; m.max_splits = S;
-        m.kv_start = prefix; m.extra0 = S; m.extra = P; m.ws_stride = Sw;
+        m.kv_start = prefix; m.extra0 = S; m.extra = P; m.ws_stride = Sw; m.packed = packed;
         if (launch_merge(m, a.q_dtype, a.D, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;

@@ -70,6 +70,7 @@ struct SplitParams {
     int kv_start;               // tokens [0, kv_start) are handled elsewhere (shared prefix), else 0
     int always_partial;         // write (m, l, acc) even for single-split rows (merged later)
     int ws_stride;              // partial slots per (row, query head) in the workspace (>= max_splits)
+    int packed;                 // multi-token: one CTA column per (query token, head) of a sequence
 };
 
 struct MergeParams {
@@ -81,6 +82,7 @@ struct MergeParams {
     int kv_start;          // the split kernel's kv_start (its splits cover [kv_start, n))
     int extra0, extra;     // extra partial slots [extra0, extra0 + extra) per row (shared prefix)
     int ws_stride;         // partial slots per (row, query head) in the workspace
+    int packed;            // the split kernel ran packed: splits follow the sequence's last token
 };
 
 struct WriteParams {

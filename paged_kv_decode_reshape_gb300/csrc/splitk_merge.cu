@@ -40,7 +40,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     const int zb = pair / p.Hq;  // (sequence, query token) row
     const int b = zb / p.L;
     bool bad;
-    const int n = query_context_len(p.context_lens[b], p.L, zb - b * p.L, p.MBPS * kBlockSize, &bad);
+    // the context the split kernel split: the row's own, or (packed) the sequence's last token's
+    const int n = query_context_len(p.context_lens[b], p.L, p.packed ? p.L - 1 : zb - b * p.L,
+                                    p.MBPS * kBlockSize, &bad);
     int per;
     const int ns = split_count(n > p.kv_start ? n - p.kv_start : 0, p.chunk, p.max_splits, &per);
     if (ns <= 1 && p.extra == 0) return;

@@ -81,3 +81,21 @@ def test_context_shorter_than_new_tokens_is_flagged():
     assert int(st.item()) & P.FLAG_BAD_CONTEXT
     got = to_f64(out)
     assert np.all(got[:, 0] == 0) and np.all(np.isfinite(got))  # token 0 sees no context
+
+
+@pytest.mark.parametrize("kv", ["bf16", "i8"])
+@pytest.mark.parametrize("g,L", [(1, 3), (2, 4), (3, 3), (4, 2), (4, 5), (6, 2), (1, 8)])
+def test_multi_token_packed_columns(kv, g, L):
+    """When L * G query rows of a sequence's kv head fit the kernel's 8 columns better than one
+    token at a time, the tensor-core kernel packs (token, head) pairs as columns, each masked at
+    its own causal limit; L * G not a multiple of 8 leaves a partial last column group."""
+    Hkv = 2
+    base = W.make_decode(name="mtp_pack", B=5, Hq=Hkv * g, Hkv=Hkv, D=128,
+                         context_lens=[L, L + 1, 17, 300, 900], kv_dtype=kv, q_dtype="bf16",
+                         seed=200 + 10 * g + L)
+    m = W.make_multi_token(base, L, seed=300 + L)
+    for chunk in (0, 64):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        got = _run(m, chunk, st)
+        assert_close(got, _oracle(m), kv, f"{kv} G={g} L={L} chunk={chunk}")
+        assert int(st.item()) == 0
