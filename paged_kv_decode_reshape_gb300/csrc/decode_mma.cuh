@@ -1,5 +1,5 @@
 // decode_mma.cuh -- split-K paged decode attention, kernel 1 of 2, tensor-core path (head_dim 128,
-// bf16 or INT8 K/V, up to 8 query heads per kv head).
+// bf16 or INT8 K/V, 8 MMA columns per CTA).
 //
 // Same unit and outputs as the CUDA-core kernel (decode_split.cuh): one CTA per (sequence b,
 // kv head, split) for the GQA group of that kv head ("EchoLLMServing inference framework
@@ -8,6 +8,11 @@
 // consumed: the per-block work is a dense [16 tokens x 128] x [128 x 8 heads] product and its
 // transpose, done with warp-level mma.sync m16n8k16 so that one instruction covers what took
 // 64 FMAs plus conversions, and the kernel stays far from the issue limit at HBM speed.
+//
+// The 8 MMA columns are query heads of one (sequence, query token) row, or, in packed multi-token
+// decode, the (token, head) pairs of one sequence's kv head, each column masked at its own causal
+// limit. With kv_start > 0 (shared-prefix calls) the CTA covers only tokens [kv_start, n) and
+// always emits a partial state: the prefix is merged in from the tcgen05 prefix kernel.
 //
 // Warp roles: every warp is its own producer and consumer. Warp w takes blocks w, w+NC, ... of
 // the split (NC warps per CTA) and owns the stages w, w+NC, ... of a STAGES-deep shared-memory
