@@ -491,6 +491,75 @@ def prefill_flops(w) -> int:
     return 4 * w.D * w.Hq * vis
 
 
+def run_multi(args):
+    """Multi-token decode (MTP verification): every sequence of config --config gets its last L
+    context positions as new query tokens, attending causally. Times the attention call
+    (pkv_paged_decode_attention_multi) with a flushed L2 and reports KV GB/s against the measured
+    HBM peak; the KV bytes are those of the one-token step (the L tokens share the context)."""
+    import torch
+
+    import paged_kv_decode_reshape_gb300 as pkv
+    pkv.load(build_if_missing=False)
+    L = args.multi
+    w = W.make_multi_token(W.make_config(args.config), L, seed=3)
+
+    def up(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(a).cuda()
+    q, kp, vp = up(w.q), up(w.k_pool), up(w.v_pool)
+    ks, vs = up(w.k_scales), up(w.v_scales)
+    bt, cl = up(w.block_tables), up(w.context_lens)
+    out = torch.empty_like(q)
+    maxc = w.max_context_len
+    nb = pkv.decode_workspace_bytes(w.B * L, w.Hq, w.Hkv, w.D, maxc, args.chunk)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    clean = torch.zeros(L2_FLUSH_BYTES // 2, dtype=torch.int32, device="cuda")
+
+    def call():
+        pkv.paged_decode_attention_multi(out, q, kp, vp, bt, cl, maxc, w.scale, ks, vs, args.chunk,
+                                         ws, status)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"kernels flagged bad inputs: status {int(status.item())}")
+    K = max(1, min(args.steps, 500))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    for k in range(K):
+        flush.fill_(k & 0xFF)
+        clean.max()
+        ev[k][0].record()
+        call()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    kvb = attention_bytes(W.make_config(args.config))
+    gbs = kvb / (ms / 1e3) / 1e9
+    hbm, peak_kind = measured_peaks()
+    line = {"metric": "multi-token decode attention KV GB/s (L query tokens per sequence)",
+            "value": round(gbs, 2), "unit": "GB/s", "n_gpus": 1, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "dtype": w.kv_dtype, "data": "synthetic",
+            "config": {"workload": w.name, "tokens_per_sequence": L, "batch": w.B,
+                       "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+                       "l2": "flushed before every call (untimed)"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "peak_kind": f"of {peak_kind}"},
+            "tokens_per_s": round(w.B * L / (ms / 1e3), 1)}
+    if clk is not None:
+        line["clocks"] = clk
+    print(json.dumps(line), flush=True)
+
+
 def run_prefill(args):
     """Paged chunked prefill on tcgen05: 4 sequences x 4096 new prompt tokens after 2048 cached
     tokens, Llama-3-8B heads (32 q / 8 kv, D = 128, bf16). Reports TFLOP/s against the measured
@@ -566,11 +635,16 @@ def main(argv=None):
     ap.add_argument("--no-cascade", action="store_true",
                     help="run a shared-prefix workload through the plain decode call instead of "
                          "the shared-prefix (cascade) call")
+    ap.add_argument("--multi", type=int, default=0, metavar="L",
+                    help="time multi-token decode (L new tokens per sequence, e.g. MTP "
+                         "verification) on the chosen config instead of the decode step")
     ap.add_argument("--prefill", action="store_true",
                     help="time the paged prefill kernel instead of the decode step")
     args = ap.parse_args(argv)
     if args.prefill:
         run_prefill(args)
+    elif args.multi:
+        run_multi(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

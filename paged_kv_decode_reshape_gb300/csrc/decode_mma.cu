@@ -25,10 +25,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <bool kI8>
+template <bool kI8, bool kPacked>
 cudaError_t launch_t(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
     using G = MmaGeom<kI8>;
-    auto kern = mma_split_kernel<kI8>;
+    auto kern = mma_split_kernel<kI8, kPacked>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.packed ? p.B : p.B * p.L), dim3(G::THREADS), G::SMEM, s,
@@ -56,7 +56,8 @@ bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, in
 
 cudaError_t launch_split_mma(const SplitParams& p, bool i8, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
-    return i8 ? launch_t<true>(p, tk, tv, s) : launch_t<false>(p, tk, tv, s);
+    if (p.packed) return i8 ? launch_t<true, true>(p, tk, tv, s) : launch_t<false, true>(p, tk, tv, s);
+    return i8 ? launch_t<true, false>(p, tk, tv, s) : launch_t<false, false>(p, tk, tv, s);
 }
 
 }  // namespace pkv

@@ -147,7 +147,9 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <bool kI8>
+// kPacked: the columns are (query token, head) pairs (packed multi-token decode); a template
+// parameter so that the one-token path keeps its exact instruction stream.
+template <bool kI8, bool kPacked>
 __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const SplitParams p,
                                                                const __grid_constant__ CUtensorMap tmk,
                                                                const __grid_constant__ CUtensorMap tmv) {
@@ -170,13 +172,13 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     // decode -- the (query token, head) pairs of one sequence's kv head, so that the L tokens
     // being verified read each K/V tile once. The splits follow the longest context (the last
     // token's); each column masks the keys past its own context n - (L - 1 - l).
-    const int b = p.packed ? blockIdx.z : blockIdx.z / p.L;
-    const int lq = p.packed ? p.L - 1 : blockIdx.z - b * p.L;  // the token the splits follow
+    const int b = kPacked ? (int)blockIdx.z : (int)blockIdx.z / p.L;
+    const int lq = kPacked ? p.L - 1 : (int)blockIdx.z - b * p.L;  // the token the splits follow
     const int c0 = hc * kMmaHeads;                               // first column of this CTA
-    const int ncols = p.packed ? p.L * p.G : p.G;
+    const int ncols = kPacked ? p.L * p.G : p.G;
     const int nh = ncols - c0 < kMmaHeads ? ncols - c0 : kMmaHeads;  // columns in use
-    auto col_zb = [&](int j) { return p.packed ? b * p.L + (c0 + j) / p.G : (int)blockIdx.z; };
-    auto col_head = [&](int j) { return kvh * p.G + (p.packed ? (c0 + j) % p.G : c0 + j); };
+    auto col_zb = [&](int j) { return kPacked ? b * p.L + (c0 + j) / p.G : (int)blockIdx.z; };
+    auto col_head = [&](int j) { return kvh * p.G + (kPacked ? (c0 + j) % p.G : c0 + j); };
 
     // Inputs (new K/V rows, tables) may come from the previous kernel: wait for it. In a
     // shared-prefix call the previous kernel is the prefix kernel, which releases this one only
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int stored = p.context_lens[b];
     bool bad;
     const int n = query_context_len(stored, p.L, lq, p.MBPS * kBlockSize, &bad);
-    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && (p.packed || lq == 0);
+    const bool reporter = tid == 0 && split == 0 && blockIdx.y == 0 && (kPacked || lq == 0);
     if (bad && reporter) flag(p.status, PKV_FLAG_BAD_CONTEXT);
     else if (stored > p.max_context_len && reporter) flag(p.status, PKV_FLAG_LONG_CONTEXT);
     // tokens [kv_start, n) are this kernel's (kv_start > 0: a shared prefix is handled elsewhere)
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int r = lane >> 2;  // fragment row group: token (QK) / head (B operand)
     const int c = lane & 3;   // thread in group: head pair 2c, 2c+1 of the C fragments
     // context of columns 2c and 2c + 1 (packed: token (c0 + col) / G sees n - (L - 1 - l) keys)
-    auto col_ctx = [&](int j) { return p.packed ? n - (p.L - 1 - (c0 + j) / p.G) : n; };
+    auto col_ctx = [&](int j) { return kPacked ? n - (p.L - 1 - (c0 + j) / p.G) : n; };
     const int ncol_lim0 = col_ctx(2 * c), ncol_lim1 = col_ctx(2 * c + 1);
 
     float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
@@ -377,8 +379,8 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                 // s[0] = (tok r, head 2c), s[1] = (tok r, 2c+1), s[2] = (tok r+8, 2c), s[3] = (tok r+8, 2c+1)
                 const int nvalid = t1 - (t0 + j * kBlockSize);  // >= 1; >= 16 for full blocks
                 // keys of this block visible to this lane's columns 2c and 2c + 1
-                const int lim0 = min(nvalid, ncol_lim0 - (t0 + j * kBlockSize));
-                const int lim1 = min(nvalid, ncol_lim1 - (t0 + j * kBlockSize));
+                const int lim0 = kPacked ? min(nvalid, ncol_lim0 - (t0 + j * kBlockSize)) : nvalid;
+                const int lim1 = kPacked ? min(nvalid, ncol_lim1 - (t0 + j * kBlockSize)) : nvalid;
                 float vs0 = 1.f, vs1 = 1.f;
                 if constexpr (kI8) {
                     const float* sc = scl + st * 2 * kBlockSize;
