@@ -190,6 +190,30 @@ def test_int8_dequant_uses_per_token_scales(orc):
     np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=F64_TOL)
 
 
+def test_int8_scores_use_each_tokens_k_scale(orc):
+    """Two tokens with int8 K codes 1 and 2 under K scales 0.05 and 0.01 and V codes 10 and -10
+    under V scales 0.1 and 0.2: scores are 64 * 0.05 / 8 = 0.4 and 64 * 0.02 / 8 = 0.16, so the
+    output is the two-key logistic mix w * 1.0 + (1 - w) * (-2.0) with w = 1 / (1 + e^-0.24).
+    Dequantising K with the V scales (or V with the K scales) gives other scores or values."""
+    D = 64
+    kp = np.zeros((1, 1, 16, D), np.int8)
+    vp = np.zeros((1, 1, 16, D), np.int8)
+    kp[0, 0, 0, :], kp[0, 0, 1, :] = 1, 2
+    vp[0, 0, 0, :], vp[0, 0, 1, :] = 10, -10
+    ks = np.zeros((1, 1, 16), np.float32)
+    vs = np.zeros((1, 1, 16), np.float32)
+    ks[0, 0, :2] = [0.05, 0.01]
+    vs[0, 0, :2] = [0.1, 0.2]
+    q = W.f32_to_bf16_bits(np.ones((1, 1, D), np.float32))
+    out = orc.paged_decode_attention(q, kp, vp, np.array([[0]], np.int32), np.array([2], np.int32),
+                                     1.0 / 8.0, ks, vs)
+    s0 = D * float(np.float32(0.05)) / 8.0
+    s1 = D * 2 * float(np.float32(0.01)) / 8.0
+    w = 1.0 / (1.0 + math.exp(-(s0 - s1)))
+    expect = w * 10 * float(np.float32(0.1)) + (1.0 - w) * (-10) * float(np.float32(0.2))
+    np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=F64_TOL)
+
+
 def test_context_len_zero_gives_zeros(orc):
     w = W.make_decode(name="z", B=3, Hq=2, Hkv=1, D=64, context_lens=[0, 5, 0], kv_dtype="f32",
                       q_dtype="f32", seed=1)
