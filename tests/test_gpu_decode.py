@@ -313,3 +313,32 @@ def test_runs_on_the_callers_stream():
         out = d2.step()
     s.synchronize()
     assert np.array_equal(to_f64(out), ref)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "i8"])
+@pytest.mark.parametrize("shape", [
+    dict(B=1, Hq=32, Hkv=8, lens="131072"),            # one sequence at the longest context
+    dict(B=512, Hq=32, Hkv=8, lens="1-200"),           # many short sequences
+    dict(B=16, Hq=64, Hkv=8, lens="100-3000"),         # 8 query heads per kv head
+    dict(B=16, Hq=16, Hkv=16, lens="100-3000"),        # MHA: one query head per kv head
+    dict(B=8, Hq=32, Hkv=2, lens="100-3000"),          # 16 query heads per kv head: two CTA groups
+    dict(B=12, Hq=20, Hkv=5, lens="1-2000"),           # odd kv-head count, G = 4
+], ids=["B1_131k", "B512_short", "G8", "MHA", "G16", "Hkv5"])
+def test_shape_sweep_sampled_rows(shape, kv):
+    """Shapes beyond the five workloads, in the auto launch configuration, checked against the
+    oracle on a sample of sequences (every head), including the longest."""
+    rng = np.random.default_rng(shape["B"] * 7 + shape["Hkv"])
+    lo_hi = shape["lens"].split("-")
+    if len(lo_hi) == 1:
+        lens = np.full(shape["B"], int(lo_hi[0]))
+    else:
+        lens = rng.integers(int(lo_hi[0]), int(lo_hi[1]) + 1, size=shape["B"])
+    w = W.make_decode(name="sweep", B=shape["B"], Hq=shape["Hq"], Hkv=shape["Hkv"], D=128,
+                      context_lens=lens, kv_dtype=kv, q_dtype="bf16", seed=int(lens.sum() % 1000))
+    rows = sorted({0, shape["B"] - 1, shape["B"] // 2, int(np.argmax(w.context_lens))})
+    d = DevWorkload(w)
+    st = status_tensor()
+    got = to_f64(d.step(status=st))[rows]
+    ref = oracle_step(w, rows=rows, num_threads=16)
+    assert_close(got, ref, kv, f"{shape} {kv} rows {rows}")
+    assert int(st.item()) == 0
