@@ -15,7 +15,7 @@ BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libpkv.so")
 
 SOURCES = ["pkv_api.cu", "kv_write.cu", "decode_f32.cu", "decode_bf16.cu", "decode_i8.cu",
-           "decode_mma.cu", "splitk_merge.cu", "decode_static_ws.cu", "block_manager.cpp",
+           "decode_mma.cu", "decode_mma2.cu", "splitk_merge.cu", "decode_static_ws.cu", "block_manager.cpp",
            "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

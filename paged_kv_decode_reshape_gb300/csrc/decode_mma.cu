@@ -1,5 +1,6 @@
-// decode_mma.cu -- instantiates the tensor-core split kernel (bf16 and INT8 K/V, head_dim 128)
-// and builds the TMA tensor maps that describe a K or V pool to the copy engine.
+// decode_mma.cu -- instantiates the tensor-core split kernel with one n-tile (bf16 and INT8 K/V,
+// head_dim 128; decode_mma2.cu has the two-n-tile kernels) and builds the TMA tensor maps that
+// describe a K or V pool to the copy engine.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -27,8 +28,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 template <bool kI8, bool kPacked>
 cudaError_t launch_t(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-    using G = MmaGeom<kI8>;
-    auto kern = mma_split_kernel<kI8, kPacked>;
+    using G = MmaGeom<kI8, 1>;
+    auto kern = mma_split_kernel<kI8, kPacked, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.max_splits, p.Hkv * p.head_chunks, p.packed ? p.B : p.B * p.L), dim3(G::THREADS), G::SMEM, s,
@@ -56,6 +57,7 @@ bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, in
 
 cudaError_t launch_split_mma(const SplitParams& p, bool i8, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
+    if (p.ntiles == 2) return launch_split_mma_nt2(p, i8, tk, tv, s);
     if (p.packed) return i8 ? launch_t<true, true>(p, tk, tv, s) : launch_t<false, true>(p, tk, tv, s);
     return i8 ? launch_t<true, false>(p, tk, tv, s) : launch_t<false, false>(p, tk, tv, s);
 }

@@ -69,7 +69,7 @@ constexpr int kMmaHeads = 8;        // MMA N: query heads per CTA
 #endif
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 
-template <bool kI8>
+template <bool kI8, int kNT = 1>
 struct MmaGeom {
     static constexpr int NC = kI8 ? PKV_MMA_WARPS_I8 : PKV_MMA_WARPS_BF16;  // warps per CTA
     static constexpr int SPW = kI8 ? PKV_MMA_SPW_I8 : PKV_MMA_SPW_BF16;     // stages per warp
@@ -83,7 +83,8 @@ struct MmaGeom {
     static constexpr int STAGES = NC * SPW;
     static constexpr int RING = STAGES * STAGE;
     static constexpr int SCALES = kI8 ? STAGES * 2 * kBlockSize * 4 : 0;
-    static constexpr int MERGE = NC * kMmaHeads * (kMmaD + 2) * 4;
+    static constexpr int NCOL = kMmaHeads * kNT;                     // MMA columns per CTA
+    static constexpr int MERGE = NC * NCOL * (kMmaD + 2) * 4;
     static constexpr int MAIN = RING > MERGE ? RING : MERGE;
     // + 1024 for aligning the ring to the 128-byte-swizzle atom
     static constexpr int SMEM = 1024 + MAIN + SCALES + STAGES * 8;
@@ -149,12 +150,14 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 
 // kPacked: the columns are (query token, head) pairs (packed multi-token decode); a template
 // parameter so that the one-token path keeps its exact instruction stream.
-template <bool kI8, bool kPacked>
-__global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const SplitParams p,
+// kNT: 8-column MMA n-tiles per CTA. With 2, a warp reads and widens each K/V tile once for 16
+// columns (G = 16, or multi-token rows of G = 8).
+template <bool kI8, bool kPacked, int kNT>
+__global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(const SplitParams p,
                                                                const __grid_constant__ CUtensorMap tmk,
                                                                const __grid_constant__ CUtensorMap tmv) {
-    using G = MmaGeom<kI8>;
-    constexpr int STAGES = G::STAGES, STAGE = G::STAGE, TILE = G::TILE;
+    using G = MmaGeom<kI8, kNT>;
+    constexpr int STAGES = G::STAGES, STAGE = G::STAGE, TILE = G::TILE, NCOL = G::NCOL;
     constexpr float kNegInf = -INFINITY;
 
     extern __shared__ unsigned char smem_raw[];
@@ -174,9 +177,9 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     // token's); each column masks the keys past its own context n - (L - 1 - l).
     const int b = kPacked ? (int)blockIdx.z : (int)blockIdx.z / p.L;
     const int lq = kPacked ? p.L - 1 : (int)blockIdx.z - b * p.L;  // the token the splits follow
-    const int c0 = hc * kMmaHeads;                               // first column of this CTA
+    const int c0 = hc * NCOL;                                    // first column of this CTA
     const int ncols = kPacked ? p.L * p.G : p.G;
-    const int nh = ncols - c0 < kMmaHeads ? ncols - c0 : kMmaHeads;  // columns in use
+    const int nh = ncols - c0 < NCOL ? ncols - c0 : NCOL;        // columns in use
     auto col_zb = [&](int j) { return kPacked ? b * p.L + (c0 + j) / p.G : (int)blockIdx.z; };
     auto col_head = [&](int j) { return kvh * p.G + (kPacked ? (c0 + j) % p.G : c0 + j); };
 
@@ -226,12 +229,23 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     const int c = lane & 3;   // thread in group: head pair 2c, 2c+1 of the C fragments
     // context of columns 2c and 2c + 1 (packed: token (c0 + col) / G sees n - (L - 1 - l) keys)
     auto col_ctx = [&](int j) { return kPacked ? n - (p.L - 1 - (c0 + j) / p.G) : n; };
-    const int ncol_lim0 = col_ctx(2 * c), ncol_lim1 = col_ctx(2 * c + 1);
-
-    float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
-    float o[8][4];
+    int ncol_lim[kNT][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int t = 0; t < kNT; ++t) {
+        ncol_lim[t][0] = col_ctx(8 * t + 2 * c);
+        ncol_lim[t][1] = col_ctx(8 * t + 2 * c + 1);
+    }
+
+    // per n-tile t: running max / sum of this lane's columns 8t + 2c, 8t + 2c + 1, and O^T
+    float m[kNT][2], l[kNT][2];
+    float o[kNT][8][4];
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        m[t][0] = m[t][1] = kNegInf;
+        l[t][0] = l[t][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[t][i][0] = o[t][i][1] = o[t][i][2] = o[t][i][3] = 0.f;
+    }
 
     // ---- this warp's blocks: k-th is split block j = warp + k * NC, in stage warp + (k % SPW) * NC ----
     constexpr int NC = G::NC, SPW = G::SPW;
@@ -286,12 +300,15 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
 
     {
         // q as the B operand of S^T = K Q^T: b0b1 = (dims k0 + 2c, +1; head r), b2b3 = (+8, +9)
-        uint32_t qb[8][2];
-        float qsum = 0.f;  // INT8: sum of this lane's fp16 q' values of head r (as the MMA sees them)
-        {
-            const bool hv = r < nh;
+        uint32_t qb[kNT][8][2];
+        float qsum[kNT];  // INT8: sum of this lane's fp16 q' values of column 8t + r (as the MMA sees them)
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            qsum[t] = 0.f;
+            const bool hv = 8 * t + r < nh;
+            const int col = hv ? 8 * t + r : 0;
             const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                        ((size_t)col_zb(hv ? r : 0) * p.Hq + col_head(hv ? r : 0)) * kMmaD;
+                                        ((size_t)col_zb(col) * p.Hq + col_head(col)) * kMmaD;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 if constexpr (kI8) {
@@ -302,24 +319,30 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                     bf16x2_to_f32(raw4.x, f0, f1);
                     bf16x2_to_f32(raw4.y, f2, f3);
                     const float sc = p.scale_log2;
-                    qb[ks][0] = hv ? pack_h2(f0 * sc, f2 * sc) : 0u;
-                    qb[ks][1] = hv ? pack_h2(f1 * sc, f3 * sc) : 0u;
-                    const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[ks][0]));
-                    const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[ks][1]));
-                    qsum += (u0.x + u0.y) + (u1.x + u1.y);
+                    qb[t][ks][0] = hv ? pack_h2(f0 * sc, f2 * sc) : 0u;
+                    qb[t][ks][1] = hv ? pack_h2(f1 * sc, f3 * sc) : 0u;
+                    const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[t][ks][0]));
+                    const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[t][ks][1]));
+                    qsum[t] += (u0.x + u0.y) + (u1.x + u1.y);
                 } else {
-                    qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c) : 0u;
-                    qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c + 8) : 0u;
+                    qb[t][ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c) : 0u;
+                    qb[t][ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c + 8) : 0u;
                 }
             }
         }
-        // INT8: 1152 * sum_d q'_d of heads 2c and 2c+1 is what the biased K adds to each score
-        float kcorr0 = 0.f, kcorr1 = 0.f, psum[2] = {0.f, 0.f};
-        if constexpr (kI8) {
-            qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-            qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // lanes 4r..4r+3: head r's full sum
-            kcorr0 = kI8Bias * __shfl_sync(0xffffffffu, qsum, 4 * (2 * c));
-            kcorr1 = kI8Bias * __shfl_sync(0xffffffffu, qsum, 4 * (2 * c + 1));
+        // INT8: 1152 * sum_d q'_d of columns 2c and 2c+1 is what the biased K adds to each score
+        float kcorr[kNT][2], psum[kNT][2];
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            kcorr[t][0] = kcorr[t][1] = 0.f;
+            psum[t][0] = psum[t][1] = 0.f;
+            if constexpr (kI8) {
+                float qs = qsum[t];
+                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 2);  // lanes 4r..4r+3: column r's full sum
+                kcorr[t][0] = kI8Bias * __shfl_sync(0xffffffffu, qs, 4 * (2 * c));
+                kcorr[t][1] = kI8Bias * __shfl_sync(0xffffffffu, qs, 4 * (2 * c + 1));
+            }
         }
 #pragma unroll 1
         for (int k = 0; k < nmine; ++k) {
@@ -344,8 +367,10 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
             if (bid >= 0) {
                 const uint32_t kt = ring + st * STAGE;
                 const uint32_t vt = kt + TILE;
-                // ---- S^T = K . Q^T ----
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                // ---- S^T = K . Q^T (each K fragment serves every n-tile) ----
+                float s[kNT][4];
+#pragma unroll
+                for (int t = 0; t < kNT; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
                 const int lr = lane & 7, mi = lane >> 3;
                 if constexpr (kI8) {
 #pragma unroll
@@ -363,7 +388,9 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                             a[1] = i8_lo_h2(hi);
                             a[2] = i8_hi_h2(lo);
                             a[3] = i8_hi_h2(hi);
-                            mma16816<true>(s, a, qb[2 * kp + h][0], qb[2 * kp + h][1]);
+#pragma unroll
+                            for (int t = 0; t < kNT; ++t)
+                                mma16816<true>(s[t], a, qb[t][2 * kp + h][0], qb[t][2 * kp + h][1]);
                         }
                     }
                 } else {
@@ -373,74 +400,94 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                         const int ch = (ks & 3) * 2 + (mi >> 1);
                         uint32_t a[4];
                         ldsm_x4(kt + (ks >> 2) * G::BOX + y * 128 + ((ch ^ (y & 7)) << 4), a);
-                        mma16816<false>(s, a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                        for (int t = 0; t < kNT; ++t) mma16816<false>(s[t], a, qb[t][ks][0], qb[t][ks][1]);
                     }
                 }
-                // s[0] = (tok r, head 2c), s[1] = (tok r, 2c+1), s[2] = (tok r+8, 2c), s[3] = (tok r+8, 2c+1)
+                // s[t][0] = (tok r, col 8t+2c), [1] = (tok r, 8t+2c+1), [2] = (tok r+8, 8t+2c), [3] = (tok r+8, 8t+2c+1)
                 const int nvalid = t1 - (t0 + j * kBlockSize);  // >= 1; >= 16 for full blocks
-                // keys of this block visible to this lane's columns 2c and 2c + 1
-                const int lim0 = kPacked ? min(nvalid, ncol_lim0 - (t0 + j * kBlockSize)) : nvalid;
-                const int lim1 = kPacked ? min(nvalid, ncol_lim1 - (t0 + j * kBlockSize)) : nvalid;
-                float vs0 = 1.f, vs1 = 1.f;
+                float vs0 = 1.f, vs1 = 1.f, ks0 = 1.f, ks1 = 1.f;
                 if constexpr (kI8) {
                     const float* sc = scl + st * 2 * kBlockSize;
-                    const float ks0 = sc[r], ks1 = sc[r + 8];
+                    ks0 = sc[r];
+                    ks1 = sc[r + 8];
                     vs0 = sc[kBlockSize + r];
                     vs1 = sc[kBlockSize + r + 8];
-                    s[0] = (s[0] - kcorr0) * ks0; s[1] = (s[1] - kcorr1) * ks0;
-                    s[2] = (s[2] - kcorr0) * ks1; s[3] = (s[3] - kcorr1) * ks1;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[e] *= p.scale_log2;
                 }
-                s[0] = r < lim0 ? s[0] : kNegInf;
-                s[1] = r < lim1 ? s[1] : kNegInf;
-                s[2] = r + 8 < lim0 ? s[2] : kNegInf;
-                s[3] = r + 8 < lim1 ? s[3] : kNegInf;
-                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+                float mx[kNT][2];
+                bool up[kNT][2];
+                bool any_up = false;
 #pragma unroll
-                for (int off = 4; off <= 16; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                for (int t = 0; t < kNT; ++t) {
+                    // keys of this block visible to this lane's columns 8t + 2c and 8t + 2c + 1
+                    const int lim0 = kPacked ? min(nvalid, ncol_lim[t][0] - (t0 + j * kBlockSize)) : nvalid;
+                    const int lim1 = kPacked ? min(nvalid, ncol_lim[t][1] - (t0 + j * kBlockSize)) : nvalid;
+                    if constexpr (kI8) {
+                        s[t][0] = (s[t][0] - kcorr[t][0]) * ks0; s[t][1] = (s[t][1] - kcorr[t][1]) * ks0;
+                        s[t][2] = (s[t][2] - kcorr[t][0]) * ks1; s[t][3] = (s[t][3] - kcorr[t][1]) * ks1;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s[t][e] *= p.scale_log2;
+                    }
+                    s[t][0] = r < lim0 ? s[t][0] : kNegInf;
+                    s[t][1] = r < lim1 ? s[t][1] : kNegInf;
+                    s[t][2] = r + 8 < lim0 ? s[t][2] : kNegInf;
+                    s[t][3] = r + 8 < lim1 ? s[t][3] : kNegInf;
+                    mx[t][0] = fmaxf(s[t][0], s[t][2]);
+                    mx[t][1] = fmaxf(s[t][1], s[t][3]);
+#pragma unroll
+                    for (int off = 4; off <= 16; off <<= 1) {
+                        mx[t][0] = fmaxf(mx[t][0], __shfl_xor_sync(0xffffffffu, mx[t][0], off));
+                        mx[t][1] = fmaxf(mx[t][1], __shfl_xor_sync(0xffffffffu, mx[t][1], off));
+                    }
+                    up[t][0] = mx[t][0] > m[t][0] + kRescaleThreshold;
+                    up[t][1] = mx[t][1] > m[t][1] + kRescaleThreshold;
+                    any_up = any_up || up[t][0] || up[t][1];
                 }
-                const bool up0 = mx0 > m[0] + kRescaleThreshold;
-                const bool up1 = mx1 > m[1] + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, up0 || up1)) {
-                    const float n0 = up0 ? mx0 : m[0], n1 = up1 ? mx1 : m[1];
-                    const float a0 = up0 ? ex2(m[0] - n0) : 1.f, a1 = up1 ? ex2(m[1] - n1) : 1.f;
-                    m[0] = n0;
-                    m[1] = n1;
-                    l[0] *= a0;
-                    l[1] *= a1;
-                    psum[0] *= a0;
-                    psum[1] *= a1;
+                if (__any_sync(0xffffffffu, any_up)) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        o[i][0] *= a0; o[i][2] *= a0;
-                        o[i][1] *= a1; o[i][3] *= a1;
+                    for (int t = 0; t < kNT; ++t) {
+                        const float n0 = up[t][0] ? mx[t][0] : m[t][0], n1 = up[t][1] ? mx[t][1] : m[t][1];
+                        const float a0 = up[t][0] ? ex2(m[t][0] - n0) : 1.f;
+                        const float a1 = up[t][1] ? ex2(m[t][1] - n1) : 1.f;
+                        m[t][0] = n0;
+                        m[t][1] = n1;
+                        l[t][0] *= a0;
+                        l[t][1] *= a1;
+                        psum[t][0] *= a0;
+                        psum[t][1] *= a1;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o[t][i][0] *= a0; o[t][i][2] *= a0;
+                            o[t][i][1] *= a1; o[t][i][3] *= a1;
+                        }
                     }
                 }
-                const float ms0 = m[0] == kNegInf ? 0.f : m[0], ms1 = m[1] == kNegInf ? 0.f : m[1];
-                const float p0 = ex2(s[0] - ms0), p1 = ex2(s[1] - ms1);
-                const float p2 = ex2(s[2] - ms0), p3 = ex2(s[3] - ms1);
-                l[0] += p0 + p2;
-                l[1] += p1 + p3;
                 // ---- O^T += V^T . P^T ----
-                uint32_t pb0, pb1;
-                if constexpr (kI8) {
-                    const uint32_t h01 = pack_h2(p0 * vs0, p1 * vs0);
-                    const uint32_t h23 = pack_h2(p2 * vs1, p3 * vs1);
-                    // the weights exactly as the MMA uses them: their sum times 1152 is what
-                    // the biased V adds to each output
-                    const float2 w01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-                    const float2 w23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-                    psum[0] += w01.x + w23.x;
-                    psum[1] += w01.y + w23.y;
-                    pb0 = movm_t(h01);
-                    pb1 = movm_t(h23);
-                } else {
-                    pb0 = movm_t(pack_bf16(p0, p1));
-                    pb1 = movm_t(pack_bf16(p2, p3));
+                uint32_t pb[kNT][2];
+#pragma unroll
+                for (int t = 0; t < kNT; ++t) {
+                    const float ms0 = m[t][0] == kNegInf ? 0.f : m[t][0];
+                    const float ms1 = m[t][1] == kNegInf ? 0.f : m[t][1];
+                    const float p0 = ex2(s[t][0] - ms0), p1 = ex2(s[t][1] - ms1);
+                    const float p2 = ex2(s[t][2] - ms0), p3 = ex2(s[t][3] - ms1);
+                    l[t][0] += p0 + p2;
+                    l[t][1] += p1 + p3;
+                    if constexpr (kI8) {
+                        const uint32_t h01 = pack_h2(p0 * vs0, p1 * vs0);
+                        const uint32_t h23 = pack_h2(p2 * vs1, p3 * vs1);
+                        // the weights exactly as the MMA uses them: their sum times 1152 is what
+                        // the biased V adds to each output
+                        const float2 w01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+                        const float2 w23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+                        psum[t][0] += w01.x + w23.x;
+                        psum[t][1] += w01.y + w23.y;
+                        pb[t][0] = movm_t(h01);
+                        pb[t][1] = movm_t(h23);
+                    } else {
+                        pb[t][0] = movm_t(pack_bf16(p0, p1));
+                        pb[t][1] = movm_t(pack_bf16(p2, p3));
+                    }
                 }
                 const bool partial = nvalid < kBlockSize;
                 if constexpr (kI8) {
@@ -465,7 +512,8 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                             a[1] = i8_hi_h2(t0w);
                             a[2] = i8_lo_h2(t8w);
                             a[3] = i8_hi_h2(t8w);
-                            mma16816<true>(o[2 * jp + h], a, pb0, pb1);
+#pragma unroll
+                            for (int t = 0; t < kNT; ++t) mma16816<true>(o[t][2 * jp + h], a, pb[t][0], pb[t][1]);
                         }
                     }
                 } else {
@@ -483,7 +531,8 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
                             const uint32_t mhi = (k8 ? 0xffffu : 0u) | (k9 ? 0xffff0000u : 0u);
                             a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
                         }
-                        mma16816<false>(o[i], a, pb0, pb1);
+#pragma unroll
+                        for (int t = 0; t < kNT; ++t) mma16816<false>(o[t][i], a, pb[t][0], pb[t][1]);
                     }
                 }
             }
@@ -500,19 +549,22 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
         }
         // finish l (and the INT8 weight sums) over the 8 token rows (lanes with the same c)
 #pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) {
-            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
-            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
-            if constexpr (kI8) {
-                psum[0] += __shfl_xor_sync(0xffffffffu, psum[0], off);
-                psum[1] += __shfl_xor_sync(0xffffffffu, psum[1], off);
-            }
-        }
-        if constexpr (kI8) {  // remove the 1152 offset of the biased V from every output
+        for (int t = 0; t < kNT; ++t) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                o[i][0] -= kI8Bias * psum[0]; o[i][2] -= kI8Bias * psum[0];
-                o[i][1] -= kI8Bias * psum[1]; o[i][3] -= kI8Bias * psum[1];
+            for (int off = 4; off <= 16; off <<= 1) {
+                l[t][0] += __shfl_xor_sync(0xffffffffu, l[t][0], off);
+                l[t][1] += __shfl_xor_sync(0xffffffffu, l[t][1], off);
+                if constexpr (kI8) {
+                    psum[t][0] += __shfl_xor_sync(0xffffffffu, psum[t][0], off);
+                    psum[t][1] += __shfl_xor_sync(0xffffffffu, psum[t][1], off);
+                }
+            }
+            if constexpr (kI8) {  // remove the 1152 offset of the biased V from every output
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[t][i][0] -= kI8Bias * psum[t][0]; o[t][i][2] -= kI8Bias * psum[t][0];
+                    o[t][i][1] -= kI8Bias * psum[t][1]; o[t][i][3] -= kI8Bias * psum[t][1];
+                }
             }
         }
     }
@@ -524,42 +576,46 @@ __global__ void __launch_bounds__(MmaGeom<kI8>::THREADS) mma_split_kernel(const 
     }
     grid_dependents_launch();  // the merge kernel may start launching
     // ---- merge the consumer warps' states (ring memory reused) ----
-    float* sm_m = reinterpret_cast<float*>(smem);               // [NC][8]
-    float* sm_l = sm_m + G::NC * kMmaHeads;               // [NC][8]
-    float* sm_o = sm_l + G::NC * kMmaHeads;               // [NC][8][128]
+    float* sm_m = reinterpret_cast<float*>(smem);               // [NC][NCOL]
+    float* sm_l = sm_m + G::NC * NCOL;                          // [NC][NCOL]
+    float* sm_o = sm_l + G::NC * NCOL;                          // [NC][NCOL][128]
     {
-        if (r == 0) {
-            sm_m[warp * 8 + 2 * c] = m[0];
-            sm_m[warp * 8 + 2 * c + 1] = m[1];
-            sm_l[warp * 8 + 2 * c] = l[0];
-            sm_l[warp * 8 + 2 * c + 1] = l[1];
-        }
-        float* ow = sm_o + warp * kMmaHeads * kMmaD;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int d0 = kI8 ? 16 * i + 2 * r : 16 * i + r;
-            const int d1 = kI8 ? d0 + 1 : d0 + 8;
-            ow[(2 * c) * kMmaD + d0] = o[i][0];
-            ow[(2 * c + 1) * kMmaD + d0] = o[i][1];
-            ow[(2 * c) * kMmaD + d1] = o[i][2];
-            ow[(2 * c + 1) * kMmaD + d1] = o[i][3];
+        for (int t = 0; t < kNT; ++t) {
+            const int cl = 8 * t + 2 * c;
+            if (r == 0) {
+                sm_m[warp * NCOL + cl] = m[t][0];
+                sm_m[warp * NCOL + cl + 1] = m[t][1];
+                sm_l[warp * NCOL + cl] = l[t][0];
+                sm_l[warp * NCOL + cl + 1] = l[t][1];
+            }
+            float* ow = sm_o + warp * NCOL * kMmaD;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d0 = kI8 ? 16 * i + 2 * r : 16 * i + r;
+                const int d1 = kI8 ? d0 + 1 : d0 + 8;
+                ow[cl * kMmaD + d0] = o[t][i][0];
+                ow[(cl + 1) * kMmaD + d0] = o[t][i][1];
+                ow[cl * kMmaD + d1] = o[t][i][2];
+                ow[(cl + 1) * kMmaD + d1] = o[t][i][3];
+            }
         }
     }
     __syncthreads();
-    for (int e = tid; e < kMmaHeads * kMmaD; e += G::THREADS) {
+    for (int e = tid; e < NCOL * kMmaD; e += G::THREADS) {
         const int hh = e / kMmaD, d = e % kMmaD;
         if (hh >= nh) continue;
         const int zb = col_zb(hh);
         float M = kNegInf;
 #pragma unroll
-        for (int w = 0; w < G::NC; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
+        for (int w = 0; w < G::NC; ++w) M = fmaxf(M, sm_m[w * NCOL + hh]);
         float L = 0.f, A = 0.f;
         if (M != kNegInf) {
 #pragma unroll
             for (int w = 0; w < G::NC; ++w) {
-                const float wt = ex2(sm_m[w * 8 + hh] - M);
-                L = fmaf(wt, sm_l[w * 8 + hh], L);
-                A = fmaf(wt, sm_o[(w * kMmaHeads + hh) * kMmaD + d], A);
+                const float wt = ex2(sm_m[w * NCOL + hh] - M);
+                L = fmaf(wt, sm_l[w * NCOL + hh], L);
+                A = fmaf(wt, sm_o[(w * NCOL + hh) * kMmaD + d], A);
             }
         }
         const size_t qh = (size_t)zb * p.Hq + col_head(hh);

@@ -114,12 +114,27 @@ pkv_status run_decode(const Decode& a) {
     // head_dim 64 on the CUDA-core kernel
     const bool mma = uses_mma(a.D, a.kv_dtype);
     const int hg = mma ? 8 : heads_per_cta(g);
-    // multi-token decode on the tensor-core kernel: pack the (token, head) pairs of a sequence's
-    // kv head into the kernel's 8 columns when that takes fewer passes over K/V than one row
-    // (query token) at a time
-    const bool packed = mma && a.L > 1 && a.prefix == 0 &&
-                        (long long)(a.L * g + 7) / 8 < (long long)a.L * ((g + 7) / 8);
-    const int head_chunks = packed ? (a.L * g + 7) / 8 : (g + hg - 1) / hg;
+    // Tensor-core kernel: 8 or 16 MMA columns per CTA (one or two n-tiles), holding the query
+    // heads of one (sequence, query token) row, or -- multi-token decode -- the (token, head)
+    // pairs of a sequence's kv head. Pick the layout with the fewest passes over each sequence's
+    // K/V, the narrower and unpacked one on ties.
+    bool packed = false;
+    int ntiles = 1, head_chunks = (g + hg - 1) / hg;
+    if (mma) {
+        long long best = -1;
+        for (int nt = 1; nt <= 2; ++nt)
+            for (int pk = 0; pk <= (a.L > 1 && a.prefix == 0 ? 1 : 0); ++pk) {
+                const int cap = 8 * nt;
+                const long long passes = pk ? (long long)(a.L * g + cap - 1) / cap
+                                            : (long long)a.L * ((g + cap - 1) / cap);
+                if (best < 0 || passes < best) {
+                    best = passes;
+                    ntiles = nt;
+                    packed = pk;
+                    head_chunks = pk ? (a.L * g + cap - 1) / cap : (g + cap - 1) / cap;
+                }
+            }
+    }
     if ((long long)a.NB * a.Hkv * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // TMA row index
     if ((long long)a.Hkv * head_chunks > 65535 || a.Hq > 65535) return PKV_ERR_UNSUPPORTED;
 
@@ -173,6 +188,7 @@ pkv_status run_decode(const Decode& a) {
     p.always_partial = P > 0;
     p.ws_stride = Sw;
     p.packed = packed;
+    p.ntiles = ntiles;
 
     cudaError_t e;
     if (mma) {

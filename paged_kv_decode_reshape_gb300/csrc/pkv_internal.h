@@ -71,6 +71,7 @@ struct SplitParams {
     int always_partial;         // write (m, l, acc) even for single-split rows (merged later)
     int ws_stride;              // partial slots per (row, query head) in the workspace (>= max_splits)
     int packed;                 // multi-token: one CTA column per (query token, head) of a sequence
+    int ntiles;                 // tensor-core kernel: 8-column MMA n-tiles per CTA (1 or 2)
 };
 
 struct MergeParams {
@@ -165,6 +166,9 @@ cudaError_t launch_merge(const MergeParams& p, pkv_dtype out_dtype, int D, cudaS
 // Tensor-core split kernel for head_dim 128, bf16 or INT8 pools, 8 query heads per CTA; the K and
 // V pools are described by TMA tensor maps built with make_pool_tensor_map (false on failure).
 bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, bool i8);
+// the kernel with two n-tiles (16 columns per CTA); same arguments as launch_split_mma
+cudaError_t launch_split_mma_nt2(const SplitParams& p, bool i8, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int splits,
                           cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
