@@ -236,12 +236,15 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
         ncol_lim[t][1] = col_ctx(8 * t + 2 * c + 1);
     }
 
-    // per n-tile t: running max / sum of this lane's columns 8t + 2c, 8t + 2c + 1, and O^T
+    // per n-tile t, for this lane's columns 8t + 2c and 8t + 2c + 1: the reference max m (base-2
+    // units; set from the column's first block with a valid key and raised only when a block
+    // exceeds it by more than 2^8), the sum l of 2^(s - m), and O^T. A column that never sees a
+    // valid key keeps l = 0 and reports its max as -inf.
     float m[kNT][2], l[kNT][2];
     float o[kNT][8][4];
 #pragma unroll
     for (int t = 0; t < kNT; ++t) {
-        m[t][0] = m[t][1] = kNegInf;
+        m[t][0] = m[t][1] = 0.f;
         l[t][0] = l[t][1] = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[t][i][0] = o[t][i][1] = o[t][i][2] = o[t][i][3] = 0.f;
@@ -344,6 +347,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                 kcorr[t][1] = kI8Bias * __shfl_sync(0xffffffffu, qs, 4 * (2 * c + 1));
             }
         }
+        bool fresh = true;  // warp-uniform: no block consumed yet, so m is not set
 #pragma unroll 1
         for (int k = 0; k < nmine; ++k) {
             const int j = warp + k * NC;
@@ -368,9 +372,14 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                 const uint32_t kt = ring + st * STAGE;
                 const uint32_t vt = kt + TILE;
                 // ---- S^T = K . Q^T (each K fragment serves every n-tile) ----
+                // INT8: the accumulators start at -1152 * sum q', which removes the bias of the
+                // widened K from every score
                 float s[kNT][4];
 #pragma unroll
-                for (int t = 0; t < kNT; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+                for (int t = 0; t < kNT; ++t) {
+                    s[t][0] = s[t][2] = -kcorr[t][0];
+                    s[t][1] = s[t][3] = -kcorr[t][1];
+                }
                 const int lr = lane & 7, mi = lane >> 3;
                 if constexpr (kI8) {
 #pragma unroll
@@ -406,7 +415,8 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                 }
                 // s[t][0] = (tok r, col 8t+2c), [1] = (tok r, 8t+2c+1), [2] = (tok r+8, 8t+2c), [3] = (tok r+8, 8t+2c+1)
                 const int nvalid = t1 - (t0 + j * kBlockSize);  // >= 1; >= 16 for full blocks
-                float vs0 = 1.f, vs1 = 1.f, ks0 = 1.f, ks1 = 1.f;
+                // score multipliers: the K scale (INT8) or scale * log2(e) (bf16) per token row
+                float vs0 = 1.f, vs1 = 1.f, ks0 = p.scale_log2, ks1 = p.scale_log2;
                 if constexpr (kI8) {
                     const float* sc = scl + st * 2 * kBlockSize;
                     ks0 = sc[r];
@@ -414,63 +424,66 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                     vs0 = sc[kBlockSize + r];
                     vs1 = sc[kBlockSize + r + 8];
                 }
-                float mx[kNT][2];
-                bool up[kNT][2];
+                // d = score - m (base 2), one FFMA per score; keys past a column's limit get -inf
+                float dm[kNT][2];
                 bool any_up = false;
 #pragma unroll
                 for (int t = 0; t < kNT; ++t) {
+                    s[t][0] = fmaf(s[t][0], ks0, -m[t][0]);
+                    s[t][1] = fmaf(s[t][1], ks0, -m[t][1]);
+                    s[t][2] = fmaf(s[t][2], ks1, -m[t][0]);
+                    s[t][3] = fmaf(s[t][3], ks1, -m[t][1]);
                     // keys of this block visible to this lane's columns 8t + 2c and 8t + 2c + 1
                     const int lim0 = kPacked ? min(nvalid, ncol_lim[t][0] - (t0 + j * kBlockSize)) : nvalid;
                     const int lim1 = kPacked ? min(nvalid, ncol_lim[t][1] - (t0 + j * kBlockSize)) : nvalid;
-                    if constexpr (kI8) {
-                        s[t][0] = (s[t][0] - kcorr[t][0]) * ks0; s[t][1] = (s[t][1] - kcorr[t][1]) * ks0;
-                        s[t][2] = (s[t][2] - kcorr[t][0]) * ks1; s[t][3] = (s[t][3] - kcorr[t][1]) * ks1;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) s[t][e] *= p.scale_log2;
+                    if (kPacked ? (lim0 < kBlockSize || lim1 < kBlockSize) : nvalid < kBlockSize) {
+                        s[t][0] = r < lim0 ? s[t][0] : kNegInf;
+                        s[t][1] = r < lim1 ? s[t][1] : kNegInf;
+                        s[t][2] = r + 8 < lim0 ? s[t][2] : kNegInf;
+                        s[t][3] = r + 8 < lim1 ? s[t][3] : kNegInf;
                     }
-                    s[t][0] = r < lim0 ? s[t][0] : kNegInf;
-                    s[t][1] = r < lim1 ? s[t][1] : kNegInf;
-                    s[t][2] = r + 8 < lim0 ? s[t][2] : kNegInf;
-                    s[t][3] = r + 8 < lim1 ? s[t][3] : kNegInf;
-                    mx[t][0] = fmaxf(s[t][0], s[t][2]);
-                    mx[t][1] = fmaxf(s[t][1], s[t][3]);
-#pragma unroll
-                    for (int off = 4; off <= 16; off <<= 1) {
-                        mx[t][0] = fmaxf(mx[t][0], __shfl_xor_sync(0xffffffffu, mx[t][0], off));
-                        mx[t][1] = fmaxf(mx[t][1], __shfl_xor_sync(0xffffffffu, mx[t][1], off));
-                    }
-                    up[t][0] = mx[t][0] > m[t][0] + kRescaleThreshold;
-                    up[t][1] = mx[t][1] > m[t][1] + kRescaleThreshold;
-                    any_up = any_up || up[t][0] || up[t][1];
+                    dm[t][0] = fmaxf(s[t][0], s[t][2]);
+                    dm[t][1] = fmaxf(s[t][1], s[t][3]);
+                    any_up = any_up || dm[t][0] > kRescaleThreshold || dm[t][1] > kRescaleThreshold;
                 }
-                if (__any_sync(0xffffffffu, any_up)) {
+                // Raising m needs the column's maximum over the 8 lanes that hold its tokens; that
+                // reduction runs only on the warp's first block (m is set from it) and when some
+                // lane's keys exceed m by more than 2^8, which is rare.
+                if (fresh || __any_sync(0xffffffffu, any_up)) {
 #pragma unroll
                     for (int t = 0; t < kNT; ++t) {
-                        const float n0 = up[t][0] ? mx[t][0] : m[t][0], n1 = up[t][1] ? mx[t][1] : m[t][1];
-                        const float a0 = up[t][0] ? ex2(m[t][0] - n0) : 1.f;
-                        const float a1 = up[t][1] ? ex2(m[t][1] - n1) : 1.f;
-                        m[t][0] = n0;
-                        m[t][1] = n1;
-                        l[t][0] *= a0;
-                        l[t][1] *= a1;
-                        psum[t][0] *= a0;
-                        psum[t][1] *= a1;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            o[t][i][0] *= a0; o[t][i][2] *= a0;
-                            o[t][i][1] *= a1; o[t][i][3] *= a1;
+                        for (int off = 4; off <= 16; off <<= 1) {
+                            dm[t][0] = fmaxf(dm[t][0], __shfl_xor_sync(0xffffffffu, dm[t][0], off));
+                            dm[t][1] = fmaxf(dm[t][1], __shfl_xor_sync(0xffffffffu, dm[t][1], off));
+                        }
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const bool up = fresh ? dm[t][e] != kNegInf : dm[t][e] > kRescaleThreshold;
+                            const float delta = up ? dm[t][e] : 0.f;
+                            // on the first block l and O are still 0: nothing to rescale (and
+                            // 2^-delta may overflow for very negative scores)
+                            const float a = up && !fresh ? ex2(-delta) : 1.f;
+                            m[t][e] += delta;
+                            s[t][e] -= delta;
+                            s[t][e + 2] -= delta;
+                            l[t][e] *= a;
+                            psum[t][e] *= a;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                o[t][i][e] *= a;
+                                o[t][i][e + 2] *= a;
+                            }
                         }
                     }
+                    fresh = false;
                 }
                 // ---- O^T += V^T . P^T ----
                 uint32_t pb[kNT][2];
 #pragma unroll
                 for (int t = 0; t < kNT; ++t) {
-                    const float ms0 = m[t][0] == kNegInf ? 0.f : m[t][0];
-                    const float ms1 = m[t][1] == kNegInf ? 0.f : m[t][1];
-                    const float p0 = ex2(s[t][0] - ms0), p1 = ex2(s[t][1] - ms1);
-                    const float p2 = ex2(s[t][2] - ms0), p3 = ex2(s[t][3] - ms1);
+                    const float p0 = ex2(s[t][0]), p1 = ex2(s[t][1]);
+                    const float p2 = ex2(s[t][2]), p3 = ex2(s[t][3]);
                     l[t][0] += p0 + p2;
                     l[t][1] += p1 + p3;
                     if constexpr (kI8) {
@@ -566,6 +579,10 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                     o[t][i][1] -= kI8Bias * psum[t][1]; o[t][i][3] -= kI8Bias * psum[t][1];
                 }
             }
+            // a column with no valid key in this warp's blocks has l = 0 (any other has l >= 1:
+            // the key that set m contributed 2^0)
+            m[t][0] = l[t][0] > 0.f ? m[t][0] : kNegInf;
+            m[t][1] = l[t][1] > 0.f ? m[t][1] : kNegInf;
         }
     }
 

@@ -266,6 +266,53 @@ def test_identical_keys_give_mean_of_v():
             np.testing.assert_allclose(got[b, h], mean[h // w.group], atol=4e-3)
 
 
+def _ranged_workload(kv, case):
+    """Scores far from the unit range. "wide": scale x8 on N(0, 1) data, so the running max is
+    raised many times. "below_zero": every key points away from its sequence's query (scale x16),
+    so all scores lie ~170 base-2 units below zero and 2^s underflows unless the reference is the
+    running max. "late_spike": one key near the end of each context is aligned with the query, so
+    the max jumps by tens of units in a late, partial block."""
+    lens = [1, 40, 700, 2100]
+    w = W.make_decode(name="ranges", B=len(lens), Hq=16, Hkv=2, D=128, context_lens=lens,
+                      kv_dtype=kv, q_dtype="bf16", seed=55 if kv == "bf16" else 56)
+    G = w.group
+    q = W.bf16_bits_to_f32(w.q).copy()
+    kp = w.k_pool.copy()
+    kf = W.bf16_bits_to_f32(kp) if kv == "bf16" else kp.astype(np.float32)
+    scale = w.scale * (8.0 if case == "wide" else 16.0)
+    if case != "wide":
+        for b, n in enumerate(lens):
+            for h in range(w.Hkv):
+                q[b, h * G:(h + 1) * G] = q[b, h * G]      # one query per group
+                sgn = np.where(q[b, h * G] < 0, -1.0, 1.0)
+                rows = [t for t in range(n)] if case == "below_zero" else [max(0, n - 3)]
+                for t in rows:
+                    blk, off = w.block_tables[b, t // 16], t % 16
+                    mag = np.abs(kf[blk, h, off]) + (0.0 if kv == "i8" else 0.25)
+                    kf[blk, h, off] = (-sgn if case == "below_zero" else sgn) * mag
+        if case == "late_spike":
+            scale = w.scale * 2.0
+    if kv == "bf16":
+        kp = W.f32_to_bf16_bits(kf)
+    else:
+        kp = np.clip(kf, -127, 127).astype(np.int8)
+    return W.DecodeWorkload(**{**w.__dict__, "q": W.f32_to_bf16_bits(q), "k_pool": kp,
+                               "scale": scale})
+
+
+@pytest.mark.parametrize("kv", ["bf16", "i8"])
+@pytest.mark.parametrize("case", ["wide", "below_zero", "late_spike"])
+def test_extreme_score_ranges(kv, case):
+    w = _ranged_workload(kv, case)
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                        w.scale, w.k_scales, w.v_scales)
+    d = DevWorkload(w)
+    for chunk in (0, 64):
+        got = to_f64(d.attend(chunk=chunk))
+        assert np.all(np.isfinite(got))
+        assert_close(got, ref, kv, f"{kv} {case} chunk {chunk}")
+
+
 def test_bad_block_ids_are_skipped_and_flagged():
     w = W.make_config(2, B=4, ctx_lo=100, ctx_hi=400, seed=3)
     bt = w.block_tables.copy()
