@@ -61,13 +61,13 @@ def test_workspace_arithmetic(pkv):
     assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 1024) == 8 * 32 * 128 * 130 * 4
     assert L.pkv_decode_workspace_bytes(4, 4, 4, 64, 100, 0) == 0    # one split: no workspace
     assert L.pkv_decode_workspace_bytes(4, 4, 4, 64, 100, 17) == 0   # chunk not a block multiple
-    # auto chunk: ~2048 units (bf16 tensor-core kernel) or ~4096 (INT8, CUDA-core), powers of
+    # auto chunk: ~1024 units (bf16 tensor-core kernel) or ~4096 (INT8, CUDA-core), powers of
     # two in [256, 4096], more only to keep splits <= 8192
     BF, I8, F32 = P.BF16, P.I8, P.F32
-    assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, BF) == 512      # Llama-3-8B GQA batch
-    assert L.pkv_decode_split_chunk(8, 8, 128, 130882, 0, BF) == 2048    # 131k-context batch
+    assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, BF) == 1024     # Llama-3-8B GQA batch
+    assert L.pkv_decode_split_chunk(8, 8, 128, 130882, 0, BF) == 4096    # 131k-context batch
     assert L.pkv_decode_split_chunk(128, 8, 128, 8083, 0, I8) == 1024    # INT8 batch
-    assert L.pkv_decode_split_chunk(256, 8, 128, 4090, 0, BF) == 2048    # shared-prefix batch
+    assert L.pkv_decode_split_chunk(256, 8, 128, 4090, 0, BF) == 4096    # shared-prefix batch
     assert L.pkv_decode_split_chunk(64, 8, 64, 4055, 0, BF) == 256       # head_dim 64: CUDA cores
     assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, F32) == 256     # fp32: CUDA cores
     assert L.pkv_decode_split_chunk(4, 4, 64, 100, 0, F32) == 256
