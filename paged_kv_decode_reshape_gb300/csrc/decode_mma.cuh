@@ -75,8 +75,7 @@ struct MmaGeom {
     static constexpr int SPW = kI8 ? PKV_MMA_SPW_I8 : PKV_MMA_SPW_BF16;     // stages per warp
     static constexpr int THREADS = 32 * NC;
     static constexpr int TILE = kBlockSize * kMmaD * (kI8 ? 1 : 2);  // one K (or V) tile
-    static constexpr int BOX = kBlockSize * 128;                     // bytes of one TMA box
-    static constexpr int BOXES = TILE / BOX;                         // boxes per tile (2 or 1)
+    static constexpr int BOX = kBlockSize * 128;  // [16 rows][128 B]: a bf16 tile's 64-dim half, an INT8 tile
     static constexpr int STAGE = 2 * TILE;                           // K then V
     // Stage s is only ever used by warp s % NC, so each warp waits on a stage's phases strictly
     // in order and a parity wait can never match a phase two behind.
@@ -280,10 +279,12 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
         if (bid >= 0) {
             const int row = (bid * p.Hkv + kvh) * kBlockSize;
             mbar_arrive_expect_tx(bar, STAGE + (kI8 ? 2 * kBlockSize * 4 : 0));
-#pragma unroll
-            for (int x = 0; x < G::BOXES; ++x) {
-                tma_load_2d(dst + x * G::BOX, &tmk, x * 64 * (kI8 ? 2 : 1), row, bar);
-                tma_load_2d(dst + TILE + x * G::BOX, &tmv, x * 64 * (kI8 ? 2 : 1), row, bar);
+            if constexpr (kI8) {  // one [16 rows][128 B] box per tile
+                tma_load_2d(dst, &tmk, 0, row, bar);
+                tma_load_2d(dst + TILE, &tmv, 0, row, bar);
+            } else {  // one box per tile: both 64-dim halves, [half][16 rows][128 B]
+                tma_load_3d(dst, &tmk, 0, row, 0, bar);
+                tma_load_3d(dst + TILE, &tmv, 0, row, 0, bar);
             }
             if constexpr (kI8) {
                 const size_t srow = (size_t)bid * p.Hkv + kvh;

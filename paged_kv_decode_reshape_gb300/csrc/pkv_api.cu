@@ -198,12 +198,16 @@ pkv_status run_decode(const Decode& a) {
             !make_pool_tensor_map(&tv, a.v_pool, a.NB, a.Hkv, i8m))
             return PKV_ERR_CUDA;
         if (P > 0) {
+            CUtensorMap pk, pv;  // the prefix kernel's one-box-per-block view of the same pools
+            if (!make_pool_tensor_map_blocks(&pk, a.k_pool, a.NB, a.Hkv) ||
+                !make_pool_tensor_map_blocks(&pv, a.v_pool, a.NB, a.Hkv))
+                return PKV_ERR_CUDA;
             PrefixParams x{};
             x.q = a.q; x.block_tables = a.block_tables; x.ws_acc = p.ws_acc; x.ws_ml = p.ws_ml;
             x.status = a.status; x.B = a.B; x.Hq = a.Hq; x.Hkv = a.Hkv; x.G = g; x.NB = a.NB;
             x.MBPS = a.MBPS; x.S = Sw; x.slot0 = S; x.prefix_tokens = prefix;
             x.split_tokens = split_tokens; x.scale_log2 = p.scale_log2;
-            if (launch_prefix(x, tk, tv, P, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
+            if (launch_prefix(x, pk, pv, P, a.stream) != cudaSuccess) return PKV_ERR_CUDA;
         }
         e = launch_split_mma(p, i8m, tk, tv, a.stream);
     } else if (a.kv_dtype == PKV_F32) e = launch_split_f32(p, a.D, hg, a.stream);
@@ -393,8 +397,8 @@ pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_p
         overlap(out, io_b, query_start, (size_t)(num_seqs + 1) * 4))
         return PKV_ERR_INVALID_ARG;
     CUtensorMap tk, tv;
-    if (!make_pool_tensor_map(&tk, k_pool, num_blocks, num_kv_heads, false) ||
-        !make_pool_tensor_map(&tv, v_pool, num_blocks, num_kv_heads, false))
+    if (!make_pool_tensor_map_blocks(&tk, k_pool, num_blocks, num_kv_heads) ||
+        !make_pool_tensor_map_blocks(&tv, v_pool, num_blocks, num_kv_heads))
         return PKV_ERR_CUDA;
     PrefillParams p{};
     p.out = out; p.q = q; p.block_tables = block_tables; p.context_lens = context_lens;

@@ -167,6 +167,8 @@ cudaError_t launch_merge(const MergeParams& p, pkv_dtype out_dtype, int D, cudaS
 // Tensor-core split kernel for head_dim 128, bf16 or INT8 pools, 8 query heads per CTA; the K and
 // V pools are described by TMA tensor maps built with make_pool_tensor_map (false on failure).
 bool make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, bool i8);
+// The tcgen05 prefill / prefix kernels' view of a bf16 pool (one box per block tile).
+bool make_pool_tensor_map_blocks(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads);
 // the kernel with two n-tiles (16 columns per CTA); same arguments as launch_split_mma
 cudaError_t launch_split_mma_nt2(const SplitParams& p, bool i8, const CUtensorMap& tk,
                                  const CUtensorMap& tv, cudaStream_t s);

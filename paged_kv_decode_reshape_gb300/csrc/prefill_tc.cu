@@ -27,9 +27,11 @@
 //   warp 11    lane 0 issues the PV products. Two issuers, because a thread that has just issued a
 //              batch of products takes several hundred cycles to notice its next barrier, and
 //              the S and PV streams depend on each other only through the softmax.
-//   warps 9-10 producers: block ids from the table, 2-D TMA copies of the 8 pool blocks of a key
-//              tile (128-byte swizzle), K by warp 9 into one ring, V by warp 10 into another. A
-//              K slot is free once S of its tile is done, so K runs well ahead of V.
+//   warps 9-10 producers: block ids from the table, one 4-D TMA copy (4 KB, 128-byte swizzle) per
+//              pool block of a key tile, K by warp 9 into one ring, V by warp 10 into another. A
+//              K slot is free once S of its tile is done, so K runs well ahead of V. (Measured on
+//              GB300: an SM takes in ~53 GB/s of 2 KB TMA boxes but ~82 GB/s of 4 KB ones, so
+//              one box per block rather than one per 64-dim half.)
 // Per key tile t the MMA thread issues S(t+1) = Q . K(t+1)^T as soon as the softmax has read S(t)
 // (s_free), and O += P(t) . V(t) once P(t) is written into P buffer t % 2 (p_full). The softmax
 // writes P(t) once the product that last read that buffer, PV(t-2), is done (pv_done). So S(t+1)
@@ -48,8 +50,11 @@ namespace {
 
 constexpr int kPfQ = 128;                      // query rows per CTA (MMA M)
 constexpr int kPfK = 128;                      // keys per tile (MMA N of S, K of PV)
-constexpr int kPfHalf = kPfK * 128;            // one 64-dim half of a K or V tile: [128 keys x 128 B]
-constexpr int kPfStage = 2 * kPfHalf;          // one K (or V) tile: dims 0-63, then dims 64-127
+// A K (or V) tile is the 8 pool blocks of 128 keys, one 4 KB TMA box each, block jj at 4 KB jj as
+// [row group (keys 0-7, 8-15)][64-dim half][8 keys][128 B]: in every half, key k's 128-byte row is
+// at (k / 8) * 2 KB + (k % 8) * 128 (+ 1 KB for dims 64-127), a uniform stride for both products.
+constexpr int kPfBlockBytes = kBlockSize * 256;  // one block's keys, both halves
+constexpr int kPfStage = 8 * kPfBlockBytes;     // one K (or V) tile
 #ifndef PKV_PF_STAGES
 #define PKV_PF_STAGES 3                        // slots per ring (K and V each)
 #endif
@@ -116,6 +121,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive 32-bit columns of this thread's lane, one load and one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,"
+        "%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,"
+        "%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -343,15 +371,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             const unsigned valid = __ballot_sync(0xffffffffu, id >= 0);
             if (lane == 0) {
                 if (valid == 0) mbar_arrive(full(g, st));
-                else mbar_arrive_expect_tx(full(g, st), __popc(valid) * 2 * (kBlockSize * 128));
+                else mbar_arrive_expect_tx(full(g, st), __popc(valid) * kPfBlockBytes);
             }
             __syncwarp();
             if (id >= 0) {
-                const uint32_t bar = full(g, st), dst = slot(g, t);
-                const int row = (id * p.Hkv + kvh) * kBlockSize;
-                const uint32_t o = lane * (kBlockSize * 128);
-                tma_load_2d(dst + o, map, 0, row, bar);
-                tma_load_2d(dst + kPfHalf + o, map, 64, row, bar);
+                const int grp = (id * p.Hkv + kvh) * (kBlockSize / 8);  // the block's first 8-row group
+                tma_load_4d(slot(g, t) + lane * kPfBlockBytes, map, 0, 0, 0, grp, full(g, st));
             }
             issued = t + 1;
         }
@@ -370,7 +395,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 const uint32_t kbase = slot(0, t);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t bd = sdesc(kbase + (ks >> 2) * kPfHalf + (ks & 3) * 32, 16, 1024);
+                    // K-major: 8-key groups 2 KB apart, dims 16 ks.. in half ks / 4 at 32 B (ks % 4)
+                    const uint64_t bd = sdesc(kbase + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048);
                     umma_ts(tmem + kSCol, tmem + kQCol + 8 * ks, bd, kIdescS, ks > 0);
                 }
                 umma_commit(s_full);
@@ -380,7 +406,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 const uint32_t vbase = slot(1, t);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = sdesc(vbase + kk * (16 * 128), kPfHalf, 1024);
+                    // MN-major: keys 16 kk.. are block kk; 8-key groups 2 KB apart, dims 64.. 1 KB on
+                    const uint64_t bd = sdesc(vbase + kk * kPfBlockBytes, 1024, 2048);
                     umma_ts(tmem + kOCol, tmem + kPCol + 64 * (t & 1) + 8 * kk, bd, kIdescO,
                             (t > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -448,8 +475,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 atomicExch(&abort_flag, 1);
                 flag(p.status, PKV_FLAG_TIMEOUT);
             }
-            // both threads of a row take the same exit
-            if (barrier_or(pair_bar, 64, !got || aborted(&abort_flag))) { ok = false; break; }
             tc_fence_after();
             if ((t + 1) * kPfK > n_tile_max || mask8 != 0xFF) {
                 // V rows of keys no row may see (past the context or in a missing block) must be
@@ -462,20 +487,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                     flag(p.status, PKV_FLAG_TIMEOUT);
                 } else if (t * kPfK + k >= n_tile_max || !((mask8 >> (k >> 4)) & 1)) {
                     uint4* z = reinterpret_cast<uint4*>(smem + kPfOffV + (t % kPfStages) * kPfStage +
-                                                        half * kPfHalf + k * 128);
+                                                        (k >> 4) * kPfBlockBytes + ((k >> 3) & 1) * 2048 +
+                                                        half * 1024 + (k & 7) * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
             }
             float s[64];
-            {
-                float t0[32], t1[32];
-                tmem_ld32(s_col, t0);
-                tmem_ld32(s_col + 32, t1);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) { s[c] = t0[c]; s[32 + c] = t1[c]; }
-            }
+            tmem_ld64(s_col, s);  // (reading TMEM is harmless even when S(t) never came)
             tc_fence_before();
             mbar_arrive(s_free);  // S(t + 1) may now be written
             // raw scores here; the scale (with log2 e) is applied inside each exponent below
@@ -496,11 +516,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             for (int w2 = 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
                 for (int e = 0; e < w2; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w2]);
-            // the row's maximum over both halves (the same value in both threads), in log2 units
-            xmax[(u * 2 + hf) * kPfQ + r] = mx8[0];
-            named_barrier_sync(pair_bar, 64);
-            const float mx = fmaxf(mx8[0], xmax[(u * 2 + (hf ^ 1)) * kPfQ + r]) * csc;
-            const bool up = mx > m + kPfRescale;
+            // One vote of the pair of warps per tile. The reference m changes only when a row's
+            // maximum exceeds it by more than 2^8, so if no thread's own half does (and no thread
+            // gives up) every row keeps m and the halves need not swap maxima. Otherwise swap them
+            // (the row's maximum over both halves, the same in both threads, log2 units) and
+            // decide together whether to stop; both warps take the same branch at every barrier.
+            const float mloc = mx8[0] * csc;
+            const bool stop = !got || aborted(&abort_flag);
+            bool up = false;
+            float mx = m;
+            if (barrier_or(pair_bar, 64, stop || mloc > m + kPfRescale)) {
+                xmax[(u * 2 + hf) * kPfQ + r] = mx8[0];
+                named_barrier_sync(pair_bar, 64);
+                mx = fmaxf(mx8[0], xmax[(u * 2 + (hf ^ 1)) * kPfQ + r]) * csc;
+                up = mx > m + kPfRescale;
+                if (barrier_or(pair_bar, 64, stop)) { ok = false; break; }
+            }
             float alpha = 1.f;
             if (up) {
                 alpha = ex2(m - mx);  // m == -inf: 0
@@ -600,13 +631,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                            int max_query_len, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e != cudaSuccess) return e;
     PfWork w{};
     w.q = p.q; w.block_tables = p.block_tables; w.status = p.status;
     w.Hq = p.Hq; w.Hkv = p.Hkv; w.G = p.G; w.NB = p.NB; w.MBPS = p.MBPS; w.scale_log2 = p.scale_log2;
     w.out = p.out; w.context_lens = p.context_lens; w.query_start = p.query_start; w.B = p.B;
     const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hq, p.B);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return e;
     return launch_pdl(prefill_kernel<false>, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
 }
 

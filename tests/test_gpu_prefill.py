@@ -27,7 +27,9 @@ def run_prefill(w, status=None, bt=None):
     return to_f64(out)
 
 
-@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2), (6, 2), (4, 2)])
+# G = 4, 1, 8, 3, 2, 16: every cluster size the launcher picks (query heads of one GQA group share
+# each K/V tile through multicast) and the unclustered path
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2), (6, 2), (4, 2), (32, 2)])
 def test_prefill_matches_oracle(hq, hkv):
     w = W.make_prefill(name="pf", query_lens=[1, 5, 127, 128, 129, 300],
                        cached_lens=[0, 17, 64, 200, 5, 1000], Hq=hq, Hkv=hkv, D=128, seed=hq + hkv)
@@ -60,8 +62,10 @@ def test_prefill_long_prompt():
     assert sub_q.shape[0] == rows.size
 
 
-def test_prefill_missing_block_is_skipped_and_flagged():
-    w = W.make_prefill(name="pfb", query_lens=[40, 70], cached_lens=[100, 30], Hq=8, Hkv=8, D=128, seed=9)
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4), (32, 4)])
+def test_prefill_missing_block_is_skipped_and_flagged(hq, hkv):
+    w = W.make_prefill(name="pfb", query_lens=[40, 70], cached_lens=[100, 30], Hq=hq, Hkv=hkv, D=128,
+                       seed=9)
     bt = w.block_tables.copy()
     bt[0, 2] = w.NB + 5  # a block of sequence 0 outside the pool
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
