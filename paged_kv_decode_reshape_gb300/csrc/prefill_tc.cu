@@ -104,6 +104,26 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
                  : "memory");
 }
 
+// Packed fp32 pairs for the FMA pipe's two-wide instructions (sm_100 and later).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -539,15 +559,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 l *= alpha;
             }
             const float ms = m == -INFINITY ? 0.f : m;
+            // two keys per instruction on the FMA pipe (packed fp32 pairs): the exponents' arguments
+            // and the running sums
             uint32_t pw[32];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t cs2 = f32x2(csc, csc), nms2 = f32x2(-ms, -ms);
+            uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float a0 = ex2(fmaf(s[2 * c], csc, -ms)), a1 = ex2(fmaf(s[2 * c + 1], csc, -ms));
-                ls[c & 3] += a0 + a1;
+                float y0, y1;
+                f32x2_split(fma_f32x2(f32x2(s[2 * c], s[2 * c + 1]), cs2, nms2), y0, y1);
+                const float a0 = ex2(y0), a1 = ex2(y1);
+                ls2[c & 1] = add_f32x2(ls2[c & 1], f32x2(a0, a1));
                 pw[c] = pack2_bf16(a0, a1);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            {
+                float e0, e1, o0, o1;
+                f32x2_split(ls2[0], e0, e1);
+                f32x2_split(ls2[1], o0, o1);
+                l += (e0 + o0) + (e1 + o1);
+            }
             // P buffer u is free once PV(t - 2) is done; O may be rescaled once PV(t - 1) is done
             const bool resc = t > 0 && __any_sync(0xffffffffu, up);
             const int wt = resc ? t - 1 : t - 2;  // the tile whose product must be complete
