@@ -104,6 +104,13 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
                  : "memory");
 }
 
+// max of three (sm_100 and later): the larger operand, ignoring a NaN like fmaxf
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Packed fp32 pairs for the FMA pipe's two-wide instructions (sm_100 and later).
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
     uint64_t r;
@@ -527,15 +534,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                     s[c] = vis ? (neg ? -s[c] : s[c]) : -INFINITY;
                 }
             }
-            float mx8[8];  // tree maximum: 8 independent chains, then 3 levels
+            float mx8[8];  // tree maximum with three-input max: 8 independent chains, then 2 levels
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = s[e];
-#pragma unroll
-            for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-#pragma unroll
-            for (int w2 = 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                for (int e = 0; e < w2; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w2]);
+            for (int e = 0; e < 8; ++e) {
+                float a = fmax3(s[e], s[e + 8], s[e + 16]);
+                a = fmax3(a, s[e + 24], s[e + 32]);
+                a = fmax3(a, s[e + 40], s[e + 48]);
+                mx8[e] = fmaxf(a, s[e + 56]);
+            }
+            mx8[0] = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             // One vote of the pair of warps per tile. The reference m changes only when a row's
             // maximum exceeds it by more than 2^8, so if no thread's own half does (and no thread
             // gives up) every row keeps m and the halves need not swap maxima. Otherwise swap them
