@@ -19,10 +19,11 @@
 //   Q   128-191   the CTA's 128 query rows, two bf16 dims per column (written once)
 //   P   192-255 (buffer 0), 256-319 (buffer 1): bf16 weights of a key tile, two keys per column
 //   S   320-447   S = Q . K^T of one key tile, fp32
-// Warp roles (320 threads):
+// Warp roles (384 threads with the default two softmax threads per row):
 //   warps 0-7  softmax. Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows); warps 0-3 take
-//              keys 0-63 of every tile, warps 4-7 keys 64-127. The two threads of a row swap
-//              their maxima through shared memory each tile and their sums at the end.
+//              keys 0-63 of every tile, warps 4-7 keys 64-127. Per tile the two warps of a lane
+//              quadrant vote whether any row may raise its reference maximum; only then do the two
+//              threads of a row swap their maxima through shared memory. They swap sums at the end.
 //   warp 8     lane 0 issues the S products (and their commits); the warp owns the TMEM allocation
 //   warp 11    lane 0 issues the PV products. Two issuers, because a thread that has just issued a
 //              batch of products takes several hundred cycles to notice its next barrier, and
@@ -61,14 +62,29 @@ constexpr int kPfStage = 8 * kPfBlockBytes;     // one K (or V) tile
 constexpr int kPfStages = PKV_PF_STAGES;
 constexpr int kPfOffK = 0;
 constexpr int kPfOffV = kPfStages * kPfStage;
-constexpr int kPfOffX = 2 * kPfStages * kPfStage;  // row maxima [2][2][128] and sums [2][128], fp32
-constexpr int kPfOffBar = kPfOffX + 6 * kPfQ * 4;
+// Softmax threads per query row (a build-time tunable): each takes 128 / kPfSplit keys of every
+// tile and 128 / kPfSplit dims of the row's output. The kPfSplit warps sharing a TMEM lane quadrant
+// (w, w + 4, ...) form one barrier group. Measured on GB300 (the 4 x 4096-token prefill): 2 threads
+// per row 1138 TFLOP/s, 4 threads per row (640-thread CTAs) 1112.
+#ifndef PKV_PF_SPLIT
+#define PKV_PF_SPLIT 2
+#endif
+constexpr int kPfSplit = PKV_PF_SPLIT;
+static_assert(kPfSplit == 2 || kPfSplit == 4, "threads per row");
+constexpr int kPfKeysPer = kPfK / kPfSplit;         // keys of a tile per thread
+constexpr int kPfDimsPer = 128 / kPfSplit;          // output dims per thread
+constexpr int kPfSoftWarps = 4 * kPfSplit;
+constexpr int kPfSoftThreads = 32 * kPfSoftWarps;
+constexpr int kPfGroup = 32 * kPfSplit;             // threads of one barrier group
+constexpr int kPfOffX = 2 * kPfStages * kPfStage;   // row maxima [2][kPfSplit][128], sums [kPfSplit][128]
+constexpr int kPfOffBar = kPfOffX + 3 * kPfSplit * kPfQ * 4;
 // barriers: full[2 rings][S], empty[2 rings][S], s_full, s_free, p_full[2], pv_done[2], o_done,
 // drain[2]; then the TMEM slot
 constexpr int kPfNumBars = 4 * kPfStages + 9;
 constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
-constexpr int kPfThreads = 384;
-constexpr int kPfMmaWarp = 8, kPfLoadWarpK = 9, kPfLoadWarpV = 10, kPfMmaWarpPV = 11;
+constexpr int kPfThreads = kPfSoftThreads + 128;
+constexpr int kPfMmaWarp = kPfSoftWarps, kPfLoadWarpK = kPfSoftWarps + 1, kPfLoadWarpV = kPfSoftWarps + 2,
+              kPfMmaWarpPV = kPfSoftWarps + 3;
 constexpr uint32_t kPfTmemCols = 512;
 constexpr uint32_t kOCol = 0, kQCol = 128, kPCol = 192, kSCol = 320;
 constexpr float kPfRescale = 8.0f;             // log2 units
@@ -151,7 +167,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // 64 consecutive 32-bit columns of this thread's lane, one load and one wait.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+[[maybe_unused]] __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     uint32_t r[64];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -192,7 +208,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+[[maybe_unused]] __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
         "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -202,6 +218,29 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[3
         "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+[[maybe_unused]] __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// N consecutive 32-bit columns of this thread's lane (N = 16 or 32), stored and waited for.
+template <int N>
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&v)[N]) {
+    if constexpr (N == 32) tmem_st32u(taddr, v);
+    else tmem_st16u(taddr, v);
+}
+
+// N consecutive 32-bit columns of this thread's lane (N = 32 or 64), loaded and waited for.
+template <int N>
+__device__ __forceinline__ void tmem_ld_words(uint32_t taddr, float (&v)[N]) {
+    if constexpr (N == 64) tmem_ld64(taddr, v);
+    else tmem_ld32(taddr, v);
 }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
@@ -303,8 +342,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sbase = smem_addr(smem);
-    float* xmax = reinterpret_cast<float*>(smem + kPfOffX);  // [2 buffers][2 halves][128 rows]
-    float* xsum = xmax + 4 * kPfQ;                           // [2 halves][128 rows]
+    float* xmax = reinterpret_cast<float*>(smem + kPfOffX);  // [2 buffers][kPfSplit parts][128 rows]
+    float* xsum = xmax + 2 * kPfSplit * kPfQ;                // [kPfSplit parts][128 rows]
     const uint32_t bar0 = sbase + kPfOffBar;
     // ring g (0: K, 1: V): slot s of tile t is t % S
     auto full = [&](int g, int s) { return bar0 + 8 * (g * kPfStages + s); };
@@ -326,9 +365,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 mbar_init(empty(g, s), 1);
             }
         mbar_init(s_full, 1);
-        mbar_init(s_free, 2 * kPfQ);
+        mbar_init(s_free, kPfSoftThreads);
         for (int u = 0; u < 2; ++u) {
-            mbar_init(p_full(u), 2 * kPfQ);
+            mbar_init(p_full(u), kPfSoftThreads);
             mbar_init(pv_done(u), 1);
         }
         mbar_init(o_done, 1);
@@ -348,8 +387,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // softmax thread (hf, r): row r, keys 64 hf .. 64 hf + 63 of each tile
-    const int hf = (warp >> 2) & 1;
+    // softmax thread (hf, r): row r, keys kPfKeysPer hf .. of each tile, output dims kPfDimsPer hf ..
+    const int hf = (warp >> 2) & (kPfSplit - 1);
     const int r = tid & 127;
     const int i = qt * kPfQ + r;
     const bool row_valid = i < L;
@@ -358,17 +397,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
     const size_t qrow = !kPrefix ? (size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h
                                  : (row_valid ? (size_t)(i / p.G) * p.Hq + kvh * p.G + i % p.G : 0);
     const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
-    if (warp < 8) {
-        // Q row r, dims 64 hf .. 64 hf + 63, into TMEM columns 128 + 32 hf .. (zeros past the rows)
+    if (warp < kPfSoftWarps) {
+        // Q row r, dims kPfDimsPer hf .., into TMEM columns 128 + kPfDimsPer / 2 hf .. (two bf16
+        // per column; zeros past the rows)
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          qrow * 128 + 64 * hf);
-        uint32_t qw[32];
+                                                          qrow * 128 + kPfDimsPer * hf);
+        uint32_t qw[kPfDimsPer / 2];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kPfDimsPer / 8; ++c) {
             const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
             qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
         }
-        tmem_st32u(tmem + tl + kQCol + 32 * hf, qw);
+        tmem_st_words(tmem + tl + kQCol + kPfDimsPer / 2 * hf, qw);
     }
     tc_fence_before();
     __syncthreads();
@@ -474,11 +514,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
         __syncwarp();
     } else {
         // ---------------- softmax: row r, key half hf ----------------
-        const uint32_t s_col = tmem + tl + kSCol + 64 * hf, o_col = tmem + tl + kOCol + 64 * hf;
-        const uint32_t p_col = tmem + tl + kPCol + 32 * hf;  // + 64 (t % 2)
+        const uint32_t s_col = tmem + tl + kSCol + kPfKeysPer * hf, o_col = tmem + tl + kOCol + kPfDimsPer * hf;
+        const uint32_t p_col = tmem + tl + kPCol + kPfKeysPer / 2 * hf;  // + 64 (t % 2)
         // keys (relative to the CTA's first key) this row sees
         const int n_row = !row_valid ? 0 : (kPrefix ? n_tile_max : first_visible + i);
-        const int pair_bar = 1 + (warp & 3);  // named barrier of warps w and w + 4 (64 threads)
+        const int pair_bar = 1 + (warp & 3);  // named barrier of warps w, w + 4, ... (kPfGroup threads)
         // scores are scaled inside the exponents by |scale| * log2 e; a negative scale flips their
         // sign. |scale| is at least FLT_MIN so a masked score (-inf) never meets a zero factor: a
         // zero scale still gives weights of exactly 1 (every visible score times FLT_MIN is ~0).
@@ -495,7 +535,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 ids_next = has_window((t >> 2) + 1) ? load_window((t >> 2) + 1, false) : -1;
             }
             const int mask8 = (present >> (8 * (t & 3))) & 0xFF;
-            const int mask = (mask8 >> (4 * hf)) & 0xF;  // this half's four blocks
+            constexpr int kMyBlocks = kPfKeysPer / kBlockSize;           // blocks of this thread's keys
+            constexpr int kAllMine = (1 << kMyBlocks) - 1;
+            const int mask = (mask8 >> (kMyBlocks * hf)) & kAllMine;
             const int u = t & 1;
             const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(s_full, t & 1));
             if (!got) {
@@ -508,28 +550,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 // finite: their weights are 0, and 0 * NaN would poison O. Zero them once the V
                 // copy of tile t has landed (PV(t) waits for this thread's P, so it reads them
                 // zeroed; the next copy into the slot waits for PV(t)).
-                const int k = tid >> 1, half = tid & 1;  // 256 threads: key k, 64-dim half
+                // kPfSoftThreads threads: key k, 64-dim half, and a 128 / kPfSplit * 2-byte piece of it
+                constexpr int kPieces = kPfSoftThreads / kPfK;     // per key: 2 halves x pieces
+                constexpr int kPieceB = 2 * 128 / kPieces;          // bytes of a piece
+                const int k = tid / kPieces, half = (tid % kPieces) / (kPieces / 2);
+                const int piece = tid % (kPieces / 2);
                 if (!mbar_wait_bounded(full(1, t % kPfStages), (t / kPfStages) & 1)) {
                     atomicExch(&abort_flag, 1);
                     flag(p.status, PKV_FLAG_TIMEOUT);
                 } else if (t * kPfK + k >= n_tile_max || !((mask8 >> (k >> 4)) & 1)) {
                     uint4* z = reinterpret_cast<uint4*>(smem + kPfOffV + (t % kPfStages) * kPfStage +
                                                         (k >> 4) * kPfBlockBytes + ((k >> 3) & 1) * 2048 +
-                                                        half * 1024 + (k & 7) * 128);
+                                                        half * 1024 + (k & 7) * 128 + piece * kPieceB);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int c = 0; c < kPieceB / 16; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
             }
-            float s[64];
-            tmem_ld64(s_col, s);  // (reading TMEM is harmless even when S(t) never came)
+            float s[kPfKeysPer];
+            tmem_ld_words(s_col, s);  // (reading TMEM is harmless even when S(t) never came)
             tc_fence_before();
             mbar_arrive(s_free);  // S(t + 1) may now be written
             // raw scores here; the scale (with log2 e) is applied inside each exponent below
-            const int kbase = t * kPfK + 64 * hf;
-            if (neg || !(kbase + 64 <= n_row && mask == 0xF)) {  // not the whole half visible to this row
+            const int kbase = t * kPfK + kPfKeysPer * hf;
+            if (neg || !(kbase + kPfKeysPer <= n_row && mask == kAllMine)) {  // not all of them visible
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < kPfKeysPer; ++c) {
                     const bool vis = kbase + c < n_row && ((mask >> (c >> 4)) & 1);
                     s[c] = vis ? (neg ? -s[c] : s[c]) : -INFINITY;
                 }
@@ -537,10 +583,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             float mx8[8];  // tree maximum with three-input max: 8 independent chains, then 2 levels
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                float a = fmax3(s[e], s[e + 8], s[e + 16]);
-                a = fmax3(a, s[e + 24], s[e + 32]);
-                a = fmax3(a, s[e + 40], s[e + 48]);
-                mx8[e] = fmaxf(a, s[e + 56]);
+                if constexpr (kPfKeysPer == 64) {
+                    float a = fmax3(s[e], s[e + 8], s[e + 16]);
+                    a = fmax3(a, s[e + 24], s[e + 32]);
+                    a = fmax3(a, s[e + 40], s[e + 48]);
+                    mx8[e] = fmaxf(a, s[e + 56]);
+                } else {
+                    mx8[e] = fmaxf(fmax3(s[e], s[e + 8], s[e + 16]), s[e + 24]);
+                }
             }
             mx8[0] = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             // One vote of the pair of warps per tile. The reference m changes only when a row's
@@ -552,12 +602,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             const bool stop = !got || aborted(&abort_flag);
             bool up = false;
             float mx = m;
-            if (barrier_or(pair_bar, 64, stop || mloc > m + kPfRescale)) {
-                xmax[(u * 2 + hf) * kPfQ + r] = mx8[0];
-                named_barrier_sync(pair_bar, 64);
-                mx = fmaxf(mx8[0], xmax[(u * 2 + (hf ^ 1)) * kPfQ + r]) * csc;
+            if (barrier_or(pair_bar, kPfGroup, stop || mloc > m + kPfRescale)) {
+                xmax[(u * kPfSplit + hf) * kPfQ + r] = mx8[0];
+                named_barrier_sync(pair_bar, kPfGroup);
+                float rm = xmax[u * kPfSplit * kPfQ + r];
+#pragma unroll
+                for (int q2 = 1; q2 < kPfSplit; ++q2) rm = fmaxf(rm, xmax[(u * kPfSplit + q2) * kPfQ + r]);
+                mx = rm * csc;
                 up = mx > m + kPfRescale;
-                if (barrier_or(pair_bar, 64, stop)) { ok = false; break; }
+                if (barrier_or(pair_bar, kPfGroup, stop)) { ok = false; break; }
             }
             float alpha = 1.f;
             if (up) {
@@ -568,11 +621,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             const float ms = m == -INFINITY ? 0.f : m;
             // two keys per instruction on the FMA pipe (packed fp32 pairs): the exponents' arguments
             // and the running sums
-            uint32_t pw[32];
+            uint32_t pw[kPfKeysPer / 2];
             const uint64_t cs2 = f32x2(csc, csc), nms2 = f32x2(-ms, -ms);
             uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < kPfKeysPer / 2; ++c) {
                 float y0, y1;
                 f32x2_split(fma_f32x2(f32x2(s[2 * c], s[2 * c + 1]), cs2, nms2), y0, y1);
                 const float a0 = ex2(y0), a1 = ex2(y1);
@@ -595,9 +648,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 }
                 tc_fence_after();
             }
-            if (resc) {  // rescale this thread's half of its O row (rare)
+            if (resc) {  // rescale this thread's dims of its O row (rare)
 #pragma unroll 1
-                for (int c0 = 0; c0 < 64; c0 += 32) {
+                for (int c0 = 0; c0 < kPfDimsPer; c0 += 32) {
                     float o[32];
                     tmem_ld32(o_col + c0, o);
 #pragma unroll
@@ -605,7 +658,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                     tmem_st32(o_col + c0, o);
                 }
             }
-            tmem_st32u(p_col + 64 * u, pw);
+            tmem_st_words(p_col + 64 * u, pw);
             tc_fence_before();
             mbar_arrive(p_full(u));
         }
@@ -614,16 +667,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             flag(p.status, PKV_FLAG_TIMEOUT);
         }
         tc_fence_after();
-        // the row's sum over both halves; both threads of the row decide together
+        // the row's sum over its parts; all threads of the group decide together
         xsum[hf * kPfQ + r] = l;
-        const bool fail = barrier_or(pair_bar, 64, !ok || aborted(&abort_flag));
-        const float lt = l + xsum[(hf ^ 1) * kPfQ + r];
+        const bool fail = barrier_or(pair_bar, kPfGroup, !ok || aborted(&abort_flag));
+        float lt = xsum[r];
+#pragma unroll
+        for (int q2 = 1; q2 < kPfSplit; ++q2) lt += xsum[q2 * kPfQ + r];
         if (!fail && kPrefix) {
             // ---- epilogue: the partial state (m in log2 units, l, acc = O unnormalised) ----
             const size_t u = qrow * p.S + p.slot0 + split;
-            float* acc = p.ws_acc + u * 128 + 64 * hf;
+            float* acc = p.ws_acc + u * 128 + kPfDimsPer * hf;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
+            for (int c0 = 0; c0 < kPfDimsPer; c0 += 32) {
                 float o[32];
                 tmem_ld32(o_col + c0, o);
                 if (row_valid) {
@@ -637,11 +692,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
                 p.ws_ml[2 * u + 1] = lt;
             }
         } else if (!fail) {
-            // ---- epilogue: dims 64 hf .. 64 hf + 63 of row r of O / l -> out ----
+            // ---- epilogue: dims kPfDimsPer hf .. of row r of O / l -> out ----
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + qrow * 128 + 64 * hf);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + qrow * 128 + kPfDimsPer * hf);
 #pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
+            for (int c0 = 0; c0 < kPfDimsPer; c0 += 32) {
                 float o[32];
                 tmem_ld32(o_col + c0, o);
                 if (row_valid) {
