@@ -82,11 +82,37 @@ def measured_peaks():
 SPLIT_KERNEL_SOURCES = ("decode_mma.cuh", "decode_mma.cu", "pkv_device.cuh", "pkv_internal.h")
 
 
+def source_code_only(text: str) -> str:
+    """C/C++ source with its comments removed (string and character literals kept) and every run of
+    whitespace collapsed to one space: what the compiler sees, so an edit of comments or layout does
+    not mark the ncu figures of unchanged code as stale."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in SPLIT_KERNEL_SOURCES:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + source_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

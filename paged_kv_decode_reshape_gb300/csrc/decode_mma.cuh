@@ -16,8 +16,8 @@
 //
 // Warp roles: every warp is its own producer and consumer. Warp w takes blocks w, w+NC, ... of
 // the split (NC warps per CTA) and owns the stages w, w+NC, ... of a STAGES-deep shared-memory
-// ring (STAGES = NC * stages per warp). Its lane 0 issues, per block, 2-D TMA tensor copies of
-// the K and V tiles with 128-byte swizzle (bank-conflict-free ldmatrix), plus 1-D bulk copies of
+// ring (STAGES = NC * stages per warp). Its lane 0 issues, per block, one TMA tensor copy of each
+// of the K and V tiles with 128-byte swizzle (bank-conflict-free ldmatrix), plus 1-D bulk copies of
 // the INT8 scale rows, completing on the stage's mbarrier; as soon as the warp has consumed a
 // block it refills that stage with its block STAGES further on. No warp waits for another until
 // the end, where the NC online-softmax states are merged in shared memory. Block ids come from

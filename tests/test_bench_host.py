@@ -89,6 +89,15 @@ def test_profiled_traffic_is_null_when_sources_changed(tmp_path, monkeypatch):
     assert bench.profiled_traffic("x") == 1234
 
 
+def test_source_fingerprint_ignores_comments_and_layout_only():
+    code = 'int f(int x) {\n    return x + 1;  // one more\n}\nconst char* s = "a // b";\n'
+    relaid = '/* header */\nint f(int x) { return x + 1; }\n\nconst char* s = "a // b";'
+    assert bench.source_code_only(code) == bench.source_code_only(relaid)
+    # code, and text inside literals, still count
+    assert bench.source_code_only(code) != bench.source_code_only(code.replace("x + 1", "x + 2"))
+    assert bench.source_code_only(code) != bench.source_code_only(code.replace('"a // b"', '"a // c"'))
+
+
 def test_launch_count_model():
     w = W.make_config(2, B=2, ctx_lo=100, ctx_hi=200)
     assert bench.cuda_launches_per_step(w, 512) == 2      # one split: no merge launch
