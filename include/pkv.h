@@ -1,7 +1,7 @@
 /*
  * pkv.h -- C ABI of libpkv.so: paged KV-cache decode on one NVIDIA GB300 (sm_103a).
  *
- * Three operations, each the GPU form of a step the pages describe:
+ * The hot path, each operation the GPU form of a step the pages describe:
  *   pkv_kv_cache_write                 -- store the new tokens' K and V into their slots of the
  *                                         paged pool ("AMD ATOM inference engine", introduction:
  *                                         the request-lifecycle step of writing into the KV
@@ -14,6 +14,16 @@
  *                                         PagedAttention V2 and FlashDecoding).
  *   pkv_paged_decode_attention_int8    -- the same over an INT8 K/V cache with per-token scales,
  *                                         dequantised inside the kernel (same notes, section 3).
+ * Around it:
+ *   pkv_kv_cache_write_int8            -- the INT8 cache's write: quantise each row, keep its scale.
+ *   pkv_paged_decode_attention_multi   -- L query tokens per sequence, causal among themselves.
+ *   pkv_paged_decode_attention_shared_prefix -- decode of a batch sharing a prefix: the prefix once
+ *                                         per kv head on the tcgen05 tensor cores, then the suffixes.
+ *   pkv_paged_prefill_attention        -- chunked, variable-length prefill (mixed batches) on tcgen05.
+ *   pkv_paged_decode_attention_static_ws -- decode with a library-held workspace (no allocation).
+ *   pkv_bm_*                           -- host block manager: allocation, refcounted prefix sharing.
+ *   pkv_decode_split_chunk, pkv_decode_workspace_bytes, pkv_decode_shared_prefix_workspace_bytes
+ *                                      -- the split rule and workspace sizes the calls use.
  *
  * Layouts (all row-major, element strides implied by the shapes):
  *   q, out       [num_seqs][num_q_heads][head_dim]
