@@ -84,11 +84,13 @@ def test_context_shorter_than_new_tokens_is_flagged():
 
 
 @pytest.mark.parametrize("kv", ["bf16", "i8"])
-@pytest.mark.parametrize("g,L", [(1, 3), (2, 4), (3, 3), (4, 2), (4, 5), (6, 2), (1, 8)])
+@pytest.mark.parametrize("g,L", [(1, 3), (2, 4), (3, 3), (4, 2), (4, 5), (6, 2), (1, 8), (8, 2), (8, 4),
+                                 (16, 2)])
 def test_multi_token_packed_columns(kv, g, L):
-    """When L * G query rows of a sequence's kv head fit the kernel's 8 columns better than one
-    token at a time, the tensor-core kernel packs (token, head) pairs as columns, each masked at
-    its own causal limit; L * G not a multiple of 8 leaves a partial last column group."""
+    """When L * G query rows of a sequence's kv head fit the kernel's columns (8 or 16 per CTA)
+    better than one token at a time, the tensor-core kernel packs (token, head) pairs as columns,
+    each masked at its own causal limit; L * G not a multiple of the column count leaves a partial
+    last column group. G = 8 with L = 2 or 4 takes the 16-column kernel, as G = 16 does."""
     Hkv = 2
     base = W.make_decode(name="mtp_pack", B=5, Hq=Hkv * g, Hkv=Hkv, D=128,
                          context_lens=[L, L + 1, 17, 300, 900], kv_dtype=kv, q_dtype="bf16",

@@ -41,6 +41,19 @@ def test_prefill_matches_oracle(hq, hkv):
     assert int(st.item()) == 0
 
 
+def test_prefill_batch_with_empty_sequences():
+    """Sequences with no new tokens (one of them with no context at all) own no rows and launch no
+    work; the others are unaffected."""
+    w = W.make_prefill(name="pfz", query_lens=[0, 130, 0, 7], cached_lens=[5, 20, 0, 300], Hq=8,
+                       Hkv=2, D=128, seed=3)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill(w, st)
+    ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                         w.query_start, w.scale)
+    assert_close(got, ref, "bf16", "prefill with empty sequences")
+    assert int(st.item()) == 0
+
+
 def test_prefill_single_token_rows_equal_decode():
     """A prefill chunk of one token per sequence is a decode step."""
     w = W.make_prefill(name="pf1", query_lens=[1, 1, 1, 1], cached_lens=[0, 15, 16, 700], Hq=32,
