@@ -22,6 +22,7 @@
  *   pkv_paged_prefill_attention        -- chunked, variable-length prefill (mixed batches) on tcgen05.
  *   pkv_paged_decode_attention_static_ws -- decode with a library-held workspace (no allocation).
  *   pkv_bm_*                           -- host block manager: allocation, refcounted prefix sharing.
+ *   pkv_xxh64, pkv_block_hash          -- the chained per-block prefix hash it keys shared blocks by.
  *   pkv_decode_split_chunk, pkv_decode_workspace_bytes, pkv_decode_shared_prefix_workspace_bytes
  *                                      -- the split rule and workspace sizes the calls use.
  *
@@ -61,7 +62,8 @@ extern "C" {
 typedef enum {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misalignment, aliasing */
-    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim not 64/128, block_size not 16 */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim not 64/128, block_size not 16,
+                                  or a pool / grid past the kernels' index limits */
     PKV_ERR_WORKSPACE = 3,     /* workspace smaller than pkv_decode_workspace_bytes() */
     PKV_ERR_CUDA = 4,          /* the CUDA runtime rejected a launch */
     PKV_ERR_NO_BLOCKS = 5      /* block manager: not enough free blocks (nothing was changed) */
