@@ -32,7 +32,8 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attn: KV GB/s vs GB300 HBM peak; decoded tokens/s per step"
-DEFAULT_CONFIG = 2          # the Llama-3-8B-shaped GQA decode: the metric's workload
+DEFAULT_CONFIG = 3          # long-context split-K decode (B=8, 32k-131k): the largest workload
+MIN_LOOP_MS = 1000.0        # the roofline and e2e loops run at least this much GPU time
 FALLBACK_HBM_GBS = 6800.0   # used only when MEASURED_PEAKS.json is absent
 L2_FLUSH_BYTES = 512 << 20
 PROFILES = os.path.join(ROOT, "profiles")
@@ -117,23 +118,42 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary for this
-    workload, if the kernel sources are unchanged since the capture (else None)."""
-    path = os.path.join(PROFILES, f"split_kernel_{workload}.md")
+    """DRAM bytes per launch of the split kernel for this workload from profiles/traffic.json (a
+    single-pass ncu capture), if the kernel sources are unchanged since the capture (else None)."""
+    path = os.path.join(PROFILES, "traffic.json")
     if not os.path.exists(path):
         return None
-    vals = {}
     with open(path) as f:
-        for line in f:
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha") != kernel_source_hash():
+        entry = json.load(f).get("split_kernel", {}).get(workload)
+    if not entry or entry.get("kernel_source_sha") != kernel_source_hash():
         return None
     try:
-        return int(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return int(entry["traffic_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
+
+
+def timed_loop(untimed, timed, min_ms: float, first: int, stream):
+    """Per iteration k: untimed(k) (the L2 flush), then timed(k) between a CUDA event pair on
+    `stream`. Runs in batches until the events add up to at least min_ms of GPU time and at least
+    `first` iterations ran. Returns (total ms inside the events, iterations)."""
+    import torch
+    total, n = 0.0, 0
+    while n < first or total < min_ms:
+        if n < first:
+            batch = first - n
+        else:  # enough iterations for the remaining time at the average so far, at most 2000
+            batch = max(1, min(2000, int((min_ms - total) / max(total / n, 1e-3)) + 1))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(batch)]
+        for i in range(batch):
+            untimed(n + i)
+            ev[i][0].record(stream)
+            timed(n + i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        total += sum(e[0].elapsed_time(e[1]) for e in ev)
+        n += batch
+    return total, n
 
 
 def attention_bytes(w: W.DecodeWorkload) -> int:
@@ -162,7 +182,7 @@ class ClockSampler:
             self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -390,6 +410,10 @@ def run_ours(args):
             pkv.paged_decode_attention(out, q, kp, vp, bt, cl, maxc, w.scale, args.chunk, ws,
                                        status, stream)
 
+    # nvidia-smi samples the clocks from before the warm-up to the end of the e2e loop: the K timed
+    # steps alone can be shorter than one sampling interval, the roofline and e2e loops are not
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(max(3, args.warmup)):
         flush_l2(1)
         write()
@@ -402,11 +426,9 @@ def run_ours(args):
     # one event pair per step: nothing between the write and the attention call, so the kernels
     # keep their programmatic-dependent-launch overlap
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
     t_wall = time.perf_counter()
     for k in range(K):
         flush_l2(k)                      # evict the previous step's lines (not timed)
@@ -418,18 +440,10 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     wall_s = time.perf_counter() - t_wall
-    clk = clocks.stop()
     step_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-    # the dominant kernels alone (the attention call: split + merge), for the roofline
-    KA = max(1, min(K, 500))
-    ea = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KA)]
-    for k in range(KA):
-        flush_l2(k)
-        ea[k][0].record(stream)
-        attend()
-        ea[k][1].record(stream)
-    torch.cuda.synchronize()
-    attn_ms = sum(e[0].elapsed_time(e[1]) for e in ea) * K / KA
+    # the dominant kernels alone (the attention call: split + merge), for the roofline: at least
+    # MIN_LOOP_MS of GPU time whatever K is
+    attn_total_ms, KA = timed_loop(flush_l2, lambda k: attend(), MIN_LOOP_MS, K, stream)
 
     step_bytes = W.kv_bytes(w)
     total_bytes, max_ms = aggregate(step_bytes * K, step_ms)
@@ -438,26 +452,22 @@ def run_ours(args):
     tokens_per_s = w.B * world * K / (max_ms / 1e3)
 
     # e2e through the public API: the step's inputs from pinned host memory each step (one copy of
-    # the staging buffer), out read back
+    # the staging buffer), out read back; also at least MIN_LOOP_MS of GPU time
     host_stage = stage.cpu().pin_memory()
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = host_stage.numel()
     d2h = out.numel() * out.element_size()
-    KE = max(1, min(K, 200))
-    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
     torch.cuda.synchronize()
-    for k in range(KE):
-        flush_l2(k)
-        ee[k][0].record(stream)
+
+    def e2e_step(k):
         stage.copy_(host_stage, non_blocking=True)
         write()
         attend()
         host_out.copy_(out, non_blocking=True)
-        ee[k][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in ee)
+    e2e_ms, KE = timed_loop(flush_l2, e2e_step, MIN_LOOP_MS, K, stream)
     e2e_bytes, e2e_max = aggregate(step_bytes * KE, e2e_ms)
     e2e_value = e2e_bytes / (e2e_max / 1e3) / 1e9
+    clk = clocks.stop()
 
     if rank != 0:
         if world > 1:
@@ -466,7 +476,7 @@ def run_ours(args):
 
     hbm, peak_kind = measured_peaks()
     attn_bytes = attention_bytes(w)
-    attn_avg_s = attn_ms / K / 1e3
+    attn_avg_s = attn_total_ms / KA / 1e3
     achieved = attn_bytes / attn_avg_s / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -491,13 +501,16 @@ def run_ours(args):
                                 " (CUDA events around the call); traffic: split kernel (ncu)"),
                      "traffic": profiled_traffic(w.name),
                      "algorithmic_bytes_per_launch": attn_bytes,
-                     "avg_launch_us": round(attn_avg_s * 1e6, 3)},
+                     "avg_launch_us": round(attn_avg_s * 1e6, 3), "launches_timed": KA,
+                     "timed_ms": round(attn_total_ms, 2)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": KE},
+                "d2h_bytes_per_step": d2h, "steps": KE, "timed_ms": round(e2e_ms, 2)},
         "gpu_launches": cuda_launches_per_step(w, chunk, cascade) * K,
         "wall_s": round(wall_s, 3),
     }
     if clk is not None:
+        clk["window"] = ("nvidia-smi every 100 ms from the warm-up to the end of the e2e loop "
+                         "(the timed steps, the roofline loop and the e2e loop)")
         line["clocks"] = clk
     if not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)

@@ -23,7 +23,8 @@
  *   pkv_paged_decode_attention_static_ws -- decode with a library-held workspace (no allocation).
  *   pkv_bm_*                           -- host block manager: allocation, refcounted prefix sharing.
  *   pkv_xxh64, pkv_block_hash          -- the chained per-block prefix hash it keys shared blocks by.
- *   pkv_decode_split_chunk, pkv_decode_workspace_bytes, pkv_decode_shared_prefix_workspace_bytes
+ *   pkv_decode_split_chunk, pkv_decode_workspace_bytes, pkv_decode_workspace_bytes_dtype,
+ *   pkv_decode_shared_prefix_workspace_bytes
  *                                      -- the split rule and workspace sizes the calls use.
  *
  * Layouts (all row-major, element strides implied by the shapes):
@@ -217,13 +218,26 @@ size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, i
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len, int split_chunk_tokens);
 
+/*
+ * The exact workspace bytes of one call of pkv_paged_decode_attention (kv_dtype PKV_F32 or
+ * PKV_BF16) or pkv_paged_decode_attention_int8 (kv_dtype PKV_I8) with this batch shape: the
+ * same split rule as pkv_decode_workspace_bytes, at the chunk pkv_decode_split_chunk gives for
+ * that K/V dtype, so it is never larger than that dtype-free bound (at most half of it when the
+ * bf16 head_dim-128 kernel takes a longer auto chunk). For the multi-token call pass
+ * num_seqs * num_query_tokens as num_seqs. 0 when no split is needed or for invalid arguments.
+ * Pure host arithmetic.
+ */
+size_t pkv_decode_workspace_bytes_dtype(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int max_context_len, int split_chunk_tokens,
+                                        pkv_dtype kv_dtype);
+
 /* The chunk (tokens per split before block rounding) that pkv_paged_decode_attention[_int8,
  * _multi] use for a request of split_chunk_tokens (0 = auto), this batch shape and K/V dtype
  * (num_seqs counts (sequence, query token) rows for the multi-token call); 0 for invalid
  * arguments. The same notes call the chunk a value calibrated by profiling the GPU; the auto rule
  * here is the power of two in [256, 4096] nearest below num_seqs * num_kv_heads *
  * max_context_len / (2 * U), where U is the number of (sequence, kv head, split) units the kernel
- * that serves the call does best with on a GB300 (152 SMs): 2048 for the bf16 head_dim-128
+ * that serves the call does best with on a GB300 (152 SMs): 1024 for the bf16 head_dim-128
  * tensor-core kernel, 4096 for the INT8 one and for the CUDA-core kernel (fp32, head_dim 64).
  * The chunk then grows until the split extent max(1, max_context_len / chunk) is at most 8192.
  * Pure host arithmetic. */
@@ -285,11 +299,14 @@ pkv_status pkv_paged_decode_attention_int8(void* out, const void* q, const int8_
  * `workspace_bytes`: the split-K partial states go to a fixed array of
  * PKV_STATIC_WORKSPACE_BYTES bytes inside the library (a file-scope __device__ array; every GPU
  * that loads the library holds it until the process exits). A batch whose partial states need
- * more than that (pkv_decode_workspace_bytes(...) > PKV_STATIC_WORKSPACE_BYTES) is refused with
- * PKV_ERR_WORKSPACE before anything is enqueued; a larger split_chunk_tokens needs less.
+ * more than that (pkv_decode_workspace_bytes_dtype(..., dtype) > PKV_STATIC_WORKSPACE_BYTES, the
+ * exact size at the chunk this call uses) is refused with PKV_ERR_WORKSPACE before anything is
+ * enqueued; a larger split_chunk_tokens needs less.
  * The first call made while a given device is current looks up the array's device address on
- * that device (cudaGetSymbolAddress) and caches it; make that first call before any stream
- * capture. The current device must be the one `stream` belongs to.
+ * that device (cudaGetSymbolAddress) and caches it with the id of the current context; a call in
+ * another context on that device (after cudaDeviceReset, for one) looks it up again. Make the
+ * first call on each device, and the first after a reset, before any stream capture. The current
+ * device must be the one `stream` belongs to.
  * All calls share the one array per device and it keeps the last call's contents (nothing in it
  * needs to start at zero): calls whose work overlaps on the GPU -- on different streams, or from
  * different host threads -- race on it and must be serialised by the caller.

@@ -26,6 +26,7 @@ SIGNATURES = {
     "pkv_kv_cache_write": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_kv_cache_write_int8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "pkv_decode_workspace_bytes_dtype": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "pkv_decode_split_chunk": ([_I, _I, _I, _I, _I, _I], _I),
     "pkv_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                     _I, _I, _P, _SZ, _P, _P], _I),
@@ -131,6 +132,14 @@ def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_co
                            split_chunk_tokens=0) -> int:
     return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  max_context_len, split_chunk_tokens))
+
+
+def decode_workspace_bytes_dtype(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                 split_chunk_tokens=0, kv_dtype=BF16) -> int:
+    """The exact workspace bytes of one decode call whose K/V pools have element type kv_dtype."""
+    return int(load().pkv_decode_workspace_bytes_dtype(num_seqs, num_q_heads, num_kv_heads,
+                                                       head_dim, max_context_len,
+                                                       split_chunk_tokens, kv_dtype))
 
 
 def decode_split_chunk(num_seqs, num_kv_heads, head_dim, max_context_len, split_chunk_tokens=0,

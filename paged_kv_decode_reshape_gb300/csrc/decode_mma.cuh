@@ -35,8 +35,9 @@
 // ldmatrix.trans of the int8 tiles read as 16-bit pairs; each register of 4 int8 becomes two
 // fp16x2 operands holding 1152 + x exactly (byte-permute conversion of Kim et al. 2022), and the
 // constant 1152 is taken out once per score (1152 * sum q') and once per output (1152 * sum of
-// the fp16 weights), not per element. q is pre-scaled by scale*log2(e) into fp16; the per-token
-// K scale multiplies the score and the V scale the softmax weight. Dims are consumed in a fixed
+// the fp16 weights), not per element. q enters fp16 exactly, scaled by one power of two per CTA;
+// the per-token K scale times scale*log2(e) and that power's inverse multiplies the score, and the
+// V scale the softmax weight. Dims are consumed in a fixed
 // permuted order that q's fragments and the output mapping follow, which leaves the dot
 // products unchanged.
 #pragma once
@@ -302,10 +303,44 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
         if (lane == 0) issue(k, bid);
     }
 
+    // INT8: q enters the fp16 MMAs as q' = q * 2^e, e one power of two for the CTA's columns, so
+    // that the largest |q'| lies in [2^14, 2^15): exact, as a bf16 value scaled by a power of two
+    // fits fp16's 11-bit significand, and never past fp16's range whatever q's magnitude. The
+    // scores' multiplier (the per-token K scale) then carries scale * log2(e) * 2^-e in fp32.
+    float score_mult = p.scale_log2;  // bf16: scale * log2(e); INT8: that times 2^-e
     {
         // q as the B operand of S^T = K Q^T: b0b1 = (dims k0 + 2c, +1; head r), b2b3 = (+8, +9)
         uint32_t qb[kNT][8][2];
         float qsum[kNT];  // INT8: sum of this lane's fp16 q' values of column 8t + r (as the MMA sees them)
+        float q_up = 1.f;  // INT8: 2^e
+        if constexpr (kI8) {
+            // every warp loads all of the CTA's columns, so a warp-wide max covers them all
+            float amax = 0.f;
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+                if (8 * t + r < nh) {
+                    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                                ((size_t)col_zb(8 * t + r) * p.Hq + col_head(8 * t + r)) * kMmaD;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
+                        float f0, f1, f2, f3;
+                        bf16x2_to_f32(raw4.x, f0, f1);
+                        bf16x2_to_f32(raw4.y, f2, f3);
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 1; off <= 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            int e = 0;
+            if (amax > 0.f) {  // floor(log2(amax)) from the exponent field (-127 for a subnormal amax)
+                e = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xffu) - 127);
+                e = e < -126 ? -126 : (e > 126 ? 126 : e);  // 2^e and 2^-e stay normal floats
+            }
+            q_up = __uint_as_float((uint32_t)(127 + e) << 23);
+            score_mult = p.scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23);
+        }
 #pragma unroll
         for (int t = 0; t < kNT; ++t) {
             qsum[t] = 0.f;
@@ -322,9 +357,8 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                     float f0, f1, f2, f3;
                     bf16x2_to_f32(raw4.x, f0, f1);
                     bf16x2_to_f32(raw4.y, f2, f3);
-                    const float sc = p.scale_log2;
-                    qb[t][ks][0] = hv ? pack_h2(f0 * sc, f2 * sc) : 0u;
-                    qb[t][ks][1] = hv ? pack_h2(f1 * sc, f3 * sc) : 0u;
+                    qb[t][ks][0] = hv ? pack_h2(f0 * q_up, f2 * q_up) : 0u;
+                    qb[t][ks][1] = hv ? pack_h2(f1 * q_up, f3 * q_up) : 0u;
                     const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[t][ks][0]));
                     const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[t][ks][1]));
                     qsum[t] += (u0.x + u0.y) + (u1.x + u1.y);
@@ -420,11 +454,11 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
                 // s[t][0] = (tok r, col 8t+2c), [1] = (tok r, 8t+2c+1), [2] = (tok r+8, 8t+2c), [3] = (tok r+8, 8t+2c+1)
                 const int nvalid = t1 - (t0 + j * kBlockSize);  // >= 1; >= 16 for full blocks
                 // score multipliers: the K scale (INT8) or scale * log2(e) (bf16) per token row
-                float vs0 = 1.f, vs1 = 1.f, ks0 = p.scale_log2, ks1 = p.scale_log2;
+                float vs0 = 1.f, vs1 = 1.f, ks0 = score_mult, ks1 = score_mult;
                 if constexpr (kI8) {
                     const float* sc = scl + st * 2 * kBlockSize;
-                    ks0 = sc[r];
-                    ks1 = sc[r + 8];
+                    ks0 = sc[r] * score_mult;
+                    ks1 = sc[r + 8] * score_mult;
                     vs0 = sc[kBlockSize + r];
                     vs1 = sc[kBlockSize + r + 8];
                 }

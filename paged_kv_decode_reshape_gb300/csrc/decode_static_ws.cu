@@ -9,8 +9,12 @@
 //
 // The array is a file-scope __device__ array of PKV_STATIC_WORKSPACE_BYTES bytes; every GPU that
 // loads this library holds it until the process exits. Its name in host code is only a host-side
-// stand-in, so the device address is looked up with cudaGetSymbolAddress, once per device, on
-// the first call made while that device is current, and cached.
+// stand-in, so the device address is looked up with cudaGetSymbolAddress on the first call made
+// while a device is current, and cached for that device together with the unique id of the
+// context it was looked up in. A later call in another context on the same device (after
+// cudaDeviceReset, say, when the module may load at another address) looks the address up again.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -22,19 +26,51 @@ static __device__ __align__(256) unsigned char g_static_workspace[PKV_STATIC_WOR
 constexpr int kMaxDevices = 128;
 std::mutex g_mutex;
 void* g_device_ptr[kMaxDevices] = {};
+unsigned long long g_context_id[kMaxDevices] = {};
 
-// Device address of the static workspace on the current device (set-up on first use).
+// Unique id of the current context (cuCtxGetId, through the runtime's driver entry-point query so
+// that the library needs no link against the driver library); false if it cannot be read.
+bool current_context_id(unsigned long long* id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the static workspace on the current device (looked up on first use there,
+// and again whenever the device's context has changed since).
 pkv_status static_workspace(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_device_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr)
-            return PKV_ERR_CUDA;
-        g_device_ptr[dev] = p;
+    if (have_ctx && g_device_ptr[dev] != nullptr && g_context_id[dev] == ctx) {
+        *out = g_device_ptr[dev];
+        return PKV_OK;
     }
-    *out = g_device_ptr[dev];
+    // set-up: the lookup also makes the device's primary context current on this thread if no
+    // context was, so the context id is read after it
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
+    if (!current_context_id(&ctx)) return PKV_ERR_CUDA;
+    g_device_ptr[dev] = p;
+    g_context_id[dev] = ctx;
+    *out = p;
     return PKV_OK;
 }
 
@@ -45,9 +81,11 @@ extern "C" pkv_status pkv_paged_decode_attention_static_ws(
     const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
     pkv_dtype dtype, int split_chunk_tokens, int32_t* status, void* stream) {
-    // bytes of partial states this batch needs; beyond the array's size the call is refused
-    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                   max_context_len, split_chunk_tokens);
+    if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    // the exact bytes of partial states this call uses (its own chunk for this dtype); beyond the
+    // array's size the call is refused before anything is enqueued
+    const size_t need = pkv_decode_workspace_bytes_dtype(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                         max_context_len, split_chunk_tokens, dtype);
     if (need > (size_t)PKV_STATIC_WORKSPACE_BYTES) return PKV_ERR_WORKSPACE;
     void* ws = nullptr;
     const pkv_status st = static_workspace(&ws);

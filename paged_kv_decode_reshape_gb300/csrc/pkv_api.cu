@@ -335,6 +335,19 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
     return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
 }
 
+size_t pkv_decode_workspace_bytes_dtype(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int max_context_len, int split_chunk_tokens,
+                                        pkv_dtype kv_dtype) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_context_len < 0 || split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize ||
+        (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8))
+        return 0;
+    // the chunk run_decode picks for this shape and K/V dtype, hence its exact split extent
+    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens,
+                                   target_units(head_dim, kv_dtype));
+    return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
+}
+
 pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_pool,
                                       const void* v_pool, const int32_t* block_tables,
                                       const int32_t* context_lens, int num_seqs, int num_q_heads,

@@ -13,8 +13,8 @@
 //
 // One CTA computes 128 query rows of one query head against 128-key tiles. Both products read
 // their A operand from tensor memory: measured on GB300, a tcgen05.mma (M = 128, K = 16) with A in
-// TMEM takes ~82 cycles at N = 128 (the tensor peak), while with A in shared memory it takes
-// ~142 cycles at N = 64 or 128 and reaches the peak only at N = 256. TMEM columns:
+// TMEM takes ~90 cycles at N = 128 (the tensor peak), while with A in shared memory it takes
+// ~157 cycles at N = 64 or 128 and reaches the peak only at N = 256. TMEM columns:
 //   O   0-127     fp32 accumulator, row r in lane r
 //   Q   128-191   the CTA's 128 query rows, two bf16 dims per column (written once)
 //   P   192-255 (buffer 0), 256-319 (buffer 1): bf16 weights of a key tile, two keys per column

@@ -89,6 +89,21 @@ def test_workspace_arithmetic(pkv):
     assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 128, 1000, 2048, 0) == 0  # prefix > context
     # the workspace bound covers the bf16 call (fewer splits) too
     assert L.pkv_decode_workspace_bytes(64, 32, 8, 128, 4055, 0) == 64 * 32 * (4055 // 256) * 130 * 4
+    # the exact per-dtype size: the split extent at that dtype's own auto chunk
+    WB = L.pkv_decode_workspace_bytes_dtype
+    assert WB(64, 32, 8, 128, 4055, 0, BF) == 64 * 32 * (4055 // 1024) * 130 * 4
+    assert WB(8, 32, 8, 128, 131072, 0, BF) == 8 * 32 * 32 * 130 * 4           # chunk 4096
+    assert WB(8, 32, 8, 128, 131072, 0, I8) == L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 0)
+    assert WB(128, 64, 8, 128, 8083, 0, I8) == 128 * 64 * (8083 // 1024) * 130 * 4
+    assert WB(64, 32, 8, 64, 4055, 0, BF) == 64 * 32 * (4055 // 256) * 66 * 4   # CUDA-core kernel
+    assert WB(8, 32, 8, 128, 131072, 1024, BF) == 8 * 32 * 128 * 130 * 4        # forced chunk
+    assert WB(4, 4, 4, 64, 100, 0, F32) == 0                                     # one split
+    assert WB(4, 4, 4, 64, 100, 0, 7) == 0                                       # unknown dtype
+    for shape in [(64, 32, 8, 128, 4055), (8, 32, 8, 128, 131072), (3, 8, 2, 128, 700),
+                  (256, 32, 8, 128, 4090), (1, 64, 8, 128, 1 << 17)]:
+        for c in (0, 16, 512):
+            for dt in (F32, BF, I8):  # never above the dtype-free bound
+                assert WB(*shape, c, dt) <= L.pkv_decode_workspace_bytes(*shape, c)
 
 
 def _attn(L, **kw):

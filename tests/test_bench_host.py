@@ -80,13 +80,27 @@ def test_clock_rows_parser():
 
 
 def test_profiled_traffic_is_null_when_sources_changed(tmp_path, monkeypatch):
+    import json
     monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
-    (tmp_path / "split_kernel_x.md").write_text(
-        "- kernel_source_sha: `deadbeef`\n- traffic_bytes_per_launch: 1234\n")
-    assert bench.profiled_traffic("x") is None
-    (tmp_path / "split_kernel_x.md").write_text(
-        f"- kernel_source_sha: `{bench.kernel_source_hash()}`\n- traffic_bytes_per_launch: 1234\n")
+    assert bench.profiled_traffic("x") is None                     # no data file
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps({"split_kernel": {"x": {"kernel_source_sha": "deadbeef",
+                                                    "traffic_bytes_per_launch": 1234}}}))
+    assert bench.profiled_traffic("x") is None                     # captured on other sources
+    f.write_text(json.dumps({"split_kernel": {"x": {"kernel_source_sha": bench.kernel_source_hash(),
+                                                    "traffic_bytes_per_launch": 1234}}}))
     assert bench.profiled_traffic("x") == 1234
+    assert bench.profiled_traffic("y") is None                     # no capture of that workload
+
+
+def test_committed_traffic_file_covers_the_bench_workloads():
+    import json
+    import os
+    with open(os.path.join(bench.PROFILES, "traffic.json")) as fh:
+        d = json.load(fh)["split_kernel"]
+    for name in ("llama3_8b_gqa", "long_splitk", "int8_kv", "prefix_shared"):
+        assert int(d[name]["traffic_bytes_per_launch"]) > 0
+        assert len(d[name]["kernel_source_sha"]) == 16
 
 
 def test_source_fingerprint_ignores_comments_and_layout_only():

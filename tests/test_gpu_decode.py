@@ -1,9 +1,10 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs.
 
 Element-by-element at sizes the oracle finishes in seconds (several splits, ragged tails), on
-sampled sequences at the five full workload sizes, plus the invariants and edge cases.
+every sequence and head of the five full workloads, plus the invariants and edge cases.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -81,17 +82,30 @@ def test_decode_step_matches_oracle(cfg):
     assert int(st.item()) == 0
 
 
-@pytest.mark.parametrize("cfg,rows", [(2, [0, 17, 63]), (3, [0, 5]), (4, [3, 64, 127]),
-                                      (5, [0, 128, 255])])
-def test_full_size_sampled_sequences(cfg, rows):
-    """The full workload in the launch configuration the bench times; the oracle checks a sample
-    of sequences (every head), including the longest one."""
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_full_size_every_sequence(cfg):
+    """The full workload, in the launch configuration the bench times (auto chunk, write then
+    attention on one stream; the shared-prefix batch also through the cascade call the bench
+    uses), compared with the oracle element by element over every sequence and every head."""
     w = W.make_config(cfg)
-    rows = sorted(set(rows) | {int(np.argmax(w.context_lens))})
     d = DevWorkload(w)
-    got = to_f64(d.step())[rows]
-    ref = oracle_step(w, rows=rows, num_threads=16)
-    assert_close(got, ref, w.kv_dtype, f"config {cfg} rows {rows}")
+    st = status_tensor()
+    got = to_f64(d.step(status=st))
+    ref = oracle_step(w, num_threads=os.cpu_count() or 8)
+    assert got.shape == (w.B, w.Hq, w.D)
+    assert_close(got, ref, w.kv_dtype, f"config {cfg}, all {w.B} sequences")
+    if w.shared_prefix_blocks:
+        prefix = w.shared_prefix_blocks * w.BS
+        nbytes = P.decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.max_context_len,
+                                                        prefix, 0)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(d.q)
+        P.paged_decode_attention_shared_prefix(out, d.q, d.k_pool, d.v_pool, d.block_tables,
+                                               d.context_lens, w.max_context_len, w.scale, prefix,
+                                               0, ws, st)
+        assert_close(to_f64(out), ref, "bf16", f"config {cfg} cascade call, all sequences")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
 
 
 @pytest.mark.parametrize("chunk", [16, 48, 64, 256, 4096])
@@ -311,6 +325,44 @@ def test_extreme_score_ranges(kv, case):
         got = to_f64(d.attend(chunk=chunk))
         assert np.all(np.isfinite(got))
         assert_close(got, ref, kv, f"{kv} {case} chunk {chunk}")
+
+
+def _outlier_workload(kv, mag, ndims, seed):
+    """A G = 8 batch (Hq 16, Hkv 2) whose queries carry `ndims` outlier dims of magnitude `mag`
+    (signs random, bf16-rounded); ndims = 128 scales the whole query by `mag` instead."""
+    lens = [1, 40, 700, 2100]
+    w = W.make_decode(name="outliers", B=len(lens), Hq=16, Hkv=2, D=128, context_lens=lens,
+                      kv_dtype=kv, q_dtype="bf16", seed=seed)
+    rng = np.random.default_rng(seed)
+    q = W.bf16_bits_to_f32(w.q).copy()
+    if ndims == w.D:
+        q *= np.float32(mag)
+    else:
+        for b in range(w.B):
+            for h in range(w.Hq):
+                dims = rng.choice(w.D, ndims, replace=False)
+                q[b, h, dims] = np.float32(mag) * np.sign(rng.standard_normal(ndims)).astype(np.float32)
+    return W.DecodeWorkload(**{**w.__dict__, "q": W.f32_to_bf16_bits(q)})
+
+
+@pytest.mark.parametrize("kv", ["bf16", "i8"])
+@pytest.mark.parametrize("mag,ndims", [(1e2, 4), (1e3, 2), (1e4, 1), (1e4, 4), (1e6, 3), (1e-6, 128),
+                                       (3e4, 128)])
+def test_outlier_query_magnitudes(kv, mag, ndims):
+    """Queries with a few outlier dims of the magnitudes LLM activations reach (10^2 - 10^4), some
+    past fp16's range once scaled (10^6 in a few dims, 3e4 in every dim: the INT8 kernel's fp16
+    operands must not overflow), and queries of tiny values throughout (1e-6: near-uniform
+    weights), at the same bars as every other parity case."""
+    w = _outlier_workload(kv, mag, ndims, seed=int(np.log10(mag) * 10) + ndims + (0 if kv == "bf16" else 500))
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                        w.scale, w.k_scales, w.v_scales)
+    d = DevWorkload(w)
+    for chunk in (0, 64):
+        st = status_tensor()
+        got = to_f64(d.attend(chunk=chunk, status=st))
+        assert np.all(np.isfinite(got))
+        assert_close(got, ref, kv, f"{kv} |q| {mag} in {ndims} dims, chunk {chunk}")
+        assert int(st.item()) == 0
 
 
 def test_bad_block_ids_are_skipped_and_flagged():

@@ -27,8 +27,8 @@ def run_prefill(w, status=None, bt=None):
     return to_f64(out)
 
 
-# G = 4, 1, 8, 3, 2, 16: every cluster size the launcher picks (query heads of one GQA group share
-# each K/V tile through multicast) and the unclustered path
+# G = 4, 1, 8, 3, 2, 16: the kernel runs one query head per CTA (no clusters); each GQA group size
+# changes which kv head a CTA's head reads and how the heads of a group fall on the grid
 @pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2), (6, 2), (4, 2), (32, 2)])
 def test_prefill_matches_oracle(hq, hkv):
     w = W.make_prefill(name="pf", query_lens=[1, 5, 127, 128, 129, 300],
