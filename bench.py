@@ -443,7 +443,7 @@ def run_ours(args):
     step_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     # the dominant kernels alone (the attention call: split + merge), for the roofline: at least
     # MIN_LOOP_MS of GPU time whatever K is
-    attn_total_ms, KA = timed_loop(flush_l2, lambda k: attend(), MIN_LOOP_MS, K, stream)
+    attn_total_ms, KA = timed_loop(flush_l2, lambda k: attend(), args.min_loop_ms, K, stream)
 
     step_bytes = W.kv_bytes(w)
     total_bytes, max_ms = aggregate(step_bytes * K, step_ms)
@@ -464,7 +464,7 @@ def run_ours(args):
         write()
         attend()
         host_out.copy_(out, non_blocking=True)
-    e2e_ms, KE = timed_loop(flush_l2, e2e_step, MIN_LOOP_MS, K, stream)
+    e2e_ms, KE = timed_loop(flush_l2, e2e_step, args.min_loop_ms, K, stream)
     e2e_bytes, e2e_max = aggregate(step_bytes * KE, e2e_ms)
     e2e_value = e2e_bytes / (e2e_max / 1e3) / 1e9
     clk = clocks.stop()
@@ -671,6 +671,9 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
     ap.add_argument("--chunk", type=int, default=0, help="split chunk in tokens (0 = auto)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--min-loop-ms", type=float, default=MIN_LOOP_MS,
+                    help="GPU time the roofline and e2e loops run at least (0: exactly --steps "
+                         "iterations each, e.g. under a profiler)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="run a shared-prefix workload through the plain decode call instead of "
                          "the shared-prefix (cascade) call")

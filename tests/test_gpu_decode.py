@@ -327,9 +327,10 @@ def test_extreme_score_ranges(kv, case):
         assert_close(got, ref, kv, f"{kv} {case} chunk {chunk}")
 
 
-def _outlier_workload(kv, mag, ndims, seed):
+def _outlier_workload(kv, mag, ndims, k_mult, seed):
     """A G = 8 batch (Hq 16, Hkv 2) whose queries carry `ndims` outlier dims of magnitude `mag`
-    (signs random, bf16-rounded); ndims = 128 scales the whole query by `mag` instead."""
+    (signs random, bf16-rounded; ndims = 128 scales the whole query by `mag` instead), with every
+    key multiplied by k_mult (bf16 pools: the values, re-rounded; INT8 pools: the K scales)."""
     lens = [1, 40, 700, 2100]
     w = W.make_decode(name="outliers", B=len(lens), Hq=16, Hkv=2, D=128, context_lens=lens,
                       kv_dtype=kv, q_dtype="bf16", seed=seed)
@@ -342,18 +343,32 @@ def _outlier_workload(kv, mag, ndims, seed):
             for h in range(w.Hq):
                 dims = rng.choice(w.D, ndims, replace=False)
                 q[b, h, dims] = np.float32(mag) * np.sign(rng.standard_normal(ndims)).astype(np.float32)
-    return W.DecodeWorkload(**{**w.__dict__, "q": W.f32_to_bf16_bits(q)})
+    changes = {"q": W.f32_to_bf16_bits(q)}
+    if kv == "bf16":
+        changes["k_pool"] = W.f32_to_bf16_bits(W.bf16_bits_to_f32(w.k_pool) * np.float32(k_mult))
+    else:
+        changes["k_scales"] = (w.k_scales * np.float32(k_mult)).astype(np.float32)
+    return W.DecodeWorkload(**{**w.__dict__, **changes})
 
 
 @pytest.mark.parametrize("kv", ["bf16", "i8"])
-@pytest.mark.parametrize("mag,ndims", [(1e2, 4), (1e3, 2), (1e4, 1), (1e4, 4), (1e6, 3), (1e-6, 128),
-                                       (3e4, 128)])
-def test_outlier_query_magnitudes(kv, mag, ndims):
-    """Queries with a few outlier dims of the magnitudes LLM activations reach (10^2 - 10^4), some
-    past fp16's range once scaled (10^6 in a few dims, 3e4 in every dim: the INT8 kernel's fp16
-    operands must not overflow), and queries of tiny values throughout (1e-6: near-uniform
-    weights), at the same bars as every other parity case."""
-    w = _outlier_workload(kv, mag, ndims, seed=int(np.log10(mag) * 10) + ndims + (0 if kv == "bf16" else 500))
+@pytest.mark.parametrize("mag,ndims,k_mult", [
+    (1e2, 4, 1.0), (1e3, 2, 1.0), (1e4, 1, 1.0), (1e4, 4, 1.0),   # outlier dims, N(0, 1) keys
+    (1e6, 3, 1e-4), (1e6, 128, 1e-5),  # |q * scale| past fp16's range, logits of ordinary size
+    (1e-6, 128, 1.0),                  # tiny queries: near-uniform weights
+    (1e-4, 128, 1e4),                  # q * scale below fp16's normal range, logits of ordinary size
+])
+def test_outlier_query_magnitudes(kv, mag, ndims, k_mult):
+    """Queries with a few outlier dims of the magnitudes LLM activations reach (10^2 - 10^4), and
+    queries whose magnitude times the softmax scale falls outside fp16's normal range while the
+    keys keep the logits of ordinary size: the INT8 kernel's fp16 operands must neither overflow
+    nor lose precision there. Same bars as every other parity case.
+
+    Not covered, by design: logits of 10^5 and more (|q| ~ 10^6 against unit keys). An fp32 score
+    of that size resolves only ~|s| * 2^-24, and a dot product whose terms span 10^6 down to 1
+    loses the small ones in any fp32 accumulation, so no fp32 kernel meets the bf16 bar there."""
+    seed = int(round(np.log10(mag) * 10)) + ndims + int(round(np.log10(k_mult))) * 7 + (0 if kv == "bf16" else 500)
+    w = _outlier_workload(kv, mag, ndims, k_mult, seed=seed)
     ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
                                         w.scale, w.k_scales, w.v_scales)
     d = DevWorkload(w)
@@ -361,7 +376,7 @@ def test_outlier_query_magnitudes(kv, mag, ndims):
         st = status_tensor()
         got = to_f64(d.attend(chunk=chunk, status=st))
         assert np.all(np.isfinite(got))
-        assert_close(got, ref, kv, f"{kv} |q| {mag} in {ndims} dims, chunk {chunk}")
+        assert_close(got, ref, kv, f"{kv} |q| {mag} in {ndims} dims, keys x {k_mult}, chunk {chunk}")
         assert int(st.item()) == 0
 
 
