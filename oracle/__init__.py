@@ -107,6 +107,21 @@ def kv_cache_write(k_new, v_new, k_pool, v_pool, slot_mapping, k_new_scales=None
     return kp, vp, ks, vs
 
 
+def copy_blocks(k_pool, v_pool, pairs, k_scales=None, v_scales=None):
+    """Copy-on-write for forked sequences ("LLM Primer VI, Chapter 8", section 8.1, blocks
+    shared by reference count; the copy itself is a reading, listed in the design notes): for
+    each (src, dst) in order, block dst of both pools -- every kv head, every slot -- and, for
+    INT8 pools, its rows of scales become a copy of block src. Returns new arrays."""
+    kp, vp = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+    ks = None if k_scales is None else np.array(k_scales, copy=True)
+    vs = None if v_scales is None else np.array(v_scales, copy=True)
+    for src, dst in pairs:
+        for a in (kp, vp, ks, vs):
+            if a is not None:
+                a[dst] = a[src]
+    return kp, vp, ks, vs
+
+
 def quantize_rows_int8(x):
     """int8 codes and fp32 scales of each last-axis row of x (float32 or bf16 bits)."""
     x = np.ascontiguousarray(x)

@@ -55,9 +55,9 @@ def test_block_hash_is_xxh64_of_prefix_then_int64_tokens(pkv):
     h.update(np.array(token_ids).tobytes()), h.intdigest()."""
     toks = np.arange(100, 116, dtype=np.int64)
     first = SYS_XXH64(toks.tobytes())
-    assert P.block_hash(toks) == first == O.compute_hash(toks)
+    assert P.block_hash(toks) == first == O.chain_hash(toks)
     second = SYS_XXH64(first.to_bytes(8, "little") + (toks + 16).tobytes())
-    assert P.block_hash(toks + 16, first) == second == O.compute_hash(toks + 16, first)
+    assert P.block_hash(toks + 16, first) == second == O.chain_hash(toks + 16, first)
     # the same tokens under a different prefix hash differently
     assert P.block_hash(toks + 16, first) != P.block_hash(toks + 16)
 
@@ -101,8 +101,8 @@ def _compare(bm, ob, live):
         a, ca = bm.batch_tables(live, mb)
         b, cb = ob.batch_tables(live, mb)
         assert np.array_equal(a, b) and np.array_equal(ca, cb)
-    for i, blk in enumerate(ob.blocks):
-        assert bm.ref_count(i) == blk.ref_count
+    for i in range(len(ob.users)):
+        assert bm.ref_count(i) == ob.ref_count(i)
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -135,7 +135,7 @@ def test_manager_matches_oracle_on_random_scripts(pkv, seed, prefix_cache):
             ok = ob.can_append(sid, k)
             assert bm.can_append(sid, k) == ok
             if ok:
-                assert np.array_equal(bm.append(sid, toks), ob.append(sid, toks))
+                assert np.array_equal(bm.append(sid, toks), ob.append(sid, toks)[0])
                 assert bm.context_len(sid) == len(ob.seqs[sid]["tokens"])
         else:
             sid = live.pop(int(rng.integers(len(live))))
@@ -169,3 +169,125 @@ def test_freed_prefix_blocks_are_found_again(pkv):
     bm.free(1)
     assert bm.allocate(2, toks) == 64  # every block still cached on the free list
     assert bm.batch_tables([2], 4)[0][0].tolist() == first
+
+
+# ---- fork and copy-on-write: pins of the oracle itself ------------------------------------------
+
+def _read_slots(pool, table, n, bs=16):
+    """The tokens a sequence sees: logical position t read through its table from the pool."""
+    return [pool[table[t // bs] * bs + t % bs] for t in range(n)]
+
+
+def _play(ob, pool, seq_id, toks):
+    """Append through the oracle and apply what it reports to a token-per-slot pool: the copies
+    first (whole blocks), then the new tokens into their slots."""
+    slots, copies = ob.append(seq_id, toks)
+    for src, dst in copies:
+        pool[dst * 16:(dst + 1) * 16] = pool[src * 16:(src + 1) * 16]
+    for sl, t in zip(slots, toks):
+        pool[int(sl)] = int(t)
+    return copies
+
+
+@pytest.mark.parametrize("prompt_len", [2000, 2001, 2013, 15, 16, 1])
+def test_oracle_fork_and_copy_on_write_keep_every_sequence_its_own_tokens(prompt_len):
+    """Best-of-8 by forking: whatever the prompt length, every sample must read back exactly its
+    own tokens through its table after all samples appended (in interleaved order) -- which
+    fails if a sample writes into a block another sample still references, or if a copy goes the
+    wrong way -- and the prompt's full blocks stay shared."""
+    rng = np.random.default_rng(prompt_len)
+    ob = O.BlockManager(2048, 16)
+    pool = [None] * (2048 * 16)
+    prompt = [int(t) for t in rng.integers(0, 32000, prompt_len)]
+    ob.allocate(0, prompt)
+    for sl, t in zip(range(prompt_len), prompt):
+        tb = ob.seqs[0]["table"]
+        pool[tb[sl // 16] * 16 + sl % 16] = t
+    for c in range(1, 8):
+        ob.fork(0, c)
+    own = {s: list(prompt) for s in range(8)}
+    ncopies = 0
+    for step in range(100):
+        for s in rng.permutation(8):
+            t = int(rng.integers(0, 32000))
+            ncopies += len(_play(ob, pool, int(s), [t]))
+            own[int(s)].append(t)
+    for s in range(8):
+        rec = ob.seqs[s]
+        assert rec["tokens"] == own[s]
+        assert _read_slots(pool, rec["table"], len(own[s])) == own[s]
+    partial = prompt_len % 16 != 0
+    assert ncopies == (7 if partial else 0)     # all but the last writer of the shared tail copy
+    full = prompt_len // 16
+    for j in range(full):                        # full prompt blocks: still one shared copy
+        assert len({ob.seqs[s]["table"][j] for s in range(8)}) == 1
+        assert ob.ref_count(ob.seqs[0]["table"][j]) == 8
+    for s in range(8):
+        ob.free_seq(s)
+    assert len(ob.free) == 2048 and all(u == 0 for u in ob.users)
+
+
+def test_oracle_best_of_8_by_fork_gives_the_pages_token_slots():
+    """Chapter 8 primer, section 8.1: best-of-8 on a 2,000-token prompt holds 2,800 token slots
+    instead of 16,800 (tests/golden/best_of_8_token_slots.txt), here by forking one prompt."""
+    g = _read_gold("best_of_8_token_slots.txt")
+    n, prompt, new = g["samples"], g["prompt_tokens"], g["new_tokens_per_sample"]
+    ob = O.BlockManager(4096, 16)
+    ob.allocate(0, list(range(prompt)))
+    for c in range(1, n):
+        ob.fork(0, c)
+    copies = []
+    for s in range(n):
+        copies += ob.append(s, [7 + s] * new)[1]
+    assert copies == []                        # 2,000 tokens fill 125 blocks: nothing to copy
+    slots = set()
+    for s in range(n):
+        rec = ob.seqs[s]
+        slots |= {rec["table"][t // 16] * 16 + t % 16 for t in range(len(rec["tokens"]))}
+    assert len(slots) == g["slots_with_sharing"]
+    assert n * (prompt + new) == g["slots_without_sharing"]
+    assert 4096 - len(ob.free) == prompt // 16 + n * -(-new // 16)
+
+
+def test_oracle_can_append_counts_the_copy():
+    ob = O.BlockManager(4, 16)
+    ob.allocate(0, list(range(20)))             # 2 blocks, the second holds 4 tokens
+    ob.fork(0, 1)
+    assert ob.can_append(0, 1)                  # 2 free: the copy takes one
+    ob.allocate(2, list(range(100, 117)))       # takes the last 2
+    assert not ob.can_append(0, 1)              # the copy needs a block, none is free
+    assert not ob.can_append(1, 12)
+    ob.free_seq(2)
+    slots, copies = ob.append(1, [5])
+    assert len(copies) == 1 and copies[0][0] == ob.seqs[0]["table"][1]
+    slots, copies = ob.append(0, [6])           # now the only user: writes in place
+    assert copies == [] and int(slots[0]) == ob.seqs[0]["table"][1] * 16 + 4
+
+
+def test_oracle_chain_hash_links_blocks():
+    """Section 5.2: a block's hash covers the previous block's hash, so equal tokens in another
+    context hash differently; the first block of a sequence hashes its tokens alone."""
+    toks = list(range(500, 516))
+    first = O.chain_hash(toks)
+    assert first == O.xxh64(np.asarray(toks, dtype="<i8").tobytes())
+    assert O.chain_hash(toks, first) == O.xxh64(first.to_bytes(8, "little") + np.asarray(toks, dtype="<i8").tobytes())
+    assert O.chain_hash(toks, first) != first
+    if SYS_XXH64 is not None:
+        assert first == SYS_XXH64(np.asarray(toks, dtype="<i8").tobytes())
+
+
+def test_oracle_prefix_hits_count_their_references():
+    """A second prompt with the same first blocks shares them (section 5.2 with the reference
+    counts of section 5.1): each shared block has two users, and freeing one sequence keeps them
+    out of the free list until the other goes too."""
+    ob = O.BlockManager(16, 16)
+    prompt = list(range(1000, 1040))            # 2 full blocks + 8 tokens
+    assert ob.allocate(0, prompt) == 0
+    assert ob.allocate(1, prompt) == 32
+    t0, t1 = ob.seqs[0]["table"], ob.seqs[1]["table"]
+    assert t0[:2] == t1[:2] and t0[2] != t1[2]
+    assert [ob.ref_count(b) for b in t0] == [2, 2, 1]
+    ob.free_seq(0)
+    assert t1[0] not in ob.free and t1[1] not in ob.free and len(ob.free) == 16 - 3
+    ob.free_seq(1)
+    assert len(ob.free) == 16 and all(u == 0 for u in ob.users)

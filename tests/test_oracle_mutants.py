@@ -128,3 +128,78 @@ def test_planted_mistake_fails_a_pin(source, tmp_path, name, subs):
     _build(text, path)
     failed = _run_pins(path)
     assert failed, f"no pin caught the planted mistake: {name}"
+
+
+# ---- the block manager's oracle (oracle/block_manager.py): same idea, Python source ------------
+
+import importlib.util  # noqa: E402
+
+import test_block_manager  # noqa: E402
+from oracle import block_manager as oracle_bm  # noqa: E402
+
+BM_MUTANTS = [
+    ("copy-on-write skipped", [('elif self.users[rec["table"][-1]] > 1:', "elif False:", 1)]),
+    ("copy reported the wrong way", [("copies.append((src, dst))", "copies.append((dst, src))", 1)]),
+    ("fork does not count its references",
+     [('for b in par["table"]:\n            self.users[b] += 1', 'for b in par["table"]:\n            pass', 1)]),
+    ("can_append ignores the copy", [("need += 1", "need += 0", 1)]),
+    ("hash chain broken", [('head = b"" if previous is None else struct.pack("<Q", previous & _M)',
+                            'head = b""', 1)]),
+    ("shared prompt blocks taken fresh", [("if self.users[b] == 0:\n                        self.free.remove(b)\n"
+                                           "                    self.users[b] += 1",
+                                           "if self.users[b] == 0:\n                        self.free.remove(b)\n"
+                                           "                    self.users[b] += 0", 1)]),
+]
+
+
+def _bm_pins():
+    return [fn for name, fn in sorted(vars(test_block_manager).items())
+            if name.startswith("test_oracle_") and callable(fn)]
+
+
+def _run_bm_pins(module):
+    saved = test_block_manager.O
+    test_block_manager.O = module
+    failed = []
+    try:
+        for fn in _bm_pins():
+            marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+            combos = [dict(zip([m.args[0]], [v])) for m in marks for v in m.args[1]] or [{}]
+            for kw in combos:
+                try:
+                    fn(**kw)
+                except Exception as e:
+                    failed.append((fn.__name__, kw, type(e).__name__))
+    finally:
+        test_block_manager.O = saved
+    return failed
+
+
+def _load_bm(text, path):
+    with open(path, "w") as f:
+        f.write(text)
+    spec = importlib.util.spec_from_file_location("bm_mutant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def bm_source():
+    with open(oracle_bm.__file__) as f:
+        return f.read()
+
+
+def test_block_manager_oracle_unmutated_copy_passes_every_pin(bm_source, tmp_path):
+    assert _run_bm_pins(_load_bm(bm_source, str(tmp_path / "bm_clean.py"))) == []
+    assert len(_bm_pins()) >= 4
+
+
+@pytest.mark.parametrize("name,subs", BM_MUTANTS, ids=[m[0] for m in BM_MUTANTS])
+def test_block_manager_oracle_planted_mistake_fails_a_pin(bm_source, tmp_path, name, subs):
+    text = bm_source
+    for old, new, count in subs:
+        assert text.count(old) == count, f"mutation site moved: {old!r}"
+        text = text.replace(old, new)
+    failed = _run_bm_pins(_load_bm(text, str(tmp_path / "bm_mutant.py")))
+    assert failed, f"no pin caught the planted mistake: {name}"
