@@ -23,6 +23,7 @@
  *   pkv_paged_decode_attention_static_ws -- decode with a library-held workspace (no allocation).
  *   pkv_bm_*                           -- host block manager: allocation, refcounted prefix sharing.
  *   pkv_xxh64, pkv_block_hash          -- the chained per-block prefix hash it keys shared blocks by.
+ *   pkv_kv_cache_copy_blocks             -- copy-on-write of blocks shared by forked sequences.
  *   pkv_decode_split_chunk, pkv_decode_workspace_bytes, pkv_decode_workspace_bytes_dtype,
  *   pkv_decode_shared_prefix_workspace_bytes
  *                                      -- the split rule and workspace sizes the calls use.
@@ -323,12 +324,29 @@ pkv_status pkv_paged_decode_attention_static_ws(void* out, const void* q, const 
                                                 int split_chunk_tokens, int32_t* status,
                                                 void* stream);
 
+/*
+ * Copy-on-write of forked sequences ("LLM Primer VI, Chapter 8", section 8.1: sequences share
+ * blocks by reference count; the block manager reports a copy when one of them writes into a
+ * shared, partly filled block). For each pair i of block_pairs ([num_pairs][2] int32, device
+ * memory: source block, destination block), block destination of k_pool and v_pool -- all kv
+ * heads, all 16 slots, [num_kv_heads][16][head_dim] elements of dtype -- and, for PKV_I8 pools,
+ * of k_scales and v_scales ([num_kv_heads][16] fp32) becomes a bit copy of block source. Pairs
+ * must name distinct destinations, none of which is a source of another pair. A pair with an id
+ * outside [0, num_blocks), or source == destination, is skipped and flagged PKV_FLAG_BAD_BLOCK.
+ * Enqueue it before the pkv_kv_cache_write of the step's new tokens, on the same stream.
+ * Pools and scale arrays 16-byte aligned; scale pointers NULL unless dtype is PKV_I8.
+ */
+pkv_status pkv_kv_cache_copy_blocks(void* k_pool, void* v_pool, float* k_scales, float* v_scales,
+                                    const int32_t* block_pairs, int num_pairs, int num_kv_heads,
+                                    int head_dim, int block_size, int num_blocks, pkv_dtype dtype,
+                                    int32_t* status, void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Host block manager: the step before the decode path, producing block_tables, context_lens and
- * slot_mapping. "AMD ATOM inference engine", section 5.1 (BlockManager: fixed 16-token blocks, a
- * block_table per sequence, Block{block_id, ref_count, hash = -1, token_ids}, reset() sets
- * ref_count to 1) and section 5.2 (prefix caching with xxhash64 chained over blocks);
- * "LLM Primer VI, Chapter 8", section 8.1 (blocks shared by reference count).
+ * slot_mapping. "AMD ATOM inference engine", section 5.1 (the KV cache as fixed 16-token blocks, a
+ * block table per sequence, a reference count per block) and section 5.2 (prefix caching with
+ * xxhash64 chained over blocks); "LLM Primer VI, Chapter 8", section 8.1 (blocks shared by
+ * reference count, which makes best-of-n sampling on one prompt nearly free).
  *
  * A pkv_block_manager is host memory owned by the caller (create / destroy); no device memory and
  * no CUDA call is involved, and it is not thread-safe. Sequences are named by caller-chosen int64
@@ -336,7 +354,9 @@ pkv_status pkv_paged_decode_attention_static_ws(void* out, const void* q, const 
  * the back of the free list, tail block first. With prefix caching on, every full block carries
  * the chained hash of its tokens; a prompt block whose hash (and tokens) match a cached block
  * shares it (ref_count + 1) instead of taking a free block, even when that block sits freed but
- * not yet reused in the free list. Partial blocks are never shared.
+ * not yet reused in the free list. The cache never shares partial blocks; a fork shares every
+ * block, and copy-on-write (pkv_bm_append_cow) splits a shared partial tail block when one of its
+ * sequences writes into it.
  * --------------------------------------------------------------------------------------------- */
 typedef struct pkv_block_manager pkv_block_manager;
 
@@ -366,6 +386,21 @@ int pkv_bm_can_append(const pkv_block_manager* bm, int64_t seq_id, int num_new_t
  * for pkv_kv_cache_write. A block that becomes full gets its chained hash. */
 pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int64_t* new_token_ids,
                          int num_new_tokens, int64_t* slot_mapping);
+/* Decode with copy-on-write: as pkv_bm_append, for sequences that may share their tail block
+ * (after pkv_bm_fork). If the tail block is partly filled and another sequence also references it,
+ * the sequence first takes a free block for its own copy and drops its reference to the shared
+ * one; copy_src_dst[0..1] receive (shared block, new block) and *num_copies 1 (else 0). The caller
+ * copies that block on the device (pkv_kv_cache_copy_blocks) before writing the new tokens into
+ * their slots. The last sequence referencing a shared block writes in place. pkv_bm_can_append
+ * counts the copy's block. pkv_bm_append returns PKV_ERR_INVALID_ARG, changing nothing, where a
+ * copy would be needed. */
+pkv_status pkv_bm_append_cow(pkv_block_manager* bm, int64_t seq_id, const int64_t* new_token_ids,
+                             int num_new_tokens, int64_t* slot_mapping, int32_t* copy_src_dst,
+                             int* num_copies);
+/* Parallel sampling (best-of-n): a new sequence child_id with the parent's tokens and block table;
+ * every block gains a reference, none is copied. INVALID_ARG for an unknown parent or a known
+ * child id. */
+pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id);
 /* Finish or preempt a sequence: its blocks lose a reference; unreferenced ones become free. */
 pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
 int pkv_bm_context_len(const pkv_block_manager* bm, int64_t seq_id);  /* -1 if unknown */

@@ -41,6 +41,7 @@ SIGNATURES = {
     "pkv_paged_decode_attention_shared_prefix": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                   _I, _I, _F, _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_decode_shared_prefix_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
+    "pkv_kv_cache_copy_blocks": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
 }
 STATIC_WORKSPACE_BYTES = 32 << 20  # PKV_STATIC_WORKSPACE_BYTES
 
@@ -126,6 +127,17 @@ def kv_cache_write_int8(k_new, v_new, k_pool, v_pool, k_scales, v_scales, slot_m
         _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
         _ptr(slot_mapping), T, Hkv, D, BS, NB, _kv_code(k_new), _ptr(status), _stream(stream))
     _check(rc, "kv_cache_write_int8")
+
+
+def kv_cache_copy_blocks(k_pool, v_pool, block_pairs, k_scales=None, v_scales=None, status=None,
+                         stream=None):
+    """pkv_kv_cache_copy_blocks: block_pairs is an int32 CUDA tensor [n, 2] of (src, dst)."""
+    NB, Hkv, BS, D = k_pool.shape
+    n = int(block_pairs.shape[0]) if block_pairs is not None else 0
+    rc = load().pkv_kv_cache_copy_blocks(
+        _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales), _ptr(block_pairs), n, Hkv, D,
+        BS, NB, _kv_code(k_pool), _ptr(status), _stream(stream))
+    _check(rc, "kv_cache_copy_blocks")
 
 
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
@@ -264,6 +276,8 @@ _BM_SIGNATURES = {
     "pkv_bm_allocate": ([_P, ctypes.c_int64, _P, _I, _P], _I),
     "pkv_bm_can_append": ([_P, ctypes.c_int64, _I], _I),
     "pkv_bm_append": ([_P, ctypes.c_int64, _P, _I, _P], _I),
+    "pkv_bm_append_cow": ([_P, ctypes.c_int64, _P, _I, _P, _P, _P], _I),
+    "pkv_bm_fork": ([_P, ctypes.c_int64, ctypes.c_int64], _I),
     "pkv_bm_free": ([_P, ctypes.c_int64], _I),
     "pkv_bm_context_len": ([_P, ctypes.c_int64], _I),
     "pkv_bm_batch_tables": ([_P, _P, _I, _I, _P, _P], _I),
@@ -336,6 +350,21 @@ class BlockManager:
         _check(load().pkv_bm_append(self._h, seq_id, _np_ptr(t), t.size, _np_ptr(slots)),
                "pkv_bm_append")
         return slots
+
+    def append_cow(self, seq_id: int, token_ids):
+        """Append with copy-on-write: (slots, copies) where copies is a list of (src, dst) block
+        pairs to copy on the device (pkv_kv_cache_copy_blocks) before writing the slots."""
+        import numpy as np
+        t = np.ascontiguousarray(token_ids, dtype=np.int64)
+        slots = np.zeros(t.size, dtype=np.int64)
+        pair = np.zeros(2, dtype=np.int32)
+        n = ctypes.c_int(0)
+        _check(load().pkv_bm_append_cow(self._h, seq_id, _np_ptr(t), t.size, _np_ptr(slots),
+                                        _np_ptr(pair), ctypes.byref(n)), "pkv_bm_append_cow")
+        return slots, [(int(pair[0]), int(pair[1]))] * n.value
+
+    def fork(self, parent_id: int, child_id: int):
+        _check(load().pkv_bm_fork(self._h, parent_id, child_id), "pkv_bm_fork")
 
     def free(self, seq_id: int):
         _check(load().pkv_bm_free(self._h, seq_id), "pkv_bm_free")

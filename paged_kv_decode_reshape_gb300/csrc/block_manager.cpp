@@ -125,7 +125,7 @@ struct pkv_block_manager {
             auto it = cached.find(blk.hash);
             if (it != cached.end() && it->second == id) cached.erase(it);
         }
-        blk.ref_count = 1;  // Block.reset()
+        blk.ref_count = 1;  // one user, nothing cached
         blk.has_hash = false;
         blk.token_ids.clear();
         return id;
@@ -224,23 +224,45 @@ pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq_id, const int64_t*
     return PKV_OK;
 }
 
+// Blocks an append of k tokens takes: those past the table's end, plus one when the tail block is
+// partly filled and also referenced by another sequence (a fork), which is copied first.
+static long long blocks_for_append(const pkv_block_manager* bm, const Sequence& s, int k) {
+    const long long n = (long long)s.tokens.size();
+    long long need = (n + k + bm->block_size - 1) / bm->block_size - (long long)s.table.size();
+    if (k > 0 && n % bm->block_size != 0 && bm->blocks[s.table.back()].ref_count > 1) need += 1;
+    return need;
+}
+
 int pkv_bm_can_append(const pkv_block_manager* bm, int64_t seq_id, int num_new_tokens) {
     if (!bm || num_new_tokens < 0) return 0;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return 0;
-    const long long n = (long long)it->second.tokens.size() + num_new_tokens;
-    const long long need = (n + bm->block_size - 1) / bm->block_size - (long long)it->second.table.size();
+    const long long need = blocks_for_append(bm, it->second, num_new_tokens);
     return need <= 0 || (long long)bm->free_ids.size() >= need;
 }
 
-pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int64_t* new_token_ids,
-                         int num_new_tokens, int64_t* slot_mapping) {
+pkv_status pkv_bm_append_cow(pkv_block_manager* bm, int64_t seq_id, const int64_t* new_token_ids,
+                             int num_new_tokens, int64_t* slot_mapping, int32_t* copy_src_dst,
+                             int* num_copies) {
+    if (num_copies) *num_copies = 0;
     if (!bm || num_new_tokens < 0 || (num_new_tokens > 0 && !new_token_ids)) return PKV_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
-    if (!pkv_bm_can_append(bm, seq_id, num_new_tokens)) return PKV_ERR_NO_BLOCKS;
     Sequence& s = it->second;
     const int bs = bm->block_size;
+    // a shared, partly filled tail block must be copied before the first new token lands in it
+    const bool cow = num_new_tokens > 0 && s.tokens.size() % bs != 0 && bm->blocks[s.table.back()].ref_count > 1;
+    if (cow && (!copy_src_dst || !num_copies)) return PKV_ERR_INVALID_ARG;
+    if (!pkv_bm_can_append(bm, seq_id, num_new_tokens)) return PKV_ERR_NO_BLOCKS;
+    if (cow) {
+        const int32_t src = s.table.back();
+        const int32_t dst = bm->take_free_block();
+        bm->blocks[src].ref_count -= 1;  // still >= 1: another sequence keeps it
+        s.table.back() = dst;
+        copy_src_dst[0] = src;
+        copy_src_dst[1] = dst;
+        *num_copies = 1;
+    }
     for (int k = 0; k < num_new_tokens; ++k) {
         const size_t pos = s.tokens.size();
         if (pos % bs == 0) s.table.push_back(bm->take_free_block());
@@ -249,6 +271,21 @@ pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int64_t* n
         s.tokens.push_back(new_token_ids[k]);
         if (pos % bs == (size_t)bs - 1) bm->seal(s, id, s.tokens.data() + (pos + 1 - bs));
     }
+    return PKV_OK;
+}
+
+pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int64_t* new_token_ids,
+                         int num_new_tokens, int64_t* slot_mapping) {
+    return pkv_bm_append_cow(bm, seq_id, new_token_ids, num_new_tokens, slot_mapping, nullptr, nullptr);
+}
+
+pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id) {
+    if (!bm || parent_id == child_id || bm->seqs.count(child_id)) return PKV_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(parent_id);
+    if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
+    Sequence child = it->second;  // same table, tokens and hash-chain link
+    for (int32_t id : child.table) bm->blocks[id].ref_count += 1;
+    bm->seqs.emplace(child_id, std::move(child));
     return PKV_OK;
 }
 

@@ -102,6 +102,33 @@ __global__ void __launch_bounds__(256) kv_write_quant_kernel(const QuantWritePar
     }
 }
 
+// Copy-on-write of forked sequences ("LLM Primer VI, Chapter 8", section 8.1: blocks shared by
+// reference count): for each (src, dst) pair, block dst of the K pool, the V pool and -- INT8
+// pools -- both scale arrays becomes a copy of block src. A block of one array is contiguous
+// ([Hkv][16][D] elements, or [Hkv][16] scales), so the copy is a flat run of 16-byte vectors:
+// one thread per vector, grid-stride, each pair's ids validated before use.
+__global__ void __launch_bounds__(256) kv_copy_blocks_kernel(const CopyBlocksParams p) {
+    grid_dependency_wait();    // the pairs, and the pools' last writes, may come from the kernel before
+    grid_dependents_launch();  // the write that follows waits for this grid to complete
+    long long per_pair = 0;
+    for (int a = 0; a < 4; ++a) per_pair += p.vec_per_block[a];
+    const long long total = (long long)p.num_pairs * per_pair;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int pair = (int)(idx / per_pair);
+        long long v = idx - (long long)pair * per_pair;
+        int a = 0;
+        while (v >= p.vec_per_block[a]) v -= p.vec_per_block[a++];
+        const int src = p.pairs[2 * pair], dst = p.pairs[2 * pair + 1];
+        if (src < 0 || src >= p.NB || dst < 0 || dst >= p.NB || src == dst) {
+            if (v == 0 && a == 0) flag(p.status, PKV_FLAG_BAD_BLOCK);
+            continue;
+        }
+        uint4* base = static_cast<uint4*>(p.arrays[a]);
+        base[(long long)dst * p.vec_per_block[a] + v] = base[(long long)src * p.vec_per_block[a] + v];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_kv_write_quant(const QuantWriteParams& p, pkv_dtype src, int D, cudaStream_t s) {
@@ -123,6 +150,20 @@ cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s) {
     long long blocks = (total + 255) / 256;
     if (blocks > 152 * 32) blocks = 152 * 32;  // grid-stride beyond 32 CTAs per SM
     return launch_pdl(kv_write_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
+}
+
+}  // namespace pkv
+
+namespace pkv {
+
+cudaError_t launch_kv_copy_blocks(const CopyBlocksParams& p, cudaStream_t s) {
+    long long per_pair = 0;
+    for (int a = 0; a < 4; ++a) per_pair += p.vec_per_block[a];
+    const long long total = (long long)p.num_pairs * per_pair;
+    if (total == 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    return launch_pdl(kv_copy_blocks_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
 }
 
 }  // namespace pkv

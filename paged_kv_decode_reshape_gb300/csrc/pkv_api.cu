@@ -315,6 +315,32 @@ pkv_status pkv_kv_cache_write_int8(const void* k_new, const void* v_new, int8_t*
                : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_kv_cache_copy_blocks(void* k_pool, void* v_pool, float* k_scales, float* v_scales,
+                                    const int32_t* block_pairs, int num_pairs, int num_kv_heads,
+                                    int head_dim, int block_size, int num_blocks, pkv_dtype dtype,
+                                    int32_t* status, void* stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_I8) return PKV_ERR_INVALID_ARG;
+    if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+    const bool i8 = dtype == PKV_I8;
+    if (i8 ? !(k_scales && v_scales) : (k_scales || v_scales)) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !block_pairs) return PKV_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)k_pool, (const void*)v_pool, (const void*)k_scales,
+                            (const void*)v_scales})
+        if (ptr && !aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(block_pairs, 4)) return PKV_ERR_INVALID_ARG;
+    const size_t blk = (size_t)num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype);
+    const size_t sblk = (size_t)num_kv_heads * kBlockSize * 4;
+    if (overlap(k_pool, blk * num_blocks, v_pool, blk * num_blocks)) return PKV_ERR_INVALID_ARG;
+    CopyBlocksParams p{};
+    p.arrays[0] = k_pool; p.arrays[1] = v_pool; p.arrays[2] = k_scales; p.arrays[3] = v_scales;
+    p.vec_per_block[0] = p.vec_per_block[1] = (long long)(blk / 16);
+    p.vec_per_block[2] = p.vec_per_block[3] = i8 ? (long long)(sblk / 16) : 0;
+    p.pairs = block_pairs; p.status = status; p.num_pairs = num_pairs; p.NB = num_blocks;
+    return launch_kv_copy_blocks(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
                            int split_chunk_tokens, pkv_dtype kv_dtype) {
     if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||

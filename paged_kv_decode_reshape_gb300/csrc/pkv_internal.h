@@ -118,6 +118,14 @@ cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t sm
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+struct CopyBlocksParams {
+    void* arrays[4];              // K pool, V pool, K scales, V scales (unused ones: 0 vectors)
+    long long vec_per_block[4];   // 16-byte vectors one block occupies in each array
+    const int32_t* pairs;         // [num_pairs][2]: source block, destination block
+    int32_t* status;
+    int num_pairs, NB;
+};
+
 struct QuantWriteParams {
     const void* k_new;          // [T][Hkv][D] fp32 or bf16
     const void* v_new;
@@ -159,6 +167,7 @@ struct PrefixParams {
 // Launchers (return the launch's error code).
 cudaError_t launch_kv_write(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_kv_write_quant(const QuantWriteParams& p, pkv_dtype src, int D, cudaStream_t s);
+cudaError_t launch_kv_copy_blocks(const CopyBlocksParams& p, cudaStream_t s);
 cudaError_t launch_split_f32(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_split_bf16(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);
 cudaError_t launch_split_i8(const SplitParams& p, int D, int heads_per_cta, cudaStream_t s);

@@ -103,19 +103,24 @@ def _compare(bm, ob, live):
         assert np.array_equal(a, b) and np.array_equal(ca, cb)
     for i in range(len(ob.users)):
         assert bm.ref_count(i) == ob.ref_count(i)
+    for s in live:
+        assert bm.context_len(s) == len(ob.seqs[s]["tokens"])
 
 
-@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
 @pytest.mark.parametrize("prefix_cache", [True, False])
 def test_manager_matches_oracle_on_random_scripts(pkv, seed, prefix_cache):
+    """Random allocate / fork / append / free scripts: the native manager's answers (cache hits,
+    slots, copy-on-write copies, errors) and state (tables, lengths, reference counts, free
+    count) equal the oracle's after every operation."""
     rng = np.random.default_rng(seed)
     NB = 300
     bm, ob = P.BlockManager(NB, 16, prefix_cache), O.BlockManager(NB, 16, prefix_cache)
     system = rng.integers(0, 1000, 64)  # shared prompt prefixes of 0..4 blocks
-    live, next_id = [], 0
-    for _ in range(250):
+    live, next_id, copies_seen = [], 0, 0
+    for _ in range(300):
         op = rng.random()
-        if op < 0.35 or not live:
+        if op < 0.3 or not live:
             n = int(rng.integers(1, 120))
             pre = int(rng.integers(0, 5)) * 16
             toks = np.concatenate([system[:pre], rng.integers(0, 1000, n)])
@@ -128,20 +133,84 @@ def test_manager_matches_oracle_on_random_scripts(pkv, seed, prefix_cache):
                 with pytest.raises(P.PkvError):
                     bm.allocate(next_id, toks)
             next_id += 1
-        elif op < 0.8:
+        elif op < 0.4:
+            parent = live[int(rng.integers(len(live)))]
+            bm.fork(parent, next_id)
+            ob.fork(parent, next_id)
+            live.append(next_id)
+            next_id += 1
+        elif op < 0.85:
             sid = live[int(rng.integers(len(live)))]
             k = int(rng.integers(1, 20))
             toks = rng.integers(0, 1000, k)
             ok = ob.can_append(sid, k)
             assert bm.can_append(sid, k) == ok
             if ok:
-                assert np.array_equal(bm.append(sid, toks), ob.append(sid, toks)[0])
+                slots, copies = bm.append_cow(sid, toks)
+                oslots, ocopies = ob.append(sid, toks)
+                assert np.array_equal(slots, oslots) and copies == ocopies
+                copies_seen += len(copies)
                 assert bm.context_len(sid) == len(ob.seqs[sid]["tokens"])
         else:
             sid = live.pop(int(rng.integers(len(live))))
             bm.free(sid)
             ob.free_seq(sid)
         _compare(bm, ob, live)
+    assert copies_seen > 0  # the scripts do reach copy-on-write
+
+
+def test_best_of_8_by_fork_through_the_manager(pkv):
+    """Chapter 8 primer, section 8.1, through pkv_bm_*: one 2,000-token prompt, seven forks, 100
+    new tokens per sample -> 2,800 token slots (16,800 unshared), the prompt's 125 blocks shared
+    by all eight, each sample with 7 blocks of its own; with a 2,001-token prompt the shared tail
+    block is copied for all but the last sample to write into it."""
+    g = _read_gold("best_of_8_token_slots.txt")
+    n, prompt, new = g["samples"], g["prompt_tokens"], g["new_tokens_per_sample"]
+    for plen in (prompt, prompt + 1):
+        bm = P.BlockManager(4096, 16)
+        toks = np.random.default_rng(plen).integers(0, 32000, plen)
+        assert bm.allocate(0, toks) == 0
+        for c in range(1, n):
+            bm.fork(0, c)
+        slots, copies = set(), []
+        for s in range(n):
+            sl, cp = bm.append_cow(s, np.full(new, 7 + s))
+            copies += cp
+        for s in range(n):
+            bt, cl = bm.batch_tables([s], 140)
+            assert cl[0] == plen + new
+            slots |= {int(bt[0, t // 16]) * 16 + t % 16 for t in range(plen + new)}
+        # each copy holds its own duplicate of the prompt tokens in the shared tail block
+        assert len(slots) == plen + n * new + (n - 1) * (plen % 16)
+        if plen == prompt:
+            assert len(slots) == g["slots_with_sharing"] and copies == []
+            assert 4096 - bm.num_free_blocks == prompt // 16 + n * -(-new // 16)
+        else:
+            assert len(copies) == n - 1 and len({src for src, _ in copies}) == 1
+        bt, _ = bm.batch_tables(list(range(n)), 140)
+        assert (bt[:, :prompt // 16] == bt[0, :prompt // 16]).all()
+        assert all(bm.ref_count(int(b)) == n for b in bt[0, :prompt // 16])
+        for s in range(n):
+            bm.free(s)
+        assert bm.num_free_blocks == 4096
+
+
+def test_fork_errors_and_append_without_copy_output(pkv):
+    bm = P.BlockManager(8, 16)
+    bm.allocate(1, np.arange(20))          # tail block holds 4 tokens
+    with pytest.raises(P.PkvError):
+        bm.fork(9, 2)                       # unknown parent
+    bm.fork(1, 2)
+    with pytest.raises(P.PkvError):
+        bm.fork(1, 2)                       # known child id
+    free = bm.num_free_blocks
+    with pytest.raises(P.PkvError) as e:    # a copy is needed but the plain append cannot report it
+        bm.append(2, [5])
+    assert e.value.status == P.ERR_INVALID_ARG
+    assert bm.num_free_blocks == free and bm.context_len(2) == 20
+    slots, copies = bm.append_cow(2, [5])
+    assert len(copies) == 1 and bm.num_free_blocks == free - 1
+    assert bm.append(1, [6]).tolist() == [copies[0][0] * 16 + 4]  # the last user writes in place
 
 
 def test_exhaustion_and_errors_change_nothing(pkv):
