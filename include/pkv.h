@@ -240,7 +240,9 @@ size_t pkv_decode_workspace_bytes_dtype(int num_seqs, int num_q_heads, int num_k
  * max_context_len / (2 * U), where U is the number of (sequence, kv head, split) units the kernel
  * that serves the call does best with on a GB300 (152 SMs): 1024 for the bf16 head_dim-128
  * tensor-core kernel, 4096 for the INT8 one and for the CUDA-core kernel (fp32, head_dim 64).
- * The chunk then grows until the split extent max(1, max_context_len / chunk) is at most 8192.
+ * The INT8 head_dim-128 kernel then takes at least 512 and doubles the chunk while the longest
+ * sequence would get more than 32 splits. The chunk then grows until the split extent
+ * max(1, max_context_len / chunk) is at most 8192.
  * Pure host arithmetic. */
 int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
                            int split_chunk_tokens, pkv_dtype kv_dtype);

@@ -68,6 +68,13 @@ constexpr int kMmaHeads = 8;        // MMA N: query heads per CTA
 #ifndef PKV_MMA_PROXY_FENCE
 #define PKV_MMA_PROXY_FENCE 1
 #endif
+#ifndef PKV_MMA_MINB_I8  // minimum resident CTAs per SM the INT8 kernel is compiled for (0: no bound)
+#define PKV_MMA_MINB_I8 0
+#endif
+#ifndef PKV_MMA_UNROLL_I8  // INT8 blocks per trip of the block loop
+#define PKV_MMA_UNROLL_I8 1
+#endif
+constexpr int kUnrollI8 = PKV_MMA_UNROLL_I8;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 
 template <bool kI8, int kNT = 1>
@@ -153,7 +160,12 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // kNT: 8-column MMA n-tiles per CTA. With 2, a warp reads and widens each K/V tile once for 16
 // columns (G = 16, or multi-token rows of G = 8).
 template <bool kI8, bool kPacked, int kNT>
-__global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(const SplitParams p,
+#if PKV_MMA_MINB_I8 > 0
+#define PKV_MMA_BOUNDS __launch_bounds__(MmaGeom<kI8, kNT>::THREADS, kI8 ? PKV_MMA_MINB_I8 : 1)
+#else
+#define PKV_MMA_BOUNDS __launch_bounds__(MmaGeom<kI8, kNT>::THREADS)
+#endif
+__global__ void PKV_MMA_BOUNDS mma_split_kernel(const SplitParams p,
                                                                const __grid_constant__ CUtensorMap tmk,
                                                                const __grid_constant__ CUtensorMap tmv) {
     using G = MmaGeom<kI8, kNT>;
@@ -386,7 +398,7 @@ __global__ void __launch_bounds__(MmaGeom<kI8, kNT>::THREADS) mma_split_kernel(c
         // bf16: two blocks per trip, so stage indices and parities are compile-time (measured: the
         // Llama-3-8B GQA batch 100.1 -> 98.4 us); INT8 stays at one, where the extra registers
         // would cost a CTA per SM
-#pragma unroll(kI8 ? 1 : 2)
+#pragma unroll(kI8 ? kUnrollI8 : 2)
         for (int k = 0; k < nmine; ++k) {
             const int j = warp + k * NC;
             const int st = warp + (k % SPW) * NC;

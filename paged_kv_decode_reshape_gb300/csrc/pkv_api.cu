@@ -24,10 +24,6 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 size_t elem_bytes(pkv_dtype t) { return t == PKV_F32 ? 4 : t == PKV_BF16 ? 2 : t == PKV_I8 ? 1 : 0; }
 
-// Tokens per split before block rounding: the request, or in auto mode the power of two in
-// [kMinAutoChunk, kMaxAutoChunk] nearest below (work units of the batch) / kTargetUnits, so that
-// a batch yields about kTargetUnits units for the GPU's SMs to share; doubled further while the
-// split extent exceeds what the merge kernel supports.
 // the tensor-core kernel serves head_dim 128 with bf16 or INT8 pools; the CUDA-core kernel the rest
 bool uses_mma(int head_dim, pkv_dtype kv_dtype) {
     return head_dim == 128 && (kv_dtype == PKV_BF16 || kv_dtype == PKV_I8);
@@ -37,12 +33,37 @@ long long target_units(int head_dim, pkv_dtype kv_dtype) {
     return uses_mma(head_dim, kv_dtype) && kv_dtype == PKV_BF16 ? kTargetUnitsBf16Mma : kTargetUnits;
 }
 
-int choose_chunk(int num_seqs, int num_kv_heads, int max_context_len, int requested, long long target) {
+// Tokens per split before block rounding: the request, or in auto mode the power of two in
+// [kMinAutoChunk, kMaxAutoChunk] nearest below (work units of the batch) / (target units of the
+// kernel), so that a batch yields about that many (row, kv head, split) units for the GPU's SMs to
+// share. The INT8 tensor-core kernel, whose units each pay a start-up of a few microseconds
+// against a slower per-byte rate, also keeps at least kMinChunkI8Mma tokens per split and at most
+// kMaxSplitsI8Mma splits for the longest sequence (measured on GB300: a 64-sequence, 512-4096
+// token batch runs 16 % faster at chunk 512 than 256, a 131k-context batch 8 % faster at 4096
+// than 1024). Doubled further while the split extent exceeds what the merge kernel supports.
+int choose_chunk(int num_seqs, int num_kv_heads, int max_context_len, int requested, int head_dim,
+                 pkv_dtype kv_dtype) {
     if (requested > 0) return requested;
+    const long long target = target_units(head_dim, kv_dtype);
     const long long tokens = (long long)num_seqs * num_kv_heads * max_context_len;
     int c = kMinAutoChunk;
     while (c < kMaxAutoChunk && tokens / (2LL * c) >= target) c *= 2;
+    if (uses_mma(head_dim, kv_dtype) && kv_dtype == PKV_I8) {
+        if (c < kMinChunkI8Mma) c = kMinChunkI8Mma;
+        while (c < kMaxAutoChunk && max_context_len / c > kMaxSplitsI8Mma) c *= 2;
+    }
     while (max_context_len / c > kMaxSplits) c *= 2;
+    return c;
+}
+
+// The smallest auto chunk any K/V dtype gets for this shape (the most splits): what a workspace
+// sized without knowing the dtype must cover.
+int min_chunk_any_dtype(int num_seqs, int num_kv_heads, int max_context_len, int requested, int head_dim) {
+    int c = choose_chunk(num_seqs, num_kv_heads, max_context_len, requested, head_dim, PKV_F32);
+    for (pkv_dtype t : {PKV_BF16, PKV_I8}) {
+        const int x = choose_chunk(num_seqs, num_kv_heads, max_context_len, requested, head_dim, t);
+        c = x < c ? x : c;
+    }
     return c;
 }
 
@@ -147,7 +168,7 @@ pkv_status run_decode(const Decode& a) {
         if (prefix % kBlockSize || prefix > a.max_ctx) return PKV_ERR_INVALID_ARG;
     }
     const int suffix_max = a.max_ctx - prefix;
-    const int chunk = choose_chunk(rows, a.Hkv, suffix_max, a.chunk_req, target_units(a.D, a.kv_dtype));
+    const int chunk = choose_chunk(rows, a.Hkv, suffix_max, a.chunk_req, a.D, a.kv_dtype);
     const int S = split_extent(suffix_max, chunk);
     if (S > kMaxSplits) return PKV_ERR_UNSUPPORTED;
     int P = 0, split_tokens = 0;
@@ -347,8 +368,7 @@ int pkv_decode_split_chunk(int num_seqs, int num_kv_heads, int head_dim, int max
         split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize ||
         (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8))
         return 0;
-    return choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens,
-                        target_units(head_dim, kv_dtype));
+    return choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens, head_dim, kv_dtype);
 }
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -356,8 +376,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_context_len < 0 || split_chunk_tokens < 0 || split_chunk_tokens % kBlockSize)
         return 0;
-    // the largest target (smallest chunk, most splits) of any K/V dtype: an upper bound for all
-    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens, kTargetUnits);
+    // the smallest chunk (most splits) of any K/V dtype: an upper bound for all
+    const int chunk = min_chunk_any_dtype(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens, head_dim);
     return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
 }
 
@@ -369,8 +389,8 @@ size_t pkv_decode_workspace_bytes_dtype(int num_seqs, int num_q_heads, int num_k
         (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8))
         return 0;
     // the chunk run_decode picks for this shape and K/V dtype, hence its exact split extent
-    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens,
-                                   target_units(head_dim, kv_dtype));
+    const int chunk = choose_chunk(num_seqs, num_kv_heads, max_context_len, split_chunk_tokens, head_dim,
+                                   kv_dtype);
     return workspace_bytes_for(num_seqs, num_q_heads, head_dim, split_extent(max_context_len, chunk));
 }
 
@@ -479,8 +499,7 @@ size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, i
         shared_prefix_tokens % kBlockSize || shared_prefix_tokens > max_context_len)
         return 0;
     const int suffix_max = max_context_len - shared_prefix_tokens;
-    const int chunk = choose_chunk(num_seqs, num_kv_heads, suffix_max, split_chunk_tokens,
-                                   target_units(head_dim, PKV_BF16));
+    const int chunk = choose_chunk(num_seqs, num_kv_heads, suffix_max, split_chunk_tokens, head_dim, PKV_BF16);
     const int S = split_extent(suffix_max, chunk);
     int P = 0, split_tokens = 0;
     prefix_splits(num_seqs, num_q_heads / num_kv_heads, num_kv_heads, shared_prefix_tokens, &P,

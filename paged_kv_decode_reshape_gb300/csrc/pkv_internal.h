@@ -21,6 +21,8 @@ constexpr int kMaxAutoChunk = 4096;
 // the INT8 one keeps 5 per SM and, doing more arithmetic per byte, does best with more of them.
 constexpr long long kTargetUnitsBf16Mma = 1024;
 constexpr long long kTargetUnits = 4096;  // INT8 tensor-core and CUDA-core kernels
+constexpr int kMinChunkI8Mma = 512;       // INT8 tensor-core kernel: auto chunk at least this,
+constexpr int kMaxSplitsI8Mma = 32;       // and at most this many splits for the longest sequence
 
 // Split rule ("EchoLLMServing inference framework notes", section 2, FlashDecoding):
 // split_num = max(1, n // chunk), capped at max_splits; each split is a whole number of

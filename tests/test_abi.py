@@ -53,9 +53,11 @@ def test_status_strings(pkv):
 
 def test_workspace_arithmetic(pkv):
     L = P.load()
-    # 8 seqs x 32 q / 8 kv heads, 131072 tokens: the workspace bound takes the INT8 auto chunk,
-    # 2048 -> 64 splits x (128 acc + m + l)
-    assert L.pkv_decode_split_chunk(8, 8, 128, 131072, 0, P.I8) == 2048
+    # 8 seqs x 32 q / 8 kv heads, 131072 tokens: the workspace bound takes the smallest auto chunk
+    # of any dtype (fp32's, 2048) -> 64 splits x (128 acc + m + l); the INT8 kernel keeps the
+    # longest sequence at <= 32 splits (chunk 4096)
+    assert L.pkv_decode_split_chunk(8, 8, 128, 131072, 0, P.I8) == 4096
+    assert L.pkv_decode_split_chunk(8, 8, 128, 131072, 0, P.F32) == 2048
     assert L.pkv_decode_split_chunk(8, 8, 128, 131072, 0, P.BF16) == 4096
     assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 0) == 8 * 32 * 64 * 130 * 4
     assert L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 1024) == 8 * 32 * 128 * 130 * 4
@@ -67,6 +69,8 @@ def test_workspace_arithmetic(pkv):
     assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, BF) == 1024     # Llama-3-8B GQA batch
     assert L.pkv_decode_split_chunk(8, 8, 128, 130882, 0, BF) == 4096    # 131k-context batch
     assert L.pkv_decode_split_chunk(128, 8, 128, 8083, 0, I8) == 1024    # INT8 batch
+    assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, I8) == 512      # INT8: at least 512
+    assert L.pkv_decode_split_chunk(512, 8, 128, 8083, 0, I8) == 4096    # 128 seqs x 4 tokens
     assert L.pkv_decode_split_chunk(256, 8, 128, 4090, 0, BF) == 4096    # shared-prefix batch
     assert L.pkv_decode_split_chunk(64, 8, 64, 4055, 0, BF) == 256       # head_dim 64: CUDA cores
     assert L.pkv_decode_split_chunk(64, 8, 128, 4055, 0, F32) == 256     # fp32: CUDA cores
@@ -93,7 +97,8 @@ def test_workspace_arithmetic(pkv):
     WB = L.pkv_decode_workspace_bytes_dtype
     assert WB(64, 32, 8, 128, 4055, 0, BF) == 64 * 32 * (4055 // 1024) * 130 * 4
     assert WB(8, 32, 8, 128, 131072, 0, BF) == 8 * 32 * 32 * 130 * 4           # chunk 4096
-    assert WB(8, 32, 8, 128, 131072, 0, I8) == L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 0)
+    assert WB(8, 32, 8, 128, 131072, 0, I8) == 8 * 32 * 32 * 130 * 4         # chunk 4096
+    assert WB(8, 32, 8, 128, 131072, 0, F32) == L.pkv_decode_workspace_bytes(8, 32, 8, 128, 131072, 0)
     assert WB(128, 64, 8, 128, 8083, 0, I8) == 128 * 64 * (8083 // 1024) * 130 * 4
     assert WB(64, 32, 8, 64, 4055, 0, BF) == 64 * 32 * (4055 // 256) * 66 * 4   # CUDA-core kernel
     assert WB(8, 32, 8, 128, 131072, 1024, BF) == 8 * 32 * 128 * 130 * 4        # forced chunk
