@@ -37,7 +37,7 @@ def lib():
         L.orc_paged_decode_attention_multi.argtypes = [P, P, I, P, P, I, P, P, P, P,
                                                        I, I, I, I, I, I, I, I, D]
         L.orc_paged_decode_attention_multi.restype = I
-        L.orc_paged_prefill_attention.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, D]
+        L.orc_paged_prefill_attention.argtypes = [P, P, I, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, D]
         L.orc_paged_prefill_attention.restype = I
         L.orc_paged_decode_partials.argtypes = [P, P, P, P, P, I, P, P, I, P, P, P, P,
                                                 I, I, I, I, I, I, I, D, I, I]
@@ -198,20 +198,23 @@ def paged_decode_attention_multi(q, k_pool, v_pool, block_tables, context_lens, 
     return out
 
 
-def paged_prefill_attention(q, k_pool, v_pool, block_tables, context_lens, query_start, scale):
+def paged_prefill_attention(q, k_pool, v_pool, block_tables, context_lens, query_start, scale,
+                            k_scales=None, v_scales=None):
     """Paged (chunked) prefill: q [total, Hq, D]; sequence b owns rows query_start[b] ..
-    query_start[b + 1] - 1, its last L_b context tokens, attending causally. fp64 [total, Hq, D]."""
+    query_start[b + 1] - 1, its last L_b context tokens, attending causally. INT8 pools come with
+    their per-token scales [NB, Hkv, BS]. fp64 [total, Hq, D]."""
     q = np.ascontiguousarray(q)
     kp, vp = np.ascontiguousarray(k_pool), np.ascontiguousarray(v_pool)
     bt = _c(block_tables, np.int32)
     cl = _c(context_lens, np.int32)
     qs = _c(query_start, np.int32)
+    ks, vs = _c(k_scales, np.float32), _c(v_scales, np.float32)
     T, Hq, D = q.shape
     NB, Hkv, BS, _ = kp.shape
     out = np.zeros((T, Hq, D), dtype=np.float64)
     rc = lib().orc_paged_prefill_attention(
-        _ptr(out), _ptr(q), _code(q), _ptr(kp), _ptr(vp), _code(kp), _ptr(bt), _ptr(cl), _ptr(qs),
-        cl.shape[0], Hq, Hkv, D, BS, NB, bt.shape[1], float(scale))
+        _ptr(out), _ptr(q), _code(q), _ptr(kp), _ptr(vp), _code(kp), _ptr(ks), _ptr(vs), _ptr(bt),
+        _ptr(cl), _ptr(qs), cl.shape[0], Hq, Hkv, D, BS, NB, bt.shape[1], float(scale))
     _check(rc)
     return out
 

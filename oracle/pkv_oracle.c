@@ -377,14 +377,14 @@ int orc_paged_decode_attention_multi(double* out, const void* q, int q_dtype, co
  * rows query_start[b] .. of q / out [total][Hq][D]. Row i of sequence b attends causally to the
  * first n_b - (L_b - 1 - i) tokens -- the multi-token rule with a per-sequence L. */
 int orc_paged_prefill_attention(double* out, const void* q, int q_dtype, const void* k_pool,
-                                const void* v_pool, int kv_dtype, const int32_t* block_tables,
+                                const void* v_pool, int kv_dtype, const float* k_scales,
+                                const float* v_scales, const int32_t* block_tables,
                                 const int32_t* context_lens, const int32_t* query_start, int B,
                                 int Hq, int Hkv, int D, int BS, int NB, int MBPS, double scale) {
-    orc_problem P = {q, q_dtype, k_pool, v_pool, kv_dtype, NULL, NULL,
+    orc_problem P = {q, q_dtype, k_pool, v_pool, kv_dtype, k_scales, v_scales,
                      block_tables, context_lens, B, Hq, Hkv, D, BS, NB, MBPS, scale};
     int rc = check_problem(&P);
     if (rc) return rc;
-    if (kv_dtype == ORC_I8) return ORC_BAD_ARG;
     int maxn = 1;
     for (int b = 0; b < B; ++b) {
         int L = query_start[b + 1] - query_start[b];

@@ -450,3 +450,57 @@ def test_prefill_matches_library_causal_attention(orc):
             torch.from_numpy(V).repeat_interleave(2, 0), is_causal=True, scale=w.scale)
         np.testing.assert_allclose(out[w.query_start[b]:w.query_start[b + 1]],
                                    ref.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)
+
+
+def _int8_prefill_with_pow2_scales(seed, query_lens, cached_lens, Hq=4, Hkv=2, D=64):
+    """An INT8 prefill whose scales are powers of two that differ per block, kv head, token and
+    between K and V, so code * scale is exact in fp32."""
+    w = W.make_prefill(name="p8", query_lens=query_lens, cached_lens=cached_lens, Hq=Hq, Hkv=Hkv,
+                       D=D, seed=seed, kv_dtype="i8")
+    idx = np.arange(w.k_scales.size).reshape(w.k_scales.shape)
+    ks = np.ldexp(np.float32(1.0), -(3 + idx % 5)).astype(np.float32)
+    vs = np.ldexp(np.float32(1.0), -(2 + (idx * 3) % 7)).astype(np.float32)
+    return w, ks, vs
+
+
+def test_prefill_int8_is_prefill_on_the_dequantised_values(orc):
+    """"EchoLLMServing notes" section 3 with the prefill of section 2: an INT8 cache attends as
+    the cache of its dequantised values K = code * k_scale, V = code * v_scale (per token and kv
+    head). With power-of-two scales those values are exact in fp32, so the INT8 prefill must equal
+    the fp32-pool prefill bit for bit -- swapping the K and V scales, or taking another token's or
+    head's scale, does not."""
+    w, ks, vs = _int8_prefill_with_pow2_scales(11, [5, 1, 40, 17], [30, 0, 7, 100])
+    a = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                    w.query_start, w.scale, ks, vs)
+    kf = (w.k_pool.astype(np.float32) * ks[..., None]).astype(np.float32)
+    vf = (w.v_pool.astype(np.float32) * vs[..., None]).astype(np.float32)
+    assert np.array_equal(kf.astype(np.float64), w.k_pool.astype(np.float64) * ks[..., None].astype(np.float64))
+    b = orc.paged_prefill_attention(w.q, kf, vf, w.block_tables, w.context_lens, w.query_start, w.scale)
+    assert np.array_equal(a, b)
+    swapped = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                          w.query_start, w.scale, vs, ks)
+    assert not np.allclose(a, swapped, atol=1e-6)
+
+
+def test_prefill_int8_matches_library_causal_attention(orc):
+    """Whole-prompt INT8 prefill is causal attention over the dequantised K/V: torch SDPA with
+    is_causal, fp64 on CPU, on values gathered here from the codes and scales."""
+    torch = pytest.importorskip("torch")
+    w = W.make_prefill(name="p8", query_lens=[33, 1, 18], cached_lens=[0, 0, 0], Hq=4, Hkv=2, D=64,
+                       seed=13, kv_dtype="i8")
+    out = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                      w.query_start, w.scale, w.k_scales, w.v_scales)
+    kf = w.k_pool.astype(np.float64) * w.k_scales[..., None].astype(np.float64)
+    vf = w.v_pool.astype(np.float64) * w.v_scales[..., None].astype(np.float64)
+    qf = W.bf16_bits_to_f32(w.q).astype(np.float64)
+    for b in range(w.B):
+        n = int(w.context_lens[b])
+        rows = [(w.block_tables[b, t // 16], t % 16) for t in range(n)]
+        K = np.stack([kf[blk, :, off] for blk, off in rows], 1)
+        V = np.stack([vf[blk, :, off] for blk, off in rows], 1)
+        Q = qf[w.query_start[b]:w.query_start[b + 1]].transpose(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(Q), torch.from_numpy(K).repeat_interleave(2, 0),
+            torch.from_numpy(V).repeat_interleave(2, 0), is_causal=True, scale=w.scale)
+        np.testing.assert_allclose(out[w.query_start[b]:w.query_start[b + 1]],
+                                   ref.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)

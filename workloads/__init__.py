@@ -355,6 +355,9 @@ class PrefillWorkload:
     context_lens: np.ndarray  # int32 [B]
     query_start: np.ndarray   # int32 [B + 1]
     scale: float
+    kv_dtype: str = "bf16"    # "bf16" or "i8"
+    k_scales: Optional[np.ndarray] = None   # float32 [NB, Hkv, BS] (int8 only)
+    v_scales: Optional[np.ndarray] = None
 
     @property
     def B(self):
@@ -365,9 +368,11 @@ class PrefillWorkload:
         return int(np.diff(self.query_start).max()) if self.B else 0
 
 
-def make_prefill(*, name, query_lens, cached_lens, Hq, Hkv, D, seed, pool_slack=0.10) -> PrefillWorkload:
+def make_prefill(*, name, query_lens, cached_lens, Hq, Hkv, D, seed, pool_slack=0.10,
+                 kv_dtype="bf16") -> PrefillWorkload:
     """Sequences with cached_lens[b] tokens already in the cache and query_lens[b] new prompt
-    tokens (also in the cache, written before attention), blocks from a shuffled pool."""
+    tokens (also in the cache, written before attention), blocks from a shuffled pool. An INT8
+    cache ("i8") holds per-row quantised codes and fp32 scales (the decode workloads' recipe)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     ql = np.asarray(query_lens, np.int64)
     cl = ql + np.asarray(cached_lens, np.int64)
@@ -380,10 +385,11 @@ def make_prefill(*, name, query_lens, cached_lens, Hq, Hkv, D, seed, pool_slack=
     for b in range(B):
         if need[b]:
             bt[b, :need[b]] = pool.allocate(need[b])
-    kp = _draw(rng, (NB, Hkv, BLOCK_SIZE, D), "bf16")
-    vp = _draw(rng, (NB, Hkv, BLOCK_SIZE, D), "bf16")
+    kp, ks = _draw_kv(rng, (NB, Hkv, BLOCK_SIZE, D), kv_dtype)
+    vp, vs = _draw_kv(rng, (NB, Hkv, BLOCK_SIZE, D), kv_dtype)
     qs = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
     q = _draw(rng, (int(qs[-1]), Hq, D), "bf16")
     return PrefillWorkload(name=name, Hq=Hq, Hkv=Hkv, D=D, BS=BLOCK_SIZE, NB=NB, q=q, k_pool=kp,
                            v_pool=vp, block_tables=bt, context_lens=cl.astype(np.int32),
-                           query_start=qs, scale=1.0 / math.sqrt(D))
+                           query_start=qs, scale=1.0 / math.sqrt(D), kv_dtype=kv_dtype,
+                           k_scales=ks, v_scales=vs)
