@@ -607,8 +607,10 @@ def run_prefill(args):
 
     import paged_kv_decode_reshape_gb300 as pkv
     pkv.load(build_if_missing=False)
-    w = W.make_prefill(name="prefill_llama3_8b", query_lens=[4096] * 4, cached_lens=[2048] * 4,
-                       Hq=32, Hkv=8, D=128, seed=7)
+    i8 = getattr(args, "prefill_kv", "bf16") == "i8"
+    w = W.make_prefill(name="prefill_llama3_8b" + ("_int8" if i8 else ""), query_lens=[4096] * 4,
+                       cached_lens=[2048] * 4, Hq=32, Hkv=8, D=128, seed=7,
+                       kv_dtype="i8" if i8 else "bf16")
 
     def up(a):
         a = np.ascontiguousarray(a)
@@ -617,11 +619,16 @@ def run_prefill(args):
         return torch.from_numpy(a).cuda()
     q, kp, vp = up(w.q), up(w.k_pool), up(w.v_pool)
     bt, cl, qs = up(w.block_tables), up(w.context_lens), up(w.query_start)
+    ks = up(w.k_scales) if i8 else None
+    vs = up(w.v_scales) if i8 else None
     out = torch.empty_like(q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
     def step():
-        pkv.paged_prefill_attention(out, q, kp, vp, bt, cl, qs, w.max_query_len, w.scale)
+        if i8:
+            pkv.paged_prefill_attention_int8(out, q, kp, vp, ks, vs, bt, cl, qs, w.max_query_len, w.scale)
+        else:
+            pkv.paged_prefill_attention(out, q, kp, vp, bt, cl, qs, w.max_query_len, w.scale)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -646,7 +653,8 @@ def run_prefill(args):
     if os.path.exists(path):
         with open(path) as f:
             peak = float(json.load(f).get("bf16_tflops", peak))
-    line = {"metric": "paged prefill attention TFLOP/s (causal, tcgen05)", "value": round(tflops, 2),
+    line = {"metric": "paged prefill attention TFLOP/s (causal, tcgen05)" + (", INT8 KV cache" if i8 else ""),
+            "value": round(tflops, 2),
             "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": max(3, args.warmup),
             "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic",
@@ -682,6 +690,8 @@ def main(argv=None):
                          "verification) on the chosen config instead of the decode step")
     ap.add_argument("--prefill", action="store_true",
                     help="time the paged prefill kernel instead of the decode step")
+    ap.add_argument("--prefill-kv", choices=["bf16", "i8"], default="bf16",
+                    help="K/V cache type of the --prefill workload")
     args = ap.parse_args(argv)
     if args.prefill:
         run_prefill(args)

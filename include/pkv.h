@@ -20,6 +20,7 @@
  *   pkv_paged_decode_attention_shared_prefix -- decode of a batch sharing a prefix: the prefix once
  *                                         per kv head on the tcgen05 tensor cores, then the suffixes.
  *   pkv_paged_prefill_attention        -- chunked, variable-length prefill (mixed batches) on tcgen05.
+ *   pkv_paged_prefill_attention_int8   -- the same over an INT8 cache, dequantised in the kernel.
  *   pkv_paged_decode_attention_static_ws -- decode with a library-held workspace (no allocation).
  *   pkv_bm_*                           -- host block manager: allocation, refcounted prefix sharing.
  *   pkv_xxh64, pkv_block_hash          -- the chained per-block prefix hash it keys shared blocks by.
@@ -149,6 +150,27 @@ pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_p
                                        int num_kv_heads, int head_dim, int block_size,
                                        int num_blocks, int max_blocks_per_seq, int max_query_len,
                                        float scale, int32_t* status, void* stream);
+
+/*
+ * Paged prefill over an INT8 cache ("EchoLLMServing inference framework notes", section 3: the
+ * per-token dequantisation fused into the attention kernels, FlashAttention prefill as well as
+ * FlashDecoding; chunked prefill and mixed prefill + decode batches over the same cache). Same
+ * rows, causal rule, arguments and errors as pkv_paged_prefill_attention, with
+ *     K_t = k_pool[blk][g][off][:] * k_scales[blk][g][off],  V_t likewise with v_scales
+ * (int8 pools [num_blocks][num_kv_heads][16][128], fp32 scales [num_blocks][num_kv_heads][16],
+ * all 16-byte aligned; q and out bf16). Inside the kernel each staged int8 row is multiplied by
+ * its token's scale and rounded to bf16 (one rounding, relative error <= 2^-9) before the tcgen05
+ * products, which take both operands in one 16-bit type (q's bf16); accumulation fp32.
+ */
+pkv_status pkv_paged_prefill_attention_int8(void* out, const void* q, const int8_t* k_pool,
+                                            const int8_t* v_pool, const float* k_scales,
+                                            const float* v_scales, const int32_t* block_tables,
+                                            const int32_t* context_lens, const int32_t* query_start,
+                                            int num_seqs, int total_query_tokens, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int num_blocks, int max_blocks_per_seq,
+                                            int max_query_len, float scale, int32_t* status,
+                                            void* stream);
 
 /*
  * Multi-token decode: L = num_query_tokens new tokens per sequence, verified in one pass, as MTP

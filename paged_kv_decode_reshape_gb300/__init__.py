@@ -36,6 +36,8 @@ SIGNATURES = {
                                           _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_paged_prefill_attention": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _P, _P], _I),
+    "pkv_paged_prefill_attention_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                          _I, _I, _I, _I, _F, _P, _P], _I),
     "pkv_paged_decode_attention_static_ws": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                               _I, _F, _I, _I, _P, _P], _I),
     "pkv_paged_decode_attention_shared_prefix": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
@@ -245,6 +247,21 @@ def paged_prefill_attention(out, q, k_pool, v_pool, block_tables, context_lens, 
         _ptr(query_start), context_lens.shape[0], T, Hq, Hkv, D, BS, NB, block_tables.shape[1],
         int(max_query_len), float(scale), _ptr(status), _stream(stream))
     _check(rc, "paged_prefill_attention")
+
+
+def paged_prefill_attention_int8(out, q, k_pool, v_pool, k_scales, v_scales, block_tables,
+                                 context_lens, query_start, max_query_len, scale, status=None,
+                                 stream=None):
+    """pkv_paged_prefill_attention_int8: as paged_prefill_attention over int8 pools with their
+    fp32 per-token scales [NB, Hkv, 16]."""
+    T, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_prefill_attention_int8(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_tables), _ptr(context_lens), _ptr(query_start), context_lens.shape[0], T, Hq,
+        Hkv, D, BS, NB, block_tables.shape[1], int(max_query_len), float(scale), _ptr(status),
+        _stream(stream))
+    _check(rc, "paged_prefill_attention_int8")
 
 
 def paged_decode_attention_static_ws(out, q, k_pool, v_pool, block_tables, context_lens,

@@ -427,6 +427,64 @@ pkv_status pkv_paged_decode_attention_int8(void* out, const void* q, const int8_
     return run_decode(a);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Paged prefill over a bf16 cache (k_scales == v_scales == null) or an INT8 cache with its scales.
+pkv_status run_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                       const float* k_scales, const float* v_scales, bool i8,
+                       const int32_t* block_tables, const int32_t* context_lens,
+                       const int32_t* query_start, int num_seqs, int total_query_tokens,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, int max_blocks_per_seq, int max_query_len, float scale,
+                       int32_t* status, void* stream) {
+    if (num_seqs < 0 || total_query_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_query_len < 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (head_dim != 128 || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
+    if (i8 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_query_tokens == 0 || max_query_len == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !query_start)
+        return PKV_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)out, q, k_pool, v_pool, (const void*)k_scales, (const void*)v_scales})
+        if (ptr && !aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || num_q_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((long long)num_blocks * num_kv_heads * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    const size_t io_b = (size_t)total_query_tokens * num_q_heads * head_dim * 2;
+    const size_t pool_b = (size_t)num_blocks * num_kv_heads * kBlockSize * head_dim * (i8 ? 1 : 2);
+    const size_t sc_b = i8 ? (size_t)num_blocks * num_kv_heads * kBlockSize * 4 : 0;
+    if (overlap(out, io_b, q, io_b) || overlap(out, io_b, k_pool, pool_b) ||
+        overlap(out, io_b, v_pool, pool_b) || overlap(out, io_b, k_scales, sc_b) ||
+        overlap(out, io_b, v_scales, sc_b) ||
+        overlap(out, io_b, block_tables, (size_t)num_seqs * max_blocks_per_seq * 4) ||
+        overlap(out, io_b, context_lens, (size_t)num_seqs * 4) ||
+        overlap(out, io_b, query_start, (size_t)(num_seqs + 1) * 4))
+        return PKV_ERR_INVALID_ARG;
+    CUtensorMap tk{}, tv{};  // INT8: the kernel copies rows with 1-D bulk copies, no tensor map
+    if (!i8 && (!make_pool_tensor_map_blocks(&tk, k_pool, num_blocks, num_kv_heads) ||
+                !make_pool_tensor_map_blocks(&tv, v_pool, num_blocks, num_kv_heads)))
+        return PKV_ERR_CUDA;
+    PrefillParams p{};
+    p.out = out; p.q = q; p.block_tables = block_tables; p.context_lens = context_lens;
+    p.query_start = query_start; p.status = status;
+    p.B = num_seqs; p.Hq = num_q_heads; p.Hkv = num_kv_heads; p.G = num_q_heads / num_kv_heads;
+    p.NB = num_blocks; p.MBPS = max_blocks_per_seq; p.scale_log2 = scale * kLog2e;
+    if (i8) {
+        p.k_i8 = static_cast<const int8_t*>(k_pool); p.v_i8 = static_cast<const int8_t*>(v_pool);
+        p.k_scales = k_scales; p.v_scales = v_scales;
+    }
+    return launch_prefill(p, tk, tv, max_query_len, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
 pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_pool,
                                        const void* v_pool, const int32_t* block_tables,
                                        const int32_t* context_lens, const int32_t* query_start,
@@ -434,39 +492,23 @@ pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_p
                                        int num_kv_heads, int head_dim, int block_size,
                                        int num_blocks, int max_blocks_per_seq, int max_query_len,
                                        float scale, int32_t* status, void* stream) {
-    if (num_seqs < 0 || total_query_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_query_len < 0 ||
-        num_q_heads % num_kv_heads != 0)
-        return PKV_ERR_INVALID_ARG;
-    if (head_dim != 128 || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
-    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
-    if (num_seqs == 0 || total_query_tokens == 0 || max_query_len == 0) return PKV_OK;
-    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !query_start)
-        return PKV_ERR_INVALID_ARG;
-    for (const void* ptr : {(const void*)out, q, k_pool, v_pool})
-        if (!aligned(ptr, 16)) return PKV_ERR_INVALID_ARG;
-    if (num_seqs > 65535 || num_q_heads > 65535) return PKV_ERR_UNSUPPORTED;
-    if ((long long)num_blocks * num_kv_heads * kBlockSize > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
-    const size_t io_b = (size_t)total_query_tokens * num_q_heads * head_dim * 2;
-    const size_t pool_b = (size_t)num_blocks * num_kv_heads * kBlockSize * head_dim * 2;
-    if (overlap(out, io_b, q, io_b) || overlap(out, io_b, k_pool, pool_b) ||
-        overlap(out, io_b, v_pool, pool_b) ||
-        overlap(out, io_b, block_tables, (size_t)num_seqs * max_blocks_per_seq * 4) ||
-        overlap(out, io_b, context_lens, (size_t)num_seqs * 4) ||
-        overlap(out, io_b, query_start, (size_t)(num_seqs + 1) * 4))
-        return PKV_ERR_INVALID_ARG;
-    CUtensorMap tk, tv;
-    if (!make_pool_tensor_map_blocks(&tk, k_pool, num_blocks, num_kv_heads) ||
-        !make_pool_tensor_map_blocks(&tv, v_pool, num_blocks, num_kv_heads))
-        return PKV_ERR_CUDA;
-    PrefillParams p{};
-    p.out = out; p.q = q; p.block_tables = block_tables; p.context_lens = context_lens;
-    p.query_start = query_start; p.status = status;
-    p.B = num_seqs; p.Hq = num_q_heads; p.Hkv = num_kv_heads; p.G = num_q_heads / num_kv_heads;
-    p.NB = num_blocks; p.MBPS = max_blocks_per_seq; p.scale_log2 = scale * kLog2e;
-    return launch_prefill(p, tk, tv, max_query_len, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PKV_OK
-               : PKV_ERR_CUDA;
+    return run_prefill(out, q, k_pool, v_pool, nullptr, nullptr, false, block_tables, context_lens,
+                       query_start, num_seqs, total_query_tokens, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, max_blocks_per_seq, max_query_len, scale, status, stream);
+}
+
+pkv_status pkv_paged_prefill_attention_int8(void* out, const void* q, const int8_t* k_pool,
+                                            const int8_t* v_pool, const float* k_scales,
+                                            const float* v_scales, const int32_t* block_tables,
+                                            const int32_t* context_lens, const int32_t* query_start,
+                                            int num_seqs, int total_query_tokens, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int num_blocks, int max_blocks_per_seq,
+                                            int max_query_len, float scale, int32_t* status,
+                                            void* stream) {
+    return run_prefill(out, q, k_pool, v_pool, k_scales, v_scales, true, block_tables, context_lens,
+                       query_start, num_seqs, total_query_tokens, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, max_blocks_per_seq, max_query_len, scale, status, stream);
 }
 
 pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void* k_pool,

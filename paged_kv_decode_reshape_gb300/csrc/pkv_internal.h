@@ -149,6 +149,11 @@ struct PrefillParams {
     int32_t* status;
     int B, Hq, Hkv, G, NB, MBPS;
     float scale_log2;
+    // INT8 cache (else null): the pools [NB][Hkv][16][128] int8 and scales [NB][Hkv][16] fp32
+    const int8_t* k_i8;
+    const int8_t* v_i8;
+    const float* k_scales;
+    const float* v_scales;
 };
 
 // Shared-prefix (cascade) decode, prefix part: every (sequence, query head) row of one kv head

@@ -83,6 +83,21 @@ constexpr int kPfOffBar = kPfOffX + 3 * kPfSplit * kPfQ * 4;
 constexpr int kPfNumBars = 4 * kPfStages + 9;
 constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
 constexpr int kPfThreads = kPfSoftThreads + 128;
+// INT8 cache: the producers copy each block's int8 K (or V) rows (2 KB) into the second half of the
+// tile's slot and its 16 scales into a row of the scale area, completing on staged[ring][slot]; four
+// converter warps (two per ring) widen them in place into the bf16 layout above and then complete
+// full[ring][slot] for the MMA issuers, as the tensor copies do for a bf16 cache.
+constexpr int kPfConvWarp0 = kPfSoftWarps + 4;       // warps 12-13: K ring, 14-15: V ring
+constexpr int kPfConvThreads = 64;                   // per ring
+constexpr int kPfI8Half = kPfStage / 2;              // int8 rows of a tile start here in the slot
+constexpr int kPfOffStaged = kPfOffBar + kPfNumBars * 8 + 16;   // after the TMEM slot
+constexpr int kPfOffScl = (kPfOffStaged + 2 * kPfStages * 8 + 15) / 16 * 16;  // [2 rings][S][8 blocks][16] fp32
+constexpr int kPfSmemI8 = 1024 + kPfOffScl + 2 * kPfStages * 8 * kBlockSize * 4;
+constexpr int kPfThreadsI8 = kPfThreads + 32 * 4;
+template <bool kI8> constexpr int pf_threads() { return kI8 ? kPfThreadsI8 : kPfThreads; }
+template <bool kI8> constexpr int pf_smem() { return kI8 ? kPfSmemI8 : kPfSmem; }
+static_assert(kPfSmemI8 <= 227 * 1024, "shared memory (INT8)");
+static_assert(kPfOffScl % 16 == 0, "scale rows are bulk-copy targets");
 constexpr int kPfMmaWarp = kPfSoftWarps, kPfLoadWarpK = kPfSoftWarps + 1, kPfLoadWarpV = kPfSoftWarps + 2,
               kPfMmaWarpPV = kPfSoftWarps + 3;
 constexpr uint32_t kPfTmemCols = 512;
@@ -144,6 +159,16 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 
@@ -285,10 +310,29 @@ struct PfWork {
     float* ws_acc;
     float* ws_ml;
     int B, S, slot0, prefix_tokens, split_tokens;
+    // INT8 cache: the pools as [NB][Hkv][16][128] int8 and their scales [NB][Hkv][16]
+    const int8_t* k_i8;
+    const int8_t* v_i8;
+    const float* k_scales;
+    const float* v_scales;
 };
 
-template <bool kPrefix>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
+// Four int8 values (one 32-bit word) times `scale`, as two bf16 pairs (RN): each byte goes to the
+// low byte of 2^23 + (x + 128) (the sign flipped by the XOR), so one subtraction gives x exactly.
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint64_t scale2, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint64_t bias2 = f32x2(8388736.0f, 8388736.0f);  // 2^23 + 128
+    float a, b, c, d;
+    f32x2_split(mul_f32x2(sub_f32x2(f32x2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
+                                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))), bias2), scale2), a, b);
+    f32x2_split(mul_f32x2(sub_f32x2(f32x2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
+                                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))), bias2), scale2), c, d);
+    lo = pack2_bf16(a, b);
+    hi = pack2_bf16(c, d);
+}
+
+template <bool kPrefix, bool kI8>
+__global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfWork p,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
     grid_dependency_wait();
@@ -356,13 +400,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
     const uint32_t o_done = bar0 + 8 * (4 * kPfStages + 6);
     auto drain = [&](int x) { return bar0 + 8 * (4 * kPfStages + 7 + x); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + kPfNumBars * 8);
+    // INT8: the int8 rows of ring g's slot s have landed (the producer's copies)
+    auto staged = [&](int g, int s) { return sbase + kPfOffStaged + 8 * (g * kPfStages + s); };
+    auto scl = [&](int g, int s) { return sbase + kPfOffScl + (g * kPfStages + s) * 8 * kBlockSize * 4; };
     __shared__ int abort_flag;
 
     if (tid == 0) {
         for (int g = 0; g < 2; ++g)
             for (int s = 0; s < kPfStages; ++s) {
-                mbar_init(full(g, s), 1);
-                mbar_init(empty(g, s), 1);
+                mbar_init(full(g, s), kI8 ? kPfConvThreads : 1);
+                // INT8 K slot: its scale row is read by the softmax warps after S is done
+                mbar_init(empty(g, s), kI8 && g == 0 ? 1 + kPfSoftWarps : 1);
+                if constexpr (kI8) mbar_init(staged(g, s), 1);
             }
         mbar_init(s_full, 1);
         mbar_init(s_free, kPfSoftThreads);
@@ -436,21 +485,84 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             int id = __shfl_sync(0xffffffffu, ids_cur, 8 * (t & 3) + (lane & 7));
             if (lane >= 8) id = -1;
             const unsigned valid = __ballot_sync(0xffffffffu, id >= 0);
+            // bf16: the tensor copies complete full(g); INT8: the row copies complete staged(g)
+            const uint32_t done = kI8 ? staged(g, st) : full(g, st);
+            constexpr int kBytes = kI8 ? kPfBlockBytes / 2 + kBlockSize * 4 : kPfBlockBytes;
             if (lane == 0) {
-                if (valid == 0) mbar_arrive(full(g, st));
-                else mbar_arrive_expect_tx(full(g, st), __popc(valid) * kPfBlockBytes);
+                if (valid == 0) mbar_arrive(done);
+                else mbar_arrive_expect_tx(done, __popc(valid) * kBytes);
             }
             __syncwarp();
             if (id >= 0) {
-                const int grp = (id * p.Hkv + kvh) * (kBlockSize / 8);  // the block's first 8-row group
-                tma_load_4d(slot(g, t) + lane * kPfBlockBytes, map, 0, 0, 0, grp, full(g, st));
+                if constexpr (kI8) {  // 2 KB of int8 rows and 64 B of scales per (block, kv head)
+                    const size_t tile = (size_t)id * p.Hkv + kvh;
+                    bulk_g2s(slot(g, t) + kPfI8Half + lane * (kPfBlockBytes / 2),
+                             (g ? p.v_i8 : p.k_i8) + tile * (kPfBlockBytes / 2), kPfBlockBytes / 2, done);
+                    bulk_g2s(scl(g, st) + lane * kBlockSize * 4, (g ? p.v_scales : p.k_scales) + tile * kBlockSize,
+                             kBlockSize * 4, done);
+                } else {
+                    const int grp = (id * p.Hkv + kvh) * (kBlockSize / 8);  // the block's first 8-row group
+                    tma_load_4d(slot(g, t) + lane * kPfBlockBytes, map, 0, 0, 0, grp, done);
+                }
             }
             issued = t + 1;
         }
         if (aborted(&abort_flag) && lane == 0) {
             // let this CTA's own copies land before shared memory goes away
             for (int t = issued - kPfStages < 0 ? 0 : issued - kPfStages; t < issued; ++t)
-                mbar_wait_bounded(full(g, t % kPfStages), (t / kPfStages) & 1);
+                mbar_wait_bounded(kI8 ? staged(g, t % kPfStages) : full(g, t % kPfStages), (t / kPfStages) & 1);
+        }
+    } else if (kI8 && warp >= kPfConvWarp0) {
+        // ---------------- INT8: converters of ring g (warps 12-13: K, 14-15: V) ----------------
+        // Thread c widens keys c and c + 64 of each tile: the key's 128 int8 values (V: times the
+        // key's scale, rounded to bf16; K: the codes, exact) into the 128-byte-swizzled rows the MMA
+        // descriptors read. All of the
+        // ring's int8 rows are read into registers before any bf16 row is written, since the bf16
+        // tile fills the whole slot, over the int8 rows in its second half.
+        const int g = (warp - kPfConvWarp0) >> 1;
+        const int c = tid - 32 * (kPfConvWarp0 + 2 * g);
+        const int bar_id = 5 + g;  // named barrier of the ring's kPfConvThreads threads
+        for (int t = 0; t < ntiles; ++t) {
+            const int st = t % kPfStages;
+            const bool got = mbar_wait_bounded(staged(g, st), (t / kPfStages) & 1);
+            if (!got && lane_of() == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
+            if (barrier_or(bar_id, kPfConvThreads, !got || aborted(&abort_flag))) break;
+            uint4 in[2][8];
+            float sc[2];
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const int key = c + 64 * kk, blk = key >> 4, kin = key & 15;
+                const uint4* row = reinterpret_cast<const uint4*>(smem + (g ? kPfOffV : kPfOffK) + st * kPfStage +
+                                                                   kPfI8Half + blk * (kPfBlockBytes / 2) + kin * 128);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) in[kk][v] = row[(v + lane) & 7];  // rotated: no bank conflicts
+                sc[kk] = reinterpret_cast<const float*>(smem + kPfOffScl)[((g * kPfStages + st) * 8 + blk) * kBlockSize + kin];
+            }
+            named_barrier_sync(bar_id, kPfConvThreads);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const int key = c + 64 * kk, blk = key >> 4, kin = key & 15;
+                // K: the codes themselves (exact in bf16); the softmax multiplies each score by its
+                // key's scale in fp32. V: code * scale rounded to bf16.
+                const uint64_t s2 = g ? f32x2(sc[kk], sc[kk]) : f32x2(1.f, 1.f);
+                unsigned char* base = smem + (g ? kPfOffV : kPfOffK) + st * kPfStage + blk * kPfBlockBytes +
+                                      (kin >> 3) * 2048 + (kin & 7) * 128;
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const int vv = (v + lane) & 7;  // dims 16 vv .. 16 vv + 15
+                    uint32_t o[8];
+                    i8x4_to_bf16x4(in[kk][v].x, s2, o[0], o[1]);
+                    i8x4_to_bf16x4(in[kk][v].y, s2, o[2], o[3]);
+                    i8x4_to_bf16x4(in[kk][v].z, s2, o[4], o[5]);
+                    i8x4_to_bf16x4(in[kk][v].w, s2, o[6], o[7]);
+                    const int half = vv >> 2, ch = (2 * vv) & 7;  // 16-byte chunks ch, ch + 1 of the half
+                    unsigned char* hb = base + half * 1024;
+                    *reinterpret_cast<uint4*>(hb + ((ch ^ (kin & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(hb + (((ch + 1) ^ (kin & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads them async
+            mbar_arrive(full(g, st));
         }
     } else if (warp == kPfMmaWarp || warp == kPfMmaWarpPV) {
         // ---------------- MMA issuers: S (warp 8) and PV (warp 11) ----------------
@@ -569,6 +681,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PfWork p,
             }
             float s[kPfKeysPer];
             tmem_ld_words(s_col, s);  // (reading TMEM is harmless even when S(t) never came)
+            if constexpr (kI8) {
+                // S holds q . codes: times each key's K scale (the staged scale row of the K slot,
+                // keys in tile order), then the slot may be refilled
+                const float4* ks4 = reinterpret_cast<const float4*>(smem + kPfOffScl) +
+                                    ((t % kPfStages) * 8 * kBlockSize + kPfKeysPer * hf) / 4;
+#pragma unroll
+                for (int c = 0; c < kPfKeysPer / 4; ++c) {
+                    const float4 k4 = ks4[c];
+                    float a, b2;
+                    f32x2_split(mul_f32x2(f32x2(s[4 * c], s[4 * c + 1]), f32x2(k4.x, k4.y)), a, b2);
+                    s[4 * c] = a; s[4 * c + 1] = b2;
+                    f32x2_split(mul_f32x2(f32x2(s[4 * c + 2], s[4 * c + 3]), f32x2(k4.z, k4.w)), a, b2);
+                    s[4 * c + 2] = a; s[4 * c + 3] = b2;
+                }
+                __syncwarp();
+                if (lane_of() == 0) mbar_arrive(empty(0, t % kPfStages));
+            }
             tc_fence_before();
             mbar_arrive(s_free);  // S(t + 1) may now be written
             // raw scores here; the scale (with log2 e) is applied inside each exponent below
@@ -727,15 +856,24 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const 
     w.q = p.q; w.block_tables = p.block_tables; w.status = p.status;
     w.Hq = p.Hq; w.Hkv = p.Hkv; w.G = p.G; w.NB = p.NB; w.MBPS = p.MBPS; w.scale_log2 = p.scale_log2;
     w.out = p.out; w.context_lens = p.context_lens; w.query_start = p.query_start; w.B = p.B;
+    w.k_i8 = p.k_i8; w.v_i8 = p.v_i8; w.k_scales = p.k_scales; w.v_scales = p.v_scales;
     const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hq, p.B);
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (p.k_i8) {
+        auto kern = prefill_kernel<false, true>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemI8);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, grid, dim3(kPfThreadsI8), kPfSmemI8, s, w, tk, tv);
+    }
+    auto kern = prefill_kernel<false, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(prefill_kernel<false>, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
+    return launch_pdl(kern, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int splits,
                           cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    auto kern = prefill_kernel<true, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return e;
     PfWork w{};
     w.q = p.q; w.block_tables = p.block_tables; w.status = p.status;
@@ -743,7 +881,7 @@ cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CU
     w.ws_acc = p.ws_acc; w.ws_ml = p.ws_ml; w.B = p.B; w.S = p.S; w.slot0 = p.slot0;
     w.prefix_tokens = p.prefix_tokens; w.split_tokens = p.split_tokens;
     const dim3 grid((p.B * p.G + kPfQ - 1) / kPfQ, p.Hkv, splits);
-    return launch_pdl(prefill_kernel<true>, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
+    return launch_pdl(kern, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
 }
 
 }  // namespace pkv

@@ -1,0 +1,125 @@
+"""GPU parity of the paged prefill over an INT8 cache (pkv_paged_prefill_attention_int8) against the
+fp64 oracle on the dequantised values: the query-length mix of a chunked-prefill / mixed batch
+(decode rows of one token beside prompt chunks of several 128-row tiles), cached prefixes, GQA
+groups, missing blocks and extreme scales, at the INT8 bar ("EchoLLMServing inference framework
+notes", section 3: per-token dequantisation fused into the FlashAttention prefill)."""
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_decode_reshape_gb300 as P
+import workloads as W
+from _gpu import assert_close, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(pkv):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_prefill_i8(w, status=None, bt=None):
+    bt = w.block_tables if bt is None else bt
+    out = torch.zeros((w.q.shape[0], w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    P.paged_prefill_attention_int8(out, to_dev(w.q), to_dev(w.k_pool), to_dev(w.v_pool),
+                                   to_dev(w.k_scales), to_dev(w.v_scales), to_dev(bt),
+                                   to_dev(w.context_lens), to_dev(w.query_start), w.max_query_len,
+                                   w.scale, status)
+    return to_f64(out)
+
+
+def reference(w):
+    return oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                          w.query_start, w.scale, w.k_scales, w.v_scales)
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2), (6, 2), (4, 2), (32, 2)])
+def test_prefill_int8_matches_oracle(hq, hkv):
+    w = W.make_prefill(name="pf8", query_lens=[1, 5, 127, 128, 129, 300],
+                       cached_lens=[0, 17, 64, 200, 5, 1000], Hq=hq, Hkv=hkv, D=128,
+                       seed=hq + hkv + 100, kv_dtype="i8")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill_i8(w, st)
+    assert_close(got, reference(w), "i8", f"INT8 prefill Hq={hq} Hkv={hkv}")
+    assert int(st.item()) == 0
+
+
+def test_prefill_int8_mixed_batch_decode_rows_equal_decode():
+    """A mixed batch: one-token rows (decode) beside prompt chunks; the decode rows must equal the
+    INT8 decode oracle and the chunks the prefill oracle."""
+    w = W.make_prefill(name="pfm8", query_lens=[1, 200, 1, 1, 64], cached_lens=[900, 30, 15, 0, 333],
+                       Hq=32, Hkv=8, D=128, seed=41, kv_dtype="i8")
+    got = run_prefill_i8(w)
+    ref = reference(w)
+    assert_close(got, ref, "i8", "mixed INT8 batch")
+    dec = [0, 2, 3]
+    rows = w.query_start[dec]
+    ref_dec = oracle.paged_decode_attention(w.q[rows], w.k_pool, w.v_pool, w.block_tables[dec],
+                                            w.context_lens[dec], w.scale, w.k_scales, w.v_scales)
+    assert_close(got[rows], ref_dec, "i8", "decode rows")
+
+
+def test_prefill_int8_long_prompt_and_empty_sequences():
+    w = W.make_prefill(name="pfl8", query_lens=[1000, 0, 37], cached_lens=[2048, 10, 3000], Hq=32,
+                       Hkv=8, D=128, seed=8, kv_dtype="i8")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill_i8(w, st)
+    assert_close(got, reference(w), "i8", "long INT8 prompt")
+    assert int(st.item()) == 0
+
+
+def test_prefill_int8_missing_block_is_skipped_and_flagged():
+    w = W.make_prefill(name="pfb8", query_lens=[40, 70], cached_lens=[100, 30], Hq=16, Hkv=4, D=128,
+                       seed=9, kv_dtype="i8")
+    bt = w.block_tables.copy()
+    bt[0, 2] = w.NB + 5
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill_i8(w, st, bt)
+    assert int(st.item()) & P.FLAG_BAD_BLOCK
+    assert np.all(np.isfinite(got))
+    s1 = slice(w.query_start[1], w.query_start[2])
+    assert_close(got[s1], reference(w)[s1], "i8", "untouched sequence")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 2.0, 0.0])
+def test_prefill_int8_scale_sign_and_running_max_rescale(scale):
+    w = W.make_prefill(name="pfs8", query_lens=[300, 129], cached_lens=[700, 0], Hq=8, Hkv=2,
+                       D=128, seed=17, kv_dtype="i8")
+    w.scale = scale
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill_i8(w, st)
+    assert_close(got, reference(w), "i8", f"INT8 prefill scale={scale}")
+    assert int(st.item()) == 0
+
+
+def test_prefill_int8_every_byte_value():
+    """One visible key per row (L = 1, context 1) with unit V scale: out = that key's int8 V row,
+    exact in bf16 for every code -128..127 across two sequences."""
+    D, Hkv = 128, 1
+    NB = 2
+    kp = np.zeros((NB, Hkv, 16, D), np.int8)
+    vp = np.zeros((NB, Hkv, 16, D), np.int8)
+    allv = np.arange(-128, 128, dtype=np.int16).astype(np.int8)
+    vp[0, 0, 0], vp[1, 0, 0] = allv[:128], allv[128:]
+    ones = np.ones((NB, Hkv, 16), np.float32)
+    w = W.PrefillWorkload(name="bytes8", Hq=1, Hkv=1, D=D, BS=16, NB=NB,
+                          q=W.f32_to_bf16_bits(np.ones((2, 1, D), np.float32)), k_pool=kp, v_pool=vp,
+                          block_tables=np.array([[0], [1]], np.int32),
+                          context_lens=np.array([1, 1], np.int32),
+                          query_start=np.array([0, 1, 2], np.int32), scale=0.1, kv_dtype="i8",
+                          k_scales=ones, v_scales=ones)
+    got = run_prefill_i8(w)
+    np.testing.assert_array_equal(got[:, 0].reshape(-1), allv.astype(np.float64))
+
+
+def test_prefill_int8_argument_errors():
+    w = W.make_prefill(name="pfe8", query_lens=[3], cached_lens=[5], Hq=8, Hkv=2, D=128, seed=2,
+                       kv_dtype="i8")
+    out = torch.zeros((3, 8, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(P.PkvError):  # scales missing
+        P.paged_prefill_attention_int8(out, to_dev(w.q), to_dev(w.k_pool), to_dev(w.v_pool), None,
+                                       to_dev(w.v_scales), to_dev(w.block_tables),
+                                       to_dev(w.context_lens), to_dev(w.query_start), 3, w.scale)
