@@ -75,6 +75,7 @@ constexpr int kMmaHeads = 8;        // MMA N: query heads per CTA
 #define PKV_MMA_UNROLL_I8 1
 #endif
 constexpr int kUnrollI8 = PKV_MMA_UNROLL_I8;
+
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 
 template <bool kI8, int kNT = 1>
@@ -96,6 +97,7 @@ struct MmaGeom {
     // + 1024 for aligning the ring to the 128-byte-swizzle atom
     static constexpr int SMEM = 1024 + MAIN + SCALES + STAGES * 8;
     static_assert(RING % 1024 == 0 && STAGE % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+    static_assert(RING >= 4 * (kLptMaxRows + 1), "longest-first scratch fits in the ring");
 
 };
 
@@ -142,6 +144,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // 0x64806480 after masking. The 1152 offset is removed once per score / per output (below),
 // never per element.
 constexpr float kI8Bias = 1152.0f;
+constexpr int kBiasFoldBlocks = 8;  // INT8: blocks between removals of the V offset from O
 __device__ __forceinline__ uint32_t i8_lo_h2(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x64806480u; }
 __device__ __forceinline__ uint32_t i8_hi_h2(uint32_t w) { return ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u; }
 
@@ -160,10 +163,12 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // kNT: 8-column MMA n-tiles per CTA. With 2, a warp reads and widens each K/V tile once for 16
 // columns (G = 16, or multi-token rows of G = 8).
 template <bool kI8, bool kPacked, int kNT>
+// bf16: three CTAs per SM (shared memory bounds it there anyway), so up to 170 registers a thread;
+// INT8: the compiler's own choice (96, five CTAs per SM), or the tunable minimum
 #if PKV_MMA_MINB_I8 > 0
-#define PKV_MMA_BOUNDS __launch_bounds__(MmaGeom<kI8, kNT>::THREADS, kI8 ? PKV_MMA_MINB_I8 : 1)
+#define PKV_MMA_BOUNDS __launch_bounds__(MmaGeom<kI8, kNT>::THREADS, kI8 ? PKV_MMA_MINB_I8 : 3)
 #else
-#define PKV_MMA_BOUNDS __launch_bounds__(MmaGeom<kI8, kNT>::THREADS)
+#define PKV_MMA_BOUNDS __launch_bounds__(MmaGeom<kI8, kNT>::THREADS, kI8 ? 0 : 3)
 #endif
 __global__ void PKV_MMA_BOUNDS mma_split_kernel(const SplitParams p,
                                                                const __grid_constant__ CUtensorMap tmk,
@@ -187,20 +192,49 @@ __global__ void PKV_MMA_BOUNDS mma_split_kernel(const SplitParams p,
     // decode -- the (query token, head) pairs of one sequence's kv head, so that the L tokens
     // being verified read each K/V tile once. The splits follow the longest context (the last
     // token's); each column masks the keys past its own context n - (L - 1 - l).
-    const int b = kPacked ? (int)blockIdx.z : (int)blockIdx.z / p.L;
-    const int lq = kPacked ? p.L - 1 : (int)blockIdx.z - b * p.L;  // the token the splits follow
-    const int c0 = hc * NCOL;                                    // first column of this CTA
-    const int ncols = kPacked ? p.L * p.G : p.G;
-    const int nh = ncols - c0 < NCOL ? ncols - c0 : NCOL;        // columns in use
-    auto col_zb = [&](int j) { return kPacked ? b * p.L + (c0 + j) / p.G : (int)blockIdx.z; };
-    auto col_head = [&](int j) { return kvh * p.G + (kPacked ? (c0 + j) % p.G : c0 + j); };
-
     // Inputs (new K/V rows, tables) may come from the previous kernel: wait for it. In a
     // shared-prefix call the previous kernel is the prefix kernel, which releases this one only
     // after its own wait (so the inputs are complete) and writes nothing this kernel reads; this
     // kernel then runs alongside it and waits for it only at exit, which keeps the merge kernel
     // (waiting for this grid) behind both.
     if (p.kv_start == 0) grid_dependency_wait();
+
+    // Grid row z of the launch is row z of q / out, or with p.lpt (one row per sequence, at most
+    // kLptMaxRows of them) the sequence of rank z when the sequences are ordered by the length of
+    // their splits, longest first (ties by index). CTAs start in grid order, so the longest
+    // (sequence, kv head, split) units start first and the last wave holds the shortest ones.
+    int zrow = (int)blockIdx.z;
+    if (p.lpt) {
+        // scratch at the start of the ring, which no copy has reached yet
+        int* lpt_key = reinterpret_cast<int*>(smem);
+        int& lpt_row = lpt_key[kLptMaxRows];
+        for (int i = tid; i < p.B; i += G::THREADS) {
+            bool bd;
+            const int ni = query_context_len(p.context_lens[i], p.L, p.L - 1, p.MBPS * kBlockSize, &bd);
+            int pi;
+            split_count(ni > p.kv_start ? ni - p.kv_start : 0, p.chunk, p.max_splits, &pi);
+            lpt_key[i] = pi;
+        }
+        __syncthreads();
+        for (int i = tid; i < p.B; i += G::THREADS) {
+            const int ki = lpt_key[i];
+            int rank = 0;
+            for (int j = 0; j < p.B; ++j) {
+                const int kj = lpt_key[j];
+                rank += (kj > ki) | ((kj == ki) & (j < i));
+            }
+            if (rank == zrow) lpt_row = i;
+        }
+        __syncthreads();
+        zrow = lpt_row;
+    }
+    const int b = kPacked ? zrow : zrow / p.L;
+    const int lq = kPacked ? p.L - 1 : zrow - b * p.L;  // the token the splits follow
+    const int c0 = hc * NCOL;                                    // first column of this CTA
+    const int ncols = kPacked ? p.L * p.G : p.G;
+    const int nh = ncols - c0 < NCOL ? ncols - c0 : NCOL;        // columns in use
+    auto col_zb = [&](int j) { return kPacked ? b * p.L + (c0 + j) / p.G : zrow; };
+    auto col_head = [&](int j) { return kvh * p.G + (kPacked ? (c0 + j) % p.G : c0 + j); };
 
     const int stored = p.context_lens[b];
     bool bad;
@@ -596,6 +630,29 @@ __global__ void PKV_MMA_BOUNDS mma_split_kernel(const SplitParams p,
                         }
 #pragma unroll
                         for (int t = 0; t < kNT; ++t) mma16816<false>(o[t][i], a, pb[t][0], pb[t][1]);
+                    }
+                }
+            }
+            if constexpr (kI8) {
+                // Every kBiasFoldBlocks blocks, take the 1152 offset of the biased V out of O (the
+                // column's weight sum over the warp's 8 token rows), so O never holds more than
+                // that many blocks' worth of offset: the subtraction then cancels no more digits
+                // of O than a short split would, whatever the split's length.
+                if ((k % kBiasFoldBlocks) == kBiasFoldBlocks - 1) {
+#pragma unroll
+                    for (int t = 0; t < kNT; ++t) {
+                        float w0 = psum[t][0], w1 = psum[t][1];
+#pragma unroll
+                        for (int off = 4; off <= 16; off <<= 1) {
+                            w0 += __shfl_xor_sync(0xffffffffu, w0, off);
+                            w1 += __shfl_xor_sync(0xffffffffu, w1, off);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o[t][i][0] = fmaf(-kI8Bias, w0, o[t][i][0]); o[t][i][2] = fmaf(-kI8Bias, w0, o[t][i][2]);
+                            o[t][i][1] = fmaf(-kI8Bias, w1, o[t][i][1]); o[t][i][3] = fmaf(-kI8Bias, w1, o[t][i][3]);
+                        }
+                        psum[t][0] = psum[t][1] = 0.f;
                     }
                 }
             }

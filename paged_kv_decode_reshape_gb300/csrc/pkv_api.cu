@@ -210,6 +210,10 @@ pkv_status run_decode(const Decode& a) {
     p.ws_stride = Sw;
     p.packed = packed;
     p.ntiles = ntiles;
+    // longest units first: the bf16 kernel (measured on GB300: the Llama-3-8B GQA batch 103.1 ->
+    // 98.3 us); not the INT8 one, whose many short CTAs pay more for the ranking than they gain
+    // (the INT8 batch 212.8 -> 234.9 us)
+    p.lpt = mma && a.kv_dtype == PKV_BF16 && (a.L == 1 || packed) && a.B > 1 && a.B <= kLptMaxRows;
 
     cudaError_t e;
     if (mma) {

@@ -21,6 +21,12 @@ constexpr int kMaxAutoChunk = 4096;
 // the INT8 one keeps 5 per SM and, doing more arithmetic per byte, does best with more of them.
 constexpr long long kTargetUnitsBf16Mma = 1024;
 constexpr long long kTargetUnits = 4096;  // INT8 tensor-core and CUDA-core kernels
+#ifndef PKV_LPT_MAX_ROWS
+#define PKV_LPT_MAX_ROWS 128
+#endif
+// the tensor-core split kernel starts the longest units first for batches of up to this many
+// sequences (each CTA ranks the sequences' split lengths at entry: work grows with the square)
+constexpr int kLptMaxRows = PKV_LPT_MAX_ROWS;
 constexpr int kMinChunkI8Mma = 512;       // INT8 tensor-core kernel: auto chunk at least this,
 constexpr int kMaxSplitsI8Mma = 32;       // and at most this many splits for the longest sequence
 
@@ -75,6 +81,8 @@ struct SplitParams {
     int ws_stride;              // partial slots per (row, query head) in the workspace (>= max_splits)
     int packed;                 // multi-token: one CTA column per (query token, head) of a sequence
     int ntiles;                 // tensor-core kernel: 8-column MMA n-tiles per CTA (1 or 2)
+    int lpt;                    // tensor-core kernel: grid row z = the sequence of rank z, longest
+                                // splits first (one row per sequence, B <= its row limit)
 };
 
 struct MergeParams {
