@@ -3,8 +3,11 @@ attention (split kernel + merge kernel), through the C ABI, on a seeded syntheti
 
 Prints one JSON line. `value` is algorithmic KV GB/s of the whole step (bytes the step must move
 divided by device time), `tokens_per_s` the decoded tokens per second of that one attention
-layer. L2 is flushed before every step (a 512 MB write, then a 256 MB read so that no dirty line
-of the flush is written back during the timed kernels), outside the timed events.
+layer. L2 is flushed before every step (a 512 MB write, then a 1 GB read so that no dirty line
+of the flush is written back during the timed kernels), outside the timed events. The flush keeps
+the GPU busy for ~0.2 ms per step, long enough that the host has queued the step's launches
+before the first timed event runs: the events then hold device time only (with a 256 MB read the
+Llama-3-8B-shaped step measures ~4 % slower, host launch time leaking into the events).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--chunk T]
     python bench.py --impl reference ...   # the fp64 oracle on the host cores, same metric
@@ -391,7 +394,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def flush_l2(k):
-        # write a buffer 4x the L2, then read another one, so the step starts with a cold L2 holding
+        # write a buffer 4x the L2, then read a 1 GB one, so the step starts with a cold L2 holding
         # clean lines (no write-back of the flush's dirty lines charged to the timed kernels)
         flush.fill_(k & 0xFF)
         clean.max()
@@ -489,7 +492,7 @@ def run_ours(args):
                    "max_context": maxc, "split_chunk": chunk,
                    "shared_prefix_call": bool(cascade),
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write, then a "
-                         f"{L2_FLUSH_BYTES >> 21} MB read so no dirty line is left; untimed)",
+                         f"{(L2_FLUSH_BYTES // 2) * 4 >> 20} MB read so no dirty line is left; untimed)",
                    "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(tokens_per_s, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
