@@ -17,7 +17,7 @@
  * Around it:
  *   pkv_kv_cache_write_int8            -- the INT8 cache's write: quantise each row, keep its scale.
  *   pkv_paged_decode_attention_multi   -- L query tokens per sequence, causal among themselves.
- *   pkv_paged_decode_attention_shared_prefix -- decode of a batch sharing a prefix: the prefix once
+ *   pkv_paged_decode_attention_shared_prefix[_int8] -- decode of a batch sharing a prefix: the prefix once
  *                                         per kv head on the tcgen05 tensor cores, then the suffixes.
  *   pkv_paged_prefill_attention        -- chunked, variable-length prefill (mixed batches) on tcgen05.
  *   pkv_paged_prefill_attention_int8   -- the same over an INT8 cache, dequantised in the kernel.
@@ -222,9 +222,23 @@ pkv_status pkv_paged_decode_attention_shared_prefix(
     int shared_prefix_tokens, int split_chunk_tokens, void* workspace, size_t workspace_bytes,
     int32_t* status, void* stream);
 
-/* Workspace bytes pkv_paged_decode_attention_shared_prefix needs (0 for invalid arguments):
- * num_seqs * num_q_heads * (suffix splits + prefix key splits) * (head_dim + 2) * 4. Pure host
- * arithmetic. */
+/*
+ * The same over an INT8 cache ("EchoLLMServing inference framework notes", section 3): int8 pools
+ * with their fp32 per-token scales [num_blocks][num_kv_heads][16], q and out bf16. The prefix goes
+ * through the INT8 prefill kernel's machinery (rows dequantised in shared memory), the suffixes
+ * through the INT8 split-K decode kernel; the result is pkv_paged_decode_attention_int8's.
+ */
+pkv_status pkv_paged_decode_attention_shared_prefix_int8(
+    void* out, const void* q, const int8_t* k_pool, const int8_t* v_pool, const float* k_scales,
+    const float* v_scales, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    int max_blocks_per_seq, int max_context_len, float scale, int shared_prefix_tokens,
+    int split_chunk_tokens, void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* Workspace bytes pkv_paged_decode_attention_shared_prefix[_int8] needs (0 for invalid arguments):
+ * num_seqs * num_q_heads * (suffix splits + prefix key splits) * (head_dim + 2) * 4, with the
+ * suffix split count of whichever of the bf16 and INT8 calls splits more (an upper bound for
+ * both). Pure host arithmetic. */
 size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                                 int head_dim, int max_context_len,
                                                 int shared_prefix_tokens, int split_chunk_tokens);

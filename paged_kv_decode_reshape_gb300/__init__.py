@@ -43,6 +43,9 @@ SIGNATURES = {
     "pkv_paged_decode_attention_shared_prefix": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                   _I, _I, _F, _I, _I, _P, _SZ, _P, _P], _I),
     "pkv_decode_shared_prefix_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
+    "pkv_paged_decode_attention_shared_prefix_int8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                                                       _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P,
+                                                       _P], _I),
     "pkv_kv_cache_copy_blocks": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
 }
 STATIC_WORKSPACE_BYTES = 32 << 20  # PKV_STATIC_WORKSPACE_BYTES
@@ -203,6 +206,22 @@ def paged_decode_attention_shared_prefix(out, q, k_pool, v_pool, block_tables, c
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream))
     _check(rc, "paged_decode_attention_shared_prefix")
+
+
+def paged_decode_attention_shared_prefix_int8(out, q, k_pool, v_pool, k_scales, v_scales,
+                                              block_tables, context_lens, max_context_len, scale,
+                                              shared_prefix_tokens, split_chunk_tokens=0,
+                                              workspace=None, status=None, stream=None):
+    """pkv_paged_decode_attention_shared_prefix_int8: the cascade decode over an INT8 cache."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    rc = load().pkv_paged_decode_attention_shared_prefix_int8(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D, BS, NB, block_tables.shape[1],
+        int(max_context_len), float(scale), int(shared_prefix_tokens), int(split_chunk_tokens),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "paged_decode_attention_shared_prefix_int8")
 
 
 def paged_decode_attention_int8(out, q, k_pool, v_pool, k_scales, v_scales, block_tables,

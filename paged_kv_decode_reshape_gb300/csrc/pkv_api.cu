@@ -164,7 +164,7 @@ pkv_status run_decode(const Decode& a) {
     const int prefix = a.prefix;
     if (prefix < 0) return PKV_ERR_INVALID_ARG;
     if (prefix > 0) {
-        if (a.kv_dtype != PKV_BF16 || a.D != 128 || a.L != 1) return PKV_ERR_UNSUPPORTED;
+        if ((a.kv_dtype != PKV_BF16 && a.kv_dtype != PKV_I8) || a.D != 128 || a.L != 1) return PKV_ERR_UNSUPPORTED;
         if (prefix % kBlockSize || prefix > a.max_ctx) return PKV_ERR_INVALID_ARG;
     }
     const int suffix_max = a.max_ctx - prefix;
@@ -223,11 +223,17 @@ pkv_status run_decode(const Decode& a) {
             !make_pool_tensor_map(&tv, a.v_pool, a.NB, a.Hkv, i8m))
             return PKV_ERR_CUDA;
         if (P > 0) {
-            CUtensorMap pk, pv;  // the prefix kernel's one-box-per-block view of the same pools
-            if (!make_pool_tensor_map_blocks(&pk, a.k_pool, a.NB, a.Hkv) ||
-                !make_pool_tensor_map_blocks(&pv, a.v_pool, a.NB, a.Hkv))
+            // the prefix kernel's one-box-per-block view of the same pools (bf16; an INT8 cache is
+            // copied row by row, no tensor map)
+            CUtensorMap pk{}, pv{};
+            if (!i8m && (!make_pool_tensor_map_blocks(&pk, a.k_pool, a.NB, a.Hkv) ||
+                         !make_pool_tensor_map_blocks(&pv, a.v_pool, a.NB, a.Hkv)))
                 return PKV_ERR_CUDA;
             PrefixParams x{};
+            if (i8m) {
+                x.k_i8 = static_cast<const int8_t*>(a.k_pool); x.v_i8 = static_cast<const int8_t*>(a.v_pool);
+                x.k_scales = a.k_scales; x.v_scales = a.v_scales;
+            }
             x.q = a.q; x.block_tables = a.block_tables; x.ws_acc = p.ws_acc; x.ws_ml = p.ws_ml;
             x.status = a.status; x.B = a.B; x.Hq = a.Hq; x.Hkv = a.Hkv; x.G = g; x.NB = a.NB;
             x.MBPS = a.MBPS; x.S = Sw; x.slot0 = S; x.prefix_tokens = prefix;
@@ -536,6 +542,21 @@ pkv_status pkv_paged_decode_attention_multi(void* out, const void* q, const void
     return run_decode(a);
 }
 
+pkv_status pkv_paged_decode_attention_shared_prefix_int8(
+    void* out, const void* q, const int8_t* k_pool, const int8_t* v_pool, const float* k_scales,
+    const float* v_scales, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    int max_blocks_per_seq, int max_context_len, float scale, int shared_prefix_tokens,
+    int split_chunk_tokens, void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+    if (shared_prefix_tokens <= 0) return PKV_ERR_INVALID_ARG;
+    Decode a{out, q, k_pool, v_pool, k_scales, v_scales, block_tables, context_lens,
+             num_seqs, 1, num_q_heads, num_kv_heads, head_dim, block_size,
+             num_blocks, max_blocks_per_seq, max_context_len, scale, PKV_BF16, PKV_I8,
+             split_chunk_tokens, workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream)};
+    a.prefix = shared_prefix_tokens;
+    return run_decode(a);
+}
+
 size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                                 int head_dim, int max_context_len,
                                                 int shared_prefix_tokens, int split_chunk_tokens) {
@@ -545,7 +566,10 @@ size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, i
         shared_prefix_tokens % kBlockSize || shared_prefix_tokens > max_context_len)
         return 0;
     const int suffix_max = max_context_len - shared_prefix_tokens;
-    const int chunk = choose_chunk(num_seqs, num_kv_heads, suffix_max, split_chunk_tokens, head_dim, PKV_BF16);
+    // the bf16 and the INT8 call: the smaller chunk (more suffix splits) covers both
+    const int cb = choose_chunk(num_seqs, num_kv_heads, suffix_max, split_chunk_tokens, head_dim, PKV_BF16);
+    const int ci = choose_chunk(num_seqs, num_kv_heads, suffix_max, split_chunk_tokens, head_dim, PKV_I8);
+    const int chunk = cb < ci ? cb : ci;
     const int S = split_extent(suffix_max, chunk);
     int P = 0, split_tokens = 0;
     prefix_splits(num_seqs, num_q_heads / num_kv_heads, num_kv_heads, shared_prefix_tokens, &P,

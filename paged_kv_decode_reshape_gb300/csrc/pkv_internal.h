@@ -177,6 +177,11 @@ struct PrefixParams {
     int S, slot0;                 // partial slots per (row, head); first prefix slot
     int prefix_tokens, split_tokens;  // both multiples of 128
     float scale_log2;
+    // INT8 cache (else null): the pools [NB][Hkv][16][128] int8 and scales [NB][Hkv][16] fp32
+    const int8_t* k_i8;
+    const int8_t* v_i8;
+    const float* k_scales;
+    const float* v_scales;
 };
 
 // Launchers (return the launch's error code).

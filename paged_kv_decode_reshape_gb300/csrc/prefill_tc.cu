@@ -872,15 +872,22 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const 
 
 cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int splits,
                           cudaStream_t s) {
-    auto kern = prefill_kernel<true, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e != cudaSuccess) return e;
     PfWork w{};
     w.q = p.q; w.block_tables = p.block_tables; w.status = p.status;
     w.Hq = p.Hq; w.Hkv = p.Hkv; w.G = p.G; w.NB = p.NB; w.MBPS = p.MBPS; w.scale_log2 = p.scale_log2;
     w.ws_acc = p.ws_acc; w.ws_ml = p.ws_ml; w.B = p.B; w.S = p.S; w.slot0 = p.slot0;
     w.prefix_tokens = p.prefix_tokens; w.split_tokens = p.split_tokens;
+    w.k_i8 = p.k_i8; w.v_i8 = p.v_i8; w.k_scales = p.k_scales; w.v_scales = p.v_scales;
     const dim3 grid((p.B * p.G + kPfQ - 1) / kPfQ, p.Hkv, splits);
+    if (p.k_i8) {
+        auto kern = prefill_kernel<true, true>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemI8);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, grid, dim3(kPfThreadsI8), kPfSmemI8, s, w, tk, tv);
+    }
+    auto kern = prefill_kernel<true, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
 }
 

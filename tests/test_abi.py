@@ -82,9 +82,9 @@ def test_workspace_arithmetic(pkv):
     assert L.pkv_decode_split_chunk(4, 4, 64, 100, 0, 7) == 0            # unknown dtype
     # shared-prefix decode: suffix splits (auto chunk over the longest suffix) + prefix key splits
     # (about 64 CTAs over (row tile of 128, kv head, split); whole 128-key tiles).
-    # 256 seqs x 32/8 heads, prefix 2048 of max 4090: suffix chunk 1024 -> 1 split; 8 row tiles
-    # x 8 kv heads = 64 -> 1 prefix split; 2 slots x 130 floats
-    assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 128, 4090, 2048, 0) == 256 * 32 * 2 * 130 * 4
+    # 256 seqs x 32/8 heads, prefix 2048 of max 4090: suffix chunk 2048 (bf16) or 512 (INT8, the
+    # bound) -> 3 splits; 8 row tiles x 8 kv heads = 64 -> 1 prefix split; 4 slots x 130 floats
+    assert L.pkv_decode_shared_prefix_workspace_bytes(256, 32, 8, 128, 4090, 2048, 0) == 256 * 32 * 4 * 130 * 4
     # 8 seqs: suffix chunk 256 -> 2042 // 256 = 7 splits; 1 row tile x 8 kv heads -> 8 prefix
     # splits of 256 tokens; 15 slots
     assert L.pkv_decode_shared_prefix_workspace_bytes(8, 32, 8, 128, 4090, 2048, 0) == 8 * 32 * 15 * 130 * 4

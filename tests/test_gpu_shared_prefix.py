@@ -103,3 +103,61 @@ def test_shared_prefix_argument_errors():
                                                d.context_lens, w.max_context_len, w.scale, 128,
                                                0, ws[:256])
     assert e.value.status == P.ERR_WORKSPACE
+
+
+def _int8_shared_prefix(B, prefix, lo, hi, Hq, Hkv, seed):
+    rng = np.random.default_rng(seed)
+    lens = prefix + rng.integers(lo, hi + 1, size=B)
+    return W.make_decode(name="casc_i8", B=B, Hq=Hq, Hkv=Hkv, D=128, context_lens=lens, kv_dtype="i8",
+                         q_dtype="bf16", seed=seed, shared_prefix_tokens=prefix)
+
+
+def cascade_i8(d: DevWorkload, prefix, chunk=0, status=None):
+    w = d.w
+    maxc = w.max_context_len
+    nbytes = P.decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, prefix, chunk)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(d.q.shape, dtype=d.q.dtype, device="cuda")
+    P.paged_decode_attention_shared_prefix_int8(out, d.q, d.k_pool, d.v_pool, d.k_scales, d.v_scales,
+                                                d.block_tables, d.context_lens, maxc, w.scale, prefix,
+                                                chunk, ws, status)
+    return out
+
+
+@pytest.mark.parametrize("B,prefix,lo,hi,Hq,Hkv", [(12, 512, 1, 500, 64, 8), (40, 2048, 1, 200, 64, 8),
+                                                   (7, 144, 1, 300, 32, 8), (9, 256, 1, 400, 16, 1),
+                                                   (3, 16, 1, 40, 8, 4)])
+def test_shared_prefix_int8_matches_oracle(B, prefix, lo, hi, Hq, Hkv):
+    """The cascade over an INT8 cache: the prefix through the INT8 prefill kernel's machinery, the
+    suffixes through the INT8 split-K kernel, one merge; against the INT8 oracle and close to the
+    plain INT8 decode call."""
+    w = _int8_shared_prefix(B, prefix, lo, hi, Hq, Hkv, seed=B * 7 + prefix)
+    d = DevWorkload(w)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = to_f64(cascade_i8(d, prefix, status=st))
+    assert int(st.item()) == 0
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                        w.scale, w.k_scales, w.v_scales)
+    assert_close(got, ref, "i8", f"INT8 cascade B={B} prefix={prefix} G={Hq // Hkv}")
+    plain = to_f64(d.attend())
+    assert np.abs(got - plain).max() <= 5e-2
+
+
+def test_shared_prefix_int8_empty_suffix_and_bad_prefix():
+    w = _int8_shared_prefix(6, 384, 1, 300, 64, 8, seed=5)
+    lens = w.context_lens.copy()
+    lens[0] = 384        # the whole context is the prefix
+    lens[3] = 385        # one private token
+    w.context_lens = lens.astype(np.int32)
+    d = DevWorkload(w)
+    got = to_f64(cascade_i8(d, 384))
+    ref = oracle.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                        w.scale, w.k_scales, w.v_scales)
+    assert_close(got, ref, "i8", "INT8 cascade with empty suffix")
+    bt = w.block_tables.copy()
+    bt[2, 3] = int(bt[2, 24])  # a private block of sequence 2 swapped into its prefix
+    w.block_tables = bt
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cascade_i8(DevWorkload(w), 384, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & P.FLAG_BAD_PREFIX
