@@ -12,13 +12,14 @@
 // prefix every sequence shares, and it writes partial states (m, l, acc) for the merge kernel.
 //
 // One CTA computes 128 query rows of one query head against 128-key tiles. Both products read
-// their A operand from tensor memory (a tcgen05.mma with M = N = 128, K = 16 takes 64 cycles on
-// GB300 with A in TMEM or in shared memory alike; A in TMEM spares shared-memory room and
-// bandwidth for the K/V rings). TMEM columns:
+// their A operand from tensor memory: a tcgen05.mma with M = N = 128, K = 16 takes 64 cycles and
+// reads its B operand from shared memory at 64 B a cycle; an A operand from shared memory would
+// double that, to the whole shared-memory bandwidth, and the TMA copies into the rings would then
+// slow the products (measured: Q in shared memory, 4 % slower). TMEM columns:
 //   O   0-127     fp32 accumulator, row r in lane r
 //   Q   128-191   the CTA's 128 query rows, two bf16 dims per column (written once)
-//   P   192-255 (buffer 0), 256-319 (buffer 1): bf16 weights of a key tile, two keys per column
-//   S   320-447   S = Q . K^T of one key tile, fp32
+//   P   192-255   bf16 weights of a key tile, two keys per column
+//   S   256-383 (buffer 0), 384-511 (buffer 1): S = Q . K^T of a key tile, fp32
 // Warp roles (384 threads with the default two softmax threads per row):
 //   warps 0-7  softmax. Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows); warps 0-3 take
 //              keys 0-63 of every tile, warps 4-7 keys 64-127. Per tile the two warps of a lane
@@ -33,14 +34,14 @@
 //              K slot is free once S of its tile is done, so K runs well ahead of V. (Measured on
 //              GB300: an SM takes in ~53 GB/s of 2 KB TMA boxes but ~82 GB/s of 4 KB ones, so
 //              one box per block rather than one per 64-dim half.)
-// Per key tile t the MMA thread issues S(t+1) = Q . K(t+1)^T as soon as the softmax has read S(t)
-// (s_free), and O += P(t) . V(t) once P(t) is written into P buffer t % 2 (p_full). The softmax
-// writes P(t) once the product that last read that buffer, PV(t-2), is done (pv_done). So S(t+1)
-// is computed while the softmax works on tile t, and the softmax never waits for a PV unless it
-// must rescale O. P has one barrier per buffer, so no barrier completes a phase its waiter has
-// not yet seen (a parity wait would miss it). The running max is raised lazily (only
-// when a tile exceeds it by more than 2^8), so O is rarely rescaled; at the end each row is
-// divided by its sum.
+// Per key tile t the S issuer computes S(t) = Q . K(t)^T into S buffer t % 2 as soon as K(t) has
+// landed and the softmax has read S(t-2) from that buffer (s_free), so it runs up to two tiles
+// ahead of the softmax; the PV issuer computes O += P(t) . V(t) once P(t) is written (p_full).
+// The softmax writes P(t) once PV(t-1), the product that last read P, is done (pv_done); PV(t-1)
+// was issued when the softmax finished tile t-1, so it has usually completed by then. S has one
+// barrier per buffer, so no barrier completes a phase its waiter has not yet seen (a parity wait
+// would miss it). The running max is raised lazily (only when a tile exceeds it by more than
+// 2^8), so O is rarely rescaled; at the end each row is divided by its sum.
 #include <cuda.h>
 
 #include "pkv_device.cuh"
@@ -57,12 +58,6 @@ constexpr int kPfK = 128;                      // keys per tile (MMA N of S, K o
 // at (k / 8) * 2 KB + (k % 8) * 128 (+ 1 KB for dims 64-127), a uniform stride for both products.
 constexpr int kPfBlockBytes = kBlockSize * 256;  // one block's keys, both halves
 constexpr int kPfStage = 8 * kPfBlockBytes;     // one K (or V) tile
-#ifndef PKV_PF_STAGES
-#define PKV_PF_STAGES 3                        // slots per ring (K and V each)
-#endif
-constexpr int kPfStages = PKV_PF_STAGES;
-constexpr int kPfOffK = 0;
-constexpr int kPfOffV = kPfStages * kPfStage;
 // Softmax threads per query row (a build-time tunable): each takes 128 / kPfSplit keys of every
 // tile and 128 / kPfSplit dims of the row's output. The kPfSplit warps sharing a TMEM lane quadrant
 // (w, w + 4, ...) form one barrier group. Measured on GB300 (the 4 x 4096-token prefill): 2 threads
@@ -77,35 +72,62 @@ constexpr int kPfDimsPer = 128 / kPfSplit;          // output dims per thread
 constexpr int kPfSoftWarps = 4 * kPfSplit;
 constexpr int kPfSoftThreads = 32 * kPfSoftWarps;
 constexpr int kPfGroup = 32 * kPfSplit;             // threads of one barrier group
-constexpr int kPfOffX = 2 * kPfStages * kPfStage;   // row maxima [2][kPfSplit][128], sums [kPfSplit][128]
-constexpr int kPfOffBar = kPfOffX + 3 * kPfSplit * kPfQ * 4;
-// barriers: full[2 rings][S], empty[2 rings][S], s_full, s_free, p_full[2], pv_done[2], o_done,
-// drain[2]; then the TMEM slot
-constexpr int kPfNumBars = 4 * kPfStages + 9;
-constexpr int kPfSmem = 1024 + kPfOffBar + kPfNumBars * 8 + 16;
 constexpr int kPfThreads = kPfSoftThreads + 128;
 // INT8 cache: the producers copy each block's int8 K (or V) rows (2 KB) into the second half of the
-// tile's slot and its 16 scales into a row of the scale area, completing on staged[ring][slot]; four
+// tile's slot and its 16 scales into a row of the scale area, completing on staged[ring slot]; four
 // converter warps (two per ring) widen them in place into the bf16 layout above and then complete
-// full[ring][slot] for the MMA issuers, as the tensor copies do for a bf16 cache.
+// full[ring slot] for the MMA issuers, as the tensor copies do for a bf16 cache.
 constexpr int kPfConvWarp0 = kPfSoftWarps + 4;       // warps 12-13: K ring, 14-15: V ring
 constexpr int kPfConvThreads = 64;                   // per ring
 constexpr int kPfI8Half = kPfStage / 2;              // int8 rows of a tile start here in the slot
-constexpr int kPfOffStaged = kPfOffBar + kPfNumBars * 8 + 16;   // after the TMEM slot
-constexpr int kPfOffScl = (kPfOffStaged + 2 * kPfStages * 8 + 15) / 16 * 16;  // [2 rings][S][8 blocks][16] fp32
-constexpr int kPfSmemI8 = 1024 + kPfOffScl + 2 * kPfStages * 8 * kBlockSize * 4;
 constexpr int kPfThreadsI8 = kPfThreads + 32 * 4;
-template <bool kI8> constexpr int pf_threads() { return kI8 ? kPfThreadsI8 : kPfThreads; }
-template <bool kI8> constexpr int pf_smem() { return kI8 ? kPfSmemI8 : kPfSmem; }
-static_assert(kPfSmemI8 <= 227 * 1024, "shared memory (INT8)");
-static_assert(kPfOffScl % 16 == 0, "scale rows are bulk-copy targets");
+
+// Ring depths, buffering and shared-memory layout of the bf16 (kI8 false) and INT8 kernels.
+//  - bf16: two S buffers, so the S products run up to two tiles ahead of the softmax, and one P
+//    buffer (TMEM has room for one more 128-column buffer, not for both). K 3 slots, V 2: measured
+//    on GB300 (the 4 x 4096-token prefill) 1210-1220 TFLOP/s, against 1162 with V 3 slots and
+//    1137 with one S and two P buffers.
+//  - INT8: the converters bound the kernel and a PV waits for its V conversion, so the softmax
+//    keeps two P buffers (it need not wait for PV(t-1) before writing P(t)) and S one buffer.
+#ifndef PKV_PF_STAGES_K
+#define PKV_PF_STAGES_K 3
+#endif
+#ifndef PKV_PF_STAGES_V
+#define PKV_PF_STAGES_V 2
+#endif
+template <bool kI8>
+struct PfGeom {
+    static constexpr int SK = kI8 ? 3 : PKV_PF_STAGES_K;  // K ring slots
+    static constexpr int SV = kI8 ? 3 : PKV_PF_STAGES_V;  // V ring slots
+    static constexpr int R = SK + SV;
+    static constexpr int SBufs = kI8 ? 1 : 2;             // S buffers (128 TMEM columns each)
+    static constexpr int PBufs = kI8 ? 2 : 1;             // P buffers (64 columns each)
+    static constexpr int OffV = SK * kPfStage;
+    static constexpr int OffX = R * kPfStage;             // row maxima [2][kPfSplit][128], sums [kPfSplit][128]
+    static constexpr int OffBar = OffX + 3 * kPfSplit * kPfQ * 4;
+    // barriers: full[ring slots], empty[ring slots] (K slots, then V slots), s_full[2], s_free[2],
+    // p_full[2], pv_done[2], o_done, drain[2]; then the TMEM slot
+    static constexpr int NumBars = 2 * R + 11;
+    static constexpr int OffStaged = OffBar + NumBars * 8 + 16;              // INT8: after the TMEM slot
+    static constexpr int OffScl = (OffStaged + R * 8 + 15) / 16 * 16;        // INT8: [ring slot][8 blocks][16] fp32
+    static constexpr int Smem = kI8 ? 1024 + OffScl + R * 8 * kBlockSize * 4 : 1024 + OffBar + NumBars * 8 + 16;
+    static constexpr int Threads = kI8 ? kPfThreadsI8 : kPfThreads;
+    // TMEM columns: O 0-127, Q 128-191, then the P buffers (64 each), then the S buffers (128 each)
+    static constexpr uint32_t PCol = 192, SCol = PCol + 64 * PBufs;
+    static_assert(SK >= 2 && SV >= 2, "a slot loads while the other is read");
+    static_assert(Smem <= 227 * 1024, "shared memory");
+    static_assert(OffScl % 16 == 0, "scale rows are bulk-copy targets");
+    static_assert(SCol + 128 * SBufs <= 512, "TMEM columns");
+};
+constexpr int kPfOffK = 0;
 constexpr int kPfMmaWarp = kPfSoftWarps, kPfLoadWarpK = kPfSoftWarps + 1, kPfLoadWarpV = kPfSoftWarps + 2,
               kPfMmaWarpPV = kPfSoftWarps + 3;
 constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kOCol = 0, kQCol = 128, kPCol = 192, kSCol = 320;
+// named barriers: 1-4 the softmax warps of a TMEM lane quadrant, 5-6 the INT8 converters of a
+// ring, 7 Q written (the softmax warps and the S issuer's warp)
+constexpr int kPfQBar = 7;
+constexpr uint32_t kOCol = 0, kQCol = 128;
 constexpr float kPfRescale = 8.0f;             // log2 units
-static_assert(kPfSmem <= 227 * 1024, "shared memory");
-static_assert(kPfStages >= 3, "S of tile t + 2 is computed while tile t still holds its stage");
 
 // What one launch computes, filled by launch_prefill (kPrefix false) or launch_prefix (true).
 struct PfWork {
@@ -145,7 +167,7 @@ __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint64_t scale2, uint
 }
 
 template <bool kPrefix, bool kI8>
-__global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfWork p,
+__global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const PfWork p,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
     grid_dependency_wait();
@@ -199,36 +221,63 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sbase = smem_addr(smem);
-    float* xmax = reinterpret_cast<float*>(smem + kPfOffX);  // [2 buffers][kPfSplit parts][128 rows]
+    float* xmax = reinterpret_cast<float*>(smem + PfGeom<kI8>::OffX);  // [2 buffers][kPfSplit parts][128 rows]
     float* xsum = xmax + 2 * kPfSplit * kPfQ;                // [kPfSplit parts][128 rows]
-    const uint32_t bar0 = sbase + kPfOffBar;
-    // ring g (0: K, 1: V): slot s of tile t is t % S
-    auto full = [&](int g, int s) { return bar0 + 8 * (g * kPfStages + s); };
-    auto empty = [&](int g, int s) { return bar0 + 8 * (2 * kPfStages + g * kPfStages + s); };
-    auto slot = [&](int g, int t) { return sbase + (g ? kPfOffV : kPfOffK) + (t % kPfStages) * kPfStage; };
-    const uint32_t s_full = bar0 + 8 * (4 * kPfStages);
-    const uint32_t s_free = bar0 + 8 * (4 * kPfStages + 1);
-    auto p_full = [&](int u) { return bar0 + 8 * (4 * kPfStages + 2 + u); };
-    auto pv_done = [&](int u) { return bar0 + 8 * (4 * kPfStages + 4 + u); };
-    const uint32_t o_done = bar0 + 8 * (4 * kPfStages + 6);
-    auto drain = [&](int x) { return bar0 + 8 * (4 * kPfStages + 7 + x); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPfOffBar + kPfNumBars * 8);
+    using Gm = PfGeom<kI8>;
+    const uint32_t bar0 = sbase + Gm::OffBar;
+    // ring g (0: K, 1: V) has nst(g) slots; tile t uses slot t % nst(g), ring slot ridx(g, s)
+    auto nst = [](int g) { return g ? Gm::SV : Gm::SK; };
+    auto ridx = [](int g, int s) { return g ? Gm::SK + s : s; };
+    auto full = [&](int g, int s) { return bar0 + 8 * ridx(g, s); };
+    auto empty = [&](int g, int s) { return bar0 + 8 * (Gm::R + ridx(g, s)); };
+    auto slot = [&](int g, int t) { return sbase + (g ? Gm::OffV : kPfOffK) + (t % nst(g)) * kPfStage; };
+    const uint32_t bar1 = bar0 + 8 * (2 * Gm::R);
+    auto s_full = [&](int u) { return bar1 + 8 * u; };
+    auto s_free = [&](int u) { return bar1 + 8 * (2 + u); };
+    auto p_full = [&](int u) { return bar1 + 8 * (4 + u); };
+    auto pv_done = [&](int u) { return bar1 + 8 * (6 + u); };
+    const uint32_t o_done = bar1 + 8 * 8;
+    auto drain = [&](int x) { return bar1 + 8 * (9 + x); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::OffBar + Gm::NumBars * 8);
     // INT8: the int8 rows of ring g's slot s have landed (the producer's copies)
-    auto staged = [&](int g, int s) { return sbase + kPfOffStaged + 8 * (g * kPfStages + s); };
-    auto scl = [&](int g, int s) { return sbase + kPfOffScl + (g * kPfStages + s) * 8 * kBlockSize * 4; };
+    auto staged = [&](int g, int s) { return sbase + Gm::OffStaged + 8 * ridx(g, s); };
+    auto scl = [&](int g, int s) { return sbase + Gm::OffScl + ridx(g, s) * 8 * kBlockSize * 4; };
     __shared__ int abort_flag;
+
+    // softmax thread (hf, r): row r, keys kPfKeysPer hf .. of each tile, output dims kPfDimsPer hf ..
+    const int hf = (warp >> 2) & (kPfSplit - 1);
+    const int r = tid & 127;
+    const int i = qt * kPfQ + r;
+    const bool row_valid = i < L;
+    // the (token, head) row of q / out: prefill query token q0 + i of head h; shared prefix: the
+    // (sequence i / G, head kvh * G + i % G) pair
+    const size_t qrow = !kPrefix ? (size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h
+                                 : (row_valid ? (size_t)(i / p.G) * p.Hq + kvh * p.G + i % p.G : 0);
+    const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
+    // Q row r, dims kPfDimsPer hf .. (zeros past the rows): loaded before the set-up below so that
+    // its latency overlaps it
+    uint32_t qw[kPfDimsPer / 2];
+    if (warp < kPfSoftWarps) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                          qrow * 128 + kPfDimsPer * hf);
+#pragma unroll
+        for (int c = 0; c < kPfDimsPer / 8; ++c) {
+            const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+            qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
+        }
+    }
 
     if (tid == 0) {
         for (int g = 0; g < 2; ++g)
-            for (int s = 0; s < kPfStages; ++s) {
+            for (int s = 0; s < nst(g); ++s) {
                 mbar_init(full(g, s), kI8 ? kPfConvThreads : 1);
                 // INT8 K slot: its scale row is read by the softmax warps after S is done
                 mbar_init(empty(g, s), kI8 && g == 0 ? 1 + kPfSoftWarps : 1);
                 if constexpr (kI8) mbar_init(staged(g, s), 1);
             }
-        mbar_init(s_full, 1);
-        mbar_init(s_free, kPfSoftThreads);
         for (int u = 0; u < 2; ++u) {
+            mbar_init(s_full(u), 1);
+            mbar_init(s_free(u), kPfSoftThreads);
             mbar_init(p_full(u), kPfSoftThreads);
             mbar_init(pv_done(u), 1);
         }
@@ -249,32 +298,23 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // softmax thread (hf, r): row r, keys kPfKeysPer hf .. of each tile, output dims kPfDimsPer hf ..
-    const int hf = (warp >> 2) & (kPfSplit - 1);
-    const int r = tid & 127;
-    const int i = qt * kPfQ + r;
-    const bool row_valid = i < L;
-    // the (token, head) row of q / out: prefill query token q0 + i of head h; shared prefix: the
-    // (sequence i / G, head kvh * G + i % G) pair
-    const size_t qrow = !kPrefix ? (size_t)(q0 + (row_valid ? i : 0)) * p.Hq + h
-                                 : (row_valid ? (size_t)(i / p.G) * p.Hq + kvh * p.G + i % p.G : 0);
-    const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quadrant
-    if (warp < kPfSoftWarps) {
-        // Q row r, dims kPfDimsPer hf .., into TMEM columns 128 + kPfDimsPer / 2 hf .. (two bf16
-        // per column; zeros past the rows)
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          qrow * 128 + kPfDimsPer * hf);
-        uint32_t qw[kPfDimsPer / 2];
-#pragma unroll
-        for (int c = 0; c < kPfDimsPer / 8; ++c) {
-            const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-            qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
-        }
+    // Q into TMEM columns 128 + kPfDimsPer / 2 hf .. (two bf16 per column). For a bf16 cache only
+    // the S issuer waits for it (named barrier kPfQBar) and the producers start their copies at
+    // once (measured: 7 % faster than a CTA-wide barrier). For an INT8 cache the CTA-wide barrier
+    // stays: producers and converters started before Q was written made that kernel 7 % slower.
+    if constexpr (kI8) {
+        if (warp < kPfSoftWarps) tmem_st_words(tmem + tl + kQCol + kPfDimsPer / 2 * hf, qw);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    } else if (warp < kPfSoftWarps) {
         tmem_st_words(tmem + tl + kQCol + kPfDimsPer / 2 * hf, qw);
+        tc_fence_before();
+        named_barrier_arrive(kPfQBar, kPfSoftThreads + 32);
+    } else if (warp == kPfMmaWarp) {
+        named_barrier_sync(kPfQBar, kPfSoftThreads + 32);
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
 
     if (warp == kPfLoadWarpK || warp == kPfLoadWarpV) {
         // ---------------- producers: ring g = K (warp 9) or V (warp 10) ----------------
@@ -283,12 +323,12 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
         int issued = 0;
         int ids_cur = load_window(0, true), ids_next = has_window(1) ? load_window(1, true) : -1;
         for (int t = 0; t < ntiles; ++t) {
-            const int st = t % kPfStages;
+            const int ns = nst(g), st = t % ns;
             if (t > 0 && (t & 3) == 0) {
                 ids_cur = ids_next;
                 ids_next = has_window((t >> 2) + 1) ? load_window((t >> 2) + 1, true) : -1;
             }
-            const bool got = t < kPfStages || mbar_wait_bounded(empty(g, st), ((t / kPfStages) - 1) & 1);
+            const bool got = t < ns || mbar_wait_bounded(empty(g, st), ((t / ns) - 1) & 1);
             if (!__all_sync(0xffffffffu, got)) {  // warp-uniform exit
                 if (lane == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
                 break;
@@ -322,8 +362,9 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
         }
         if (aborted(&abort_flag) && lane == 0) {
             // let this CTA's own copies land before shared memory goes away
-            for (int t = issued - kPfStages < 0 ? 0 : issued - kPfStages; t < issued; ++t)
-                mbar_wait_bounded(kI8 ? staged(g, t % kPfStages) : full(g, t % kPfStages), (t / kPfStages) & 1);
+            const int ns = nst(g);
+            for (int t = issued - ns < 0 ? 0 : issued - ns; t < issued; ++t)
+                mbar_wait_bounded(kI8 ? staged(g, t % ns) : full(g, t % ns), (t / ns) & 1);
         }
     } else if (kI8 && warp >= kPfConvWarp0) {
         // ---------------- INT8: converters of ring g (warps 12-13: K, 14-15: V) ----------------
@@ -335,9 +376,10 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
         const int g = (warp - kPfConvWarp0) >> 1;
         const int c = tid - 32 * (kPfConvWarp0 + 2 * g);
         const int bar_id = 5 + g;  // named barrier of the ring's kPfConvThreads threads
+        const int ns = nst(g);
         for (int t = 0; t < ntiles; ++t) {
-            const int st = t % kPfStages;
-            const bool got = mbar_wait_bounded(staged(g, st), (t / kPfStages) & 1);
+            const int st = t % ns;
+            const bool got = mbar_wait_bounded(staged(g, st), (t / ns) & 1);
             if (!got && lane_of() == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
             if (barrier_or(bar_id, kPfConvThreads, !got || aborted(&abort_flag))) break;
             uint4 in[2][8];
@@ -345,11 +387,11 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int key = c + 64 * kk, blk = key >> 4, kin = key & 15;
-                const uint4* row = reinterpret_cast<const uint4*>(smem + (g ? kPfOffV : kPfOffK) + st * kPfStage +
+                const uint4* row = reinterpret_cast<const uint4*>(smem + (g ? Gm::OffV : kPfOffK) + st * kPfStage +
                                                                    kPfI8Half + blk * (kPfBlockBytes / 2) + kin * 128);
 #pragma unroll
                 for (int v = 0; v < 8; ++v) in[kk][v] = row[(v + lane) & 7];  // rotated: no bank conflicts
-                sc[kk] = reinterpret_cast<const float*>(smem + kPfOffScl)[((g * kPfStages + st) * 8 + blk) * kBlockSize + kin];
+                sc[kk] = reinterpret_cast<const float*>(smem + Gm::OffScl)[(ridx(g, st) * 8 + blk) * kBlockSize + kin];
             }
             named_barrier_sync(bar_id, kPfConvThreads);
 #pragma unroll
@@ -358,7 +400,7 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                 // K: the codes themselves (exact in bf16); the softmax multiplies each score by its
                 // key's scale in fp32. V: code * scale rounded to bf16.
                 const uint64_t s2 = g ? f32x2(sc[kk], sc[kk]) : f32x2(1.f, 1.f);
-                unsigned char* base = smem + (g ? kPfOffV : kPfOffK) + st * kPfStage + blk * kPfBlockBytes +
+                unsigned char* base = smem + (g ? Gm::OffV : kPfOffK) + st * kPfStage + blk * kPfBlockBytes +
                                       (kin >> 3) * 2048 + (kin & 7) * 128;
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
@@ -383,28 +425,28 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
             const bool is_s = warp == kPfMmaWarp;
             constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
             constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
-            auto issue_s = [&](int t) {  // S(t) = Q . K(t)^T
+            auto issue_s = [&](int t) {  // S(t) = Q . K(t)^T into S buffer t % SBufs
                 const uint32_t kbase = slot(0, t);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     // K-major: 8-key groups 2 KB apart, dims 16 ks.. in half ks / 4 at 32 B (ks % 4)
                     const uint64_t bd = sdesc(kbase + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048);
-                    umma_ts(tmem + kSCol, tmem + kQCol + 8 * ks, bd, kIdescS, ks > 0);
+                    umma_ts(tmem + Gm::SCol + 128 * (t % Gm::SBufs), tmem + kQCol + 8 * ks, bd, kIdescS, ks > 0);
                 }
-                umma_commit(s_full);
-                umma_commit(empty(0, t % kPfStages));  // the K slot is free once S(t) is done
+                umma_commit(s_full(t % Gm::SBufs));
+                umma_commit(empty(0, t % Gm::SK));  // the K slot is free once S(t) is done
             };
-            auto issue_pv = [&](int t) {  // O += P(t) . V(t), P(t) in buffer t % 2
+            auto issue_pv = [&](int t) {  // O += P(t) . V(t), P(t) in buffer t % PBufs
                 const uint32_t vbase = slot(1, t);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     // MN-major: keys 16 kk.. are block kk; 8-key groups 2 KB apart, dims 64.. 1 KB on
                     const uint64_t bd = sdesc(vbase + kk * kPfBlockBytes, 1024, 2048);
-                    umma_ts(tmem + kOCol, tmem + kPCol + 64 * (t & 1) + 8 * kk, bd, kIdescO,
+                    umma_ts(tmem + kOCol, tmem + Gm::PCol + 64 * (t % Gm::PBufs) + 8 * kk, bd, kIdescO,
                             (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(pv_done(t & 1));
-                umma_commit(empty(1, t % kPfStages));  // the V slot is free once PV(t) is done
+                umma_commit(empty(1, t % Gm::SV));  // the V slot is free once PV(t) is done
             };
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t par) {
@@ -418,16 +460,17 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                 return ok;
             };
             if (is_s) {
-                if (wait(full(0, 0), 0)) issue_s(0);
-                for (int t = 0; t + 1 < ntiles && ok; ++t) {  // S is free once the softmax has read S(t)
-                    if (!wait(s_free, t & 1)) break;
-                    if (!wait(full(0, (t + 1) % kPfStages), ((t + 1) / kPfStages) & 1)) break;
-                    issue_s(t + 1);
+                // S buffer t % SBufs is free once the softmax has read S(t - SBufs) from it
+                for (int t = 0; t < ntiles && ok; ++t) {
+                    const int tf = t - Gm::SBufs;
+                    if (tf >= 0 && !wait(s_free(tf % Gm::SBufs), (tf / Gm::SBufs) & 1)) break;
+                    if (!wait(full(0, t % Gm::SK), (t / Gm::SK) & 1)) break;
+                    issue_s(t);
                 }
             } else {
                 for (int t = 0; t < ntiles && ok; ++t) {
                     if (!wait(p_full(t & 1), (t >> 1) & 1)) break;
-                    if (!wait(full(1, t % kPfStages), (t / kPfStages) & 1)) break;
+                    if (!wait(full(1, t % Gm::SV), (t / Gm::SV) & 1)) break;
                     issue_pv(t);
                 }
                 umma_commit(o_done);
@@ -439,8 +482,9 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
         __syncwarp();
     } else {
         // ---------------- softmax: row r, key half hf ----------------
-        const uint32_t s_col = tmem + tl + kSCol + kPfKeysPer * hf, o_col = tmem + tl + kOCol + kPfDimsPer * hf;
-        const uint32_t p_col = tmem + tl + kPCol + kPfKeysPer / 2 * hf;  // + 64 (t % 2)
+        // + 128 (t % SBufs), + 64 (t % PBufs)
+        const uint32_t s_col = tmem + tl + Gm::SCol + kPfKeysPer * hf, o_col = tmem + tl + kOCol + kPfDimsPer * hf;
+        const uint32_t p_col = tmem + tl + Gm::PCol + kPfKeysPer / 2 * hf;
         // keys (relative to the CTA's first key) this row sees
         const int n_row = !row_valid ? 0 : (kPrefix ? n_tile_max : first_visible + i);
         const int pair_bar = 1 + (warp & 3);  // named barrier of warps w, w + 4, ... (kPfGroup threads)
@@ -463,8 +507,9 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
             constexpr int kMyBlocks = kPfKeysPer / kBlockSize;           // blocks of this thread's keys
             constexpr int kAllMine = (1 << kMyBlocks) - 1;
             const int mask = (mask8 >> (kMyBlocks * hf)) & kAllMine;
-            const int u = t & 1;
-            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(s_full, t & 1));
+            const int u = t & 1;                                       // row-maxima buffer
+            const int su = t % Gm::SBufs, pu = t % Gm::PBufs;          // S and P buffers
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(su), (t / Gm::SBufs) & 1));
             if (!got) {
                 atomicExch(&abort_flag, 1);
                 flag(p.status, PKV_FLAG_TIMEOUT);
@@ -480,11 +525,11 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                 constexpr int kPieceB = 2 * 128 / kPieces;          // bytes of a piece
                 const int k = tid / kPieces, half = (tid % kPieces) / (kPieces / 2);
                 const int piece = tid % (kPieces / 2);
-                if (!mbar_wait_bounded(full(1, t % kPfStages), (t / kPfStages) & 1)) {
+                if (!mbar_wait_bounded(full(1, t % Gm::SV), (t / Gm::SV) & 1)) {
                     atomicExch(&abort_flag, 1);
                     flag(p.status, PKV_FLAG_TIMEOUT);
                 } else if (t * kPfK + k >= n_tile_max || !((mask8 >> (k >> 4)) & 1)) {
-                    uint4* z = reinterpret_cast<uint4*>(smem + kPfOffV + (t % kPfStages) * kPfStage +
+                    uint4* z = reinterpret_cast<uint4*>(smem + Gm::OffV + (t % Gm::SV) * kPfStage +
                                                         (k >> 4) * kPfBlockBytes + ((k >> 3) & 1) * 2048 +
                                                         half * 1024 + (k & 7) * 128 + piece * kPieceB);
 #pragma unroll
@@ -493,12 +538,12 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                 }
             }
             float s[kPfKeysPer];
-            tmem_ld_words(s_col, s);  // (reading TMEM is harmless even when S(t) never came)
+            tmem_ld_words(s_col + 128 * su, s);  // (reading TMEM is harmless even when S(t) never came)
             if constexpr (kI8) {
                 // S holds q . codes: times each key's K scale (the staged scale row of the K slot,
                 // keys in tile order), then the slot may be refilled
-                const float4* ks4 = reinterpret_cast<const float4*>(smem + kPfOffScl) +
-                                    ((t % kPfStages) * 8 * kBlockSize + kPfKeysPer * hf) / 4;
+                const float4* ks4 = reinterpret_cast<const float4*>(smem + Gm::OffScl) +
+                                    ((t % Gm::SK) * 8 * kBlockSize + kPfKeysPer * hf) / 4;
 #pragma unroll
                 for (int c = 0; c < kPfKeysPer / 4; ++c) {
                     const float4 k4 = ks4[c];
@@ -509,10 +554,10 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                     s[4 * c + 2] = a; s[4 * c + 3] = b2;
                 }
                 __syncwarp();
-                if (lane_of() == 0) mbar_arrive(empty(0, t % kPfStages));
+                if (lane_of() == 0) mbar_arrive(empty(0, t % Gm::SK));
             }
             tc_fence_before();
-            mbar_arrive(s_free);  // S(t + 1) may now be written
+            mbar_arrive(s_free(su));  // S(t + SBufs) may now be written into this buffer
             // raw scores here; the scale (with log2 e) is applied inside each exponent below
             const int kbase = t * kPfK + kPfKeysPer * hf;
             if (neg || !(kbase + kPfKeysPer <= n_row && mask == kAllMine)) {  // not all of them visible
@@ -580,9 +625,9 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                 f32x2_split(ls2[1], o0, o1);
                 l += (e0 + o0) + (e1 + o1);
             }
-            // P buffer u is free once PV(t - 2) is done; O may be rescaled once PV(t - 1) is done
+            // P buffer pu is free once PV(t - PBufs) is done; O may be rescaled once PV(t - 1) is done
             const bool resc = t > 0 && __any_sync(0xffffffffu, up);
-            const int wt = resc ? t - 1 : t - 2;  // the tile whose product must be complete
+            const int wt = resc ? t - 1 : t - Gm::PBufs;  // the tile whose product must be complete
             if (wt >= 0) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done(wt & 1), (wt >> 1) & 1))) {
                     atomicExch(&abort_flag, 1);
@@ -600,7 +645,7 @@ __global__ void __launch_bounds__(pf_threads<kI8>(), 1) prefill_kernel(const PfW
                     tmem_st32(o_col + c0, o);
                 }
             }
-            tmem_st_words(p_col + 64 * u, pw);
+            tmem_st_words(p_col + 64 * pu, pw);
             tc_fence_before();
             mbar_arrive(p_full(u));
         }
@@ -673,14 +718,14 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const 
     const dim3 grid((max_query_len + kPfQ - 1) / kPfQ, p.Hq, p.B);
     if (p.k_i8) {
         auto kern = prefill_kernel<false, true>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemI8);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PfGeom<true>::Smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(kern, grid, dim3(kPfThreadsI8), kPfSmemI8, s, w, tk, tv);
+        return launch_pdl(kern, grid, dim3(PfGeom<true>::Threads), PfGeom<true>::Smem, s, w, tk, tv);
     }
     auto kern = prefill_kernel<false, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PfGeom<false>::Smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
+    return launch_pdl(kern, grid, dim3(PfGeom<false>::Threads), PfGeom<false>::Smem, s, w, tk, tv);
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int splits,
@@ -694,14 +739,14 @@ cudaError_t launch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CU
     const dim3 grid((p.B * p.G + kPfQ - 1) / kPfQ, p.Hkv, splits);
     if (p.k_i8) {
         auto kern = prefill_kernel<true, true>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemI8);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PfGeom<true>::Smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(kern, grid, dim3(kPfThreadsI8), kPfSmemI8, s, w, tk, tv);
+        return launch_pdl(kern, grid, dim3(PfGeom<true>::Threads), PfGeom<true>::Smem, s, w, tk, tv);
     }
     auto kern = prefill_kernel<true, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PfGeom<false>::Smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, grid, dim3(kPfThreads), kPfSmem, s, w, tk, tv);
+    return launch_pdl(kern, grid, dim3(PfGeom<false>::Threads), PfGeom<false>::Smem, s, w, tk, tv);
 }
 
 }  // namespace pkv

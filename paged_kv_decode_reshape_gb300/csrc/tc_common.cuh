@@ -184,6 +184,11 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// bar.arrive on named barrier `id` for `count` threads: counts this warp without waiting
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // OR of `pred` over the `count` threads (whole warps) of named barrier `id`
 __device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
     int res;
