@@ -532,9 +532,14 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             if ((t + 1) * kPfK > n_tile_max || mask8 != 0xFF) {
                 // V rows of keys no row may see (past the context or in a missing block) must be
                 // finite: their weights are 0, and 0 * NaN would poison O. Thread r zeroes key r
-                // of the tile once its V copy has landed (PV(t) waits for this warp's P).
+                // of the tile once its V copy has landed (PV(t) waits for this warp's P). The
+                // parity wait on the slot's barrier is sound only once the slot's previous tile,
+                // t - SV, is known landed: PV(t - SV) done says so (and this warp already knows
+                // PV(t - SV - 2) done, so that wait is sound too).
                 const int k = r;
-                if (!mbar_wait_bounded(full(1, t % Gm::SV), (t / Gm::SV) & 1)) {
+                const int tv = t - Gm::SV;
+                const bool prev_ok = tv < 0 || mbar_wait_bounded(pv_done(tv & 1), (tv >> 1) & 1);
+                if (!prev_ok || !mbar_wait_bounded(full(1, t % Gm::SV), (t / Gm::SV) & 1)) {
                     atomicExch(&abort_flag, 1);
                     flag(p.status, PKV_FLAG_TIMEOUT);
                 } else if (t * kPfK + k >= n_tile_max || !((mask8 >> (k >> 4)) & 1)) {
@@ -611,7 +616,11 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
                 l += (e0 + o0) + (e1 + o1);
             }
             // P may be written, and O rescaled, once PV(t - 1) is done (it read the last P and
-            // accumulated O relative to mprev)
+            // accumulated O relative to mprev). This warp waited for PV(t - 3) in its previous
+            // tile, so the parity wait for PV(t - 1), on the same barrier, cannot be answered by
+            // the phase of PV(t - 3). (With two P buffers and a wait for PV(t - 2) only, a
+            // rescale's wait for PV(t - 1) would lack that: measured as wrong results.)
+            static_assert(Gm::PBufs == 1, "the waits below assume one P buffer");
             if (t > 0) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done((t - 1) & 1), ((t - 1) >> 1) & 1))) {
                     atomicExch(&abort_flag, 1);
