@@ -105,3 +105,26 @@ def test_prefill_scale_sign_and_running_max_rescale(scale):
                                          w.query_start, w.scale)
     assert_close(got, ref, "bf16", f"prefill scale={scale}")
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("growth", [2.0, 6.0])
+def test_prefill_reference_raised_on_alternate_tiles(growth):
+    """Keys whose magnitude grows with their position, so that most 128-key tiles raise a row's
+    reference maximum by more than the kernel's lazy margin of 2^8. The two softmax warps of a row
+    take alternate tiles, so the raised reference is handed from one to the other on almost every
+    tile, and O is rescaled on almost every tile, by either warp; query tiles with odd and even
+    numbers of key tiles, a ragged last tile."""
+    w = W.make_prefill(name="pfg", query_lens=[300, 129, 77], cached_lens=[700, 0, 333], Hq=8,
+                       Hkv=2, D=128, seed=23)
+    k = W.bf16_bits_to_f32(w.k_pool)
+    for b in range(len(w.context_lens)):
+        for pos in range(int(w.context_lens[b])):
+            blk = w.block_tables[b][pos // w.BS]
+            k[blk, :, pos % w.BS, :] *= np.float32(1.0 + growth * pos / 128.0)
+    w.k_pool = W.f32_to_bf16_bits(k)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill(w, st)
+    ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                         w.query_start, w.scale)
+    assert_close(got, ref, "bf16", f"prefill rising keys x{growth}")
+    assert int(st.item()) == 0

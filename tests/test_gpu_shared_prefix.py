@@ -52,6 +52,24 @@ def test_shared_prefix_matches_oracle(B, prefix, lo, hi):
     assert np.abs(got - reg).max() <= 2e-2
 
 
+
+def test_shared_prefix_reference_raised_on_alternate_tiles():
+    """Prefix keys whose magnitude grows with their position: most 128-key tiles of the prefix raise
+    each row's reference maximum past the lazy margin, so the prefix kernel's two softmax warps of
+    a row hand a raised reference to each other on almost every tile. The partial states it writes
+    (m, l, acc) must stay consistent for the merge with the suffixes."""
+    prefix = 1024
+    w = W.make_config(5, B=10, ctx_lo=16, ctx_hi=300, prefix_tokens=prefix, seed=91)
+    k = W.bf16_bits_to_f32(w.k_pool)
+    for pos in range(prefix):  # the shared blocks: row 0's first prefix / 16 entries
+        k[w.block_tables[0][pos // w.BS], :, pos % w.BS, :] *= np.float32(1.0 + 6.0 * pos / 128.0)
+    w.k_pool = W.f32_to_bf16_bits(k)
+    d = DevWorkload(w)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = to_f64(cascade(d, prefix, status=st))
+    assert int(st.item()) == 0
+    assert_close(got, reference(w), "bf16", "cascade with rising prefix keys")
+
 @pytest.mark.parametrize("g", [1, 2, 8, 16])
 def test_shared_prefix_head_groups(g):
     Hkv = 2
