@@ -280,6 +280,14 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
         }
     }
 
+    // the producers' first two windows of block ids, read before the set-up too (the first copies
+    // wait for them)
+    int ids_first = -1, ids_second = -1;
+    if (warp == kPfLoadWarpK || warp == kPfLoadWarpV) {
+        ids_first = load_window(0, warp == kPfLoadWarpK);
+        ids_second = has_window(1) ? load_window(1, warp == kPfLoadWarpK) : -1;
+    }
+
     if (tid == 0) {
         for (int g = 0; g < 2; ++g)
             for (int s = 0; s < nst(g); ++s) {
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
         const int g = warp - kPfLoadWarpK;
         const CUtensorMap* map = g ? &tmv : &tmk;
         int issued = 0;
-        int ids_cur = load_window(0, true), ids_next = has_window(1) ? load_window(1, true) : -1;
+        int ids_cur = ids_first, ids_next = ids_second;
         for (int t = 0; t < ntiles; ++t) {
             const int ns = nst(g), st = t % ns;
             if (t > 0 && (t & 3) == 0) {
