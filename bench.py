@@ -37,6 +37,7 @@ import workloads as W  # noqa: E402
 METRIC = "paged decode attn: KV GB/s vs GB300 HBM peak; decoded tokens/s per step"
 DEFAULT_CONFIG = 3          # long-context split-K decode (B=8, 32k-131k): the largest workload
 MIN_LOOP_MS = 1000.0        # the roofline and e2e loops run at least this much GPU time
+SECONDARY_LOOP_MS = 300.0   # each secondary workload's attention loop
 FALLBACK_HBM_GBS = 6800.0   # used only when MEASURED_PEAKS.json is absent
 L2_FLUSH_BYTES = 512 << 20
 PROFILES = os.path.join(ROOT, "profiles")
@@ -346,6 +347,103 @@ def run_reference(args):
 # the CUDA path
 # ------------------------------------------------------------------------------------------
 
+class DecodeRun:
+    """One decode workload resident on the device, with the calls a step makes: the L2 flush
+    (untimed), the KV write and the attention call."""
+
+    def __init__(self, pkv, w, dev, chunk_req=0, no_cascade=False):
+        import torch
+        self.pkv, self.w = pkv, w
+
+        def up(a):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+            return torch.from_numpy(a).to(dev)
+
+        self.kp, self.vp = up(w.k_pool), up(w.v_pool)
+        self.ks, self.vs = up(w.k_scales), up(w.v_scales)
+        # the step's own inputs (q, tables, lengths, slots, new K/V rows) live in one device
+        # buffer, 256-byte aligned segments, so a step fed from the host needs a single copy
+        self.stage, views = stage_buffers(dev, {n: up(a) for n, a in dict(
+            q=w.q, bt=w.block_tables, cl=w.context_lens, sm=w.slot_mapping, kn=w.k_new, vn=w.v_new,
+            kns=w.k_new_scales, vns=w.v_new_scales).items() if a is not None})
+        self.q, self.bt, self.cl, self.sm, self.kn, self.vn = (
+            views[n] for n in ("q", "bt", "cl", "sm", "kn", "vn"))
+        self.kns, self.vns = views.get("kns"), views.get("vns")
+        self.out = torch.empty_like(self.q)
+        self.maxc = maxc = w.max_context_len
+        self.chunk_req = chunk_req
+        # a batch whose sequences share a prefix runs through the shared-prefix (cascade) call
+        self.prefix = prefix = w.shared_prefix_blocks * w.BS
+        self.cascade = prefix > 0 and not no_cascade
+        self.chunk = pkv.decode_split_chunk(w.B, w.Hkv, w.D, maxc - (prefix if self.cascade else 0),
+                                            chunk_req, {"f32": pkv.F32, "bf16": pkv.BF16, "i8": pkv.I8}[w.kv_dtype])
+        nws = (pkv.decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, prefix, chunk_req)
+               if self.cascade else pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, chunk_req))
+        self.ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.clean = torch.zeros(L2_FLUSH_BYTES // 2, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def flush_l2(self, k):
+        # write a buffer 4x the L2, then read a 1 GB one, so the step starts with a cold L2 holding
+        # clean lines (no write-back of the flush's dirty lines charged to the timed kernels)
+        self.flush.fill_(k & 0xFF)
+        self.clean.max()
+
+    def write(self):
+        self.pkv.kv_cache_write(self.kn, self.vn, self.kp, self.vp, self.sm, self.kns, self.vns, self.ks,
+                                self.vs, status=self.status, stream=self.stream)
+
+    def attend(self):
+        pkv, w = self.pkv, self.w
+        if self.cascade:
+            pkv.paged_decode_attention_shared_prefix(self.out, self.q, self.kp, self.vp, self.bt, self.cl,
+                                                     self.maxc, w.scale, self.prefix, self.chunk_req,
+                                                     self.ws, self.status, self.stream)
+        elif w.kv_dtype == "i8":
+            pkv.paged_decode_attention_int8(self.out, self.q, self.kp, self.vp, self.ks, self.vs, self.bt,
+                                            self.cl, self.maxc, w.scale, self.chunk_req, self.ws,
+                                            self.status, self.stream)
+        else:
+            pkv.paged_decode_attention(self.out, self.q, self.kp, self.vp, self.bt, self.cl, self.maxc,
+                                       w.scale, self.chunk_req, self.ws, self.status, self.stream)
+
+
+def measure_attention(pkv, cfg: int, dev, min_ms: float, warmup: int = 5) -> dict:
+    """The attention call alone on config `cfg` (L2 flushed before each call, CUDA events around
+    it, at least min_ms of GPU time), as a roofline record: a secondary measurement next to the
+    headline line."""
+    import torch
+    w = W.make_config(cfg, seed=rank_seed(cfg, 0))
+    run = DecodeRun(pkv, w, dev)
+    for _ in range(max(3, warmup)):
+        run.flush_l2(1)
+        run.write()
+        run.attend()
+    torch.cuda.synchronize()
+    if int(run.status.item()) != 0:
+        raise RuntimeError(f"{w.name}: kernels flagged bad inputs: status {int(run.status.item())}")
+    total_ms, n = timed_loop(run.flush_l2, lambda k: run.attend(), min_ms, 20, run.stream)
+    hbm, peak_kind = measured_peaks()
+    nbytes = attention_bytes(w)
+    avg_s = total_ms / n / 1e3
+    achieved = nbytes / avg_s / 1e9
+    rec = {"workload": w.name, "description": W.CONFIGS[cfg], "dtype": w.kv_dtype,
+           "attention_call_us": round(avg_s * 1e6, 3), "achieved_gbs": round(achieved, 2),
+           "peak_gbs": hbm, "frac": round(achieved / hbm, 4), "peak_kind": f"of {peak_kind}",
+           "algorithmic_bytes_per_launch": nbytes, "split_chunk": run.chunk,
+           "shared_prefix_call": bool(run.cascade), "launches_timed": n,
+           "timed_ms": round(total_ms, 2), "traffic": profiled_traffic(w.name)}
+    del run
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -360,58 +458,10 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     w = W.make_config(args.config, seed=rank_seed(args.config, rank))
-
-    def up(a):
-        if a is None:
-            return None
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(a).to(dev)
-
-    kp, vp = up(w.k_pool), up(w.v_pool)
-    ks, vs = up(w.k_scales), up(w.v_scales)
-    # the step's own inputs (q, tables, lengths, slots, new K/V rows) live in one device buffer,
-    # 256-byte aligned segments, so a step fed from the host needs a single copy
-    stage, views = stage_buffers(dev, {n: up(a) for n, a in dict(
-        q=w.q, bt=w.block_tables, cl=w.context_lens, sm=w.slot_mapping, kn=w.k_new, vn=w.v_new,
-        kns=w.k_new_scales, vns=w.v_new_scales).items() if a is not None})
-    q, bt, cl, sm, kn, vn = (views[n] for n in ("q", "bt", "cl", "sm", "kn", "vn"))
-    kns, vns = views.get("kns"), views.get("vns")
-    out = torch.empty_like(q)
-    maxc = w.max_context_len
-    # a batch whose sequences share a prefix runs through the shared-prefix (cascade) call
-    prefix = w.shared_prefix_blocks * w.BS
-    cascade = prefix > 0 and not getattr(args, "no_cascade", False)
-    chunk = pkv.decode_split_chunk(w.B, w.Hkv, w.D, maxc - (prefix if cascade else 0), args.chunk,
-                                   {"f32": pkv.F32, "bf16": pkv.BF16, "i8": pkv.I8}[w.kv_dtype])
-    nws = (pkv.decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, prefix, args.chunk)
-           if cascade else pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, maxc, args.chunk))
-    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    clean = torch.zeros(L2_FLUSH_BYTES // 2, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def flush_l2(k):
-        # write a buffer 4x the L2, then read a 1 GB one, so the step starts with a cold L2 holding
-        # clean lines (no write-back of the flush's dirty lines charged to the timed kernels)
-        flush.fill_(k & 0xFF)
-        clean.max()
-
-    def write():
-        pkv.kv_cache_write(kn, vn, kp, vp, sm, kns, vns, ks, vs, status=status, stream=stream)
-
-    def attend():
-        if cascade:
-            pkv.paged_decode_attention_shared_prefix(out, q, kp, vp, bt, cl, maxc, w.scale, prefix,
-                                                     args.chunk, ws, status, stream)
-        elif w.kv_dtype == "i8":
-            pkv.paged_decode_attention_int8(out, q, kp, vp, ks, vs, bt, cl, maxc, w.scale,
-                                            args.chunk, ws, status, stream)
-        else:
-            pkv.paged_decode_attention(out, q, kp, vp, bt, cl, maxc, w.scale, args.chunk, ws,
-                                       status, stream)
+    run = DecodeRun(pkv, w, dev, args.chunk, getattr(args, "no_cascade", False))
+    stage, out, status, stream = run.stage, run.out, run.status, run.stream
+    maxc, chunk, cascade = run.maxc, run.chunk, run.cascade
+    flush_l2, write, attend = run.flush_l2, run.write, run.attend
 
     # nvidia-smi samples the clocks from before the warm-up to the end of the e2e loop: the K timed
     # steps alone can be shorter than one sampling interval, the roofline and e2e loops are not
@@ -517,6 +567,31 @@ def run_ours(args):
         line["clocks"] = clk
     if not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
+    if world == 1 and not args.no_secondary:
+        # the other workloads, each as its own record (the headline keys above stay as they are):
+        # the Llama-3-8B GQA batch, the INT8 batch, the shared-prefix batch, and the paged prefill
+        # over a bf16 and an INT8 cache
+        del run, stage, out, status, flush_l2, write, attend
+        torch.cuda.empty_cache()
+        clocks2 = ClockSampler(local)
+        clocks2.start()
+        rec = {}
+        for cfg in (2, 4, 5):
+            r = measure_attention(pkv, cfg, dev, SECONDARY_LOOP_MS)
+            rec[r["workload"]] = r
+        for kv in ("bf16", "i8"):
+            p = measure_prefill(pkv, kv, 60, 5)
+            rec[p["config"]["workload"]] = {
+                "metric": p["metric"], "tflops": p["value"], "ms_per_call": p["ms_per_step"],
+                "peak_tflops": p["roofline"]["peak"], "frac": p["roofline"]["frac"],
+                "peak_kind": p["roofline"]["peak_kind"], "calls_timed": p["steps"],
+                "flops_per_call": p["config"]["flops_per_step"]}
+        clk2 = clocks2.stop()
+        line["secondary"] = {"note": ("separate workloads measured after the headline, each on its "
+                                      "own: decode attention calls (L2 flushed before each call, at "
+                                      f"least {SECONDARY_LOOP_MS:.0f} ms of GPU time) and paged "
+                                      "prefill calls"),
+                             "workloads": rec, "clocks": clk2}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -602,15 +677,12 @@ def run_multi(args):
     print(json.dumps(line), flush=True)
 
 
-def run_prefill(args):
+def measure_prefill(pkv, kv: str, steps: int, warmup: int) -> dict:
     """Paged chunked prefill on tcgen05: 4 sequences x 4096 new prompt tokens after 2048 cached
-    tokens, Llama-3-8B heads (32 q / 8 kv, D = 128, bf16). Reports TFLOP/s against the measured
-    dense bf16 tensor peak."""
+    tokens, Llama-3-8B heads (32 q / 8 kv, D = 128), over a bf16 or an INT8 cache. Returns the
+    JSON line: TFLOP/s against the measured dense bf16 tensor peak."""
     import torch
-
-    import paged_kv_decode_reshape_gb300 as pkv
-    pkv.load(build_if_missing=False)
-    i8 = getattr(args, "prefill_kv", "bf16") == "i8"
+    i8 = kv == "i8"
     w = W.make_prefill(name="prefill_llama3_8b" + ("_int8" if i8 else ""), query_lens=[4096] * 4,
                        cached_lens=[2048] * 4, Hq=32, Hkv=8, D=128, seed=7,
                        kv_dtype="i8" if i8 else "bf16")
@@ -632,10 +704,10 @@ def run_prefill(args):
             pkv.paged_prefill_attention_int8(out, q, kp, vp, ks, vs, bt, cl, qs, w.max_query_len, w.scale)
         else:
             pkv.paged_prefill_attention(out, q, kp, vp, bt, cl, qs, w.max_query_len, w.scale)
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
-    K = max(1, min(args.steps, 200))
+    K = max(1, min(steps, 200))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     clocks = ClockSampler(0)
     clocks.start()
@@ -658,7 +730,7 @@ def run_prefill(args):
             peak = float(json.load(f).get("bf16_tflops", peak))
     line = {"metric": "paged prefill attention TFLOP/s (causal, tcgen05)" + (", INT8 KV cache" if i8 else ""),
             "value": round(tflops, 2),
-            "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": max(3, args.warmup),
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": max(3, warmup),
             "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": w.name, "sequences": w.B, "new_tokens": 4096, "cached_tokens": 2048,
@@ -670,7 +742,16 @@ def run_prefill(args):
             "tokens_per_s": round(int(w.query_start[-1]) / (ms / 1e3), 1)}
     if clk is not None:
         line["clocks"] = clk
-    print(json.dumps(line), flush=True)
+    del q, kp, vp, out, flush, clean
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_prefill(args):
+    import paged_kv_decode_reshape_gb300 as pkv
+    pkv.load(build_if_missing=False)
+    print(json.dumps(measure_prefill(pkv, getattr(args, "prefill_kv", "bf16"), args.steps, args.warmup)),
+          flush=True)
 
 
 def main(argv=None):
@@ -685,6 +766,9 @@ def main(argv=None):
     ap.add_argument("--min-loop-ms", type=float, default=MIN_LOOP_MS,
                     help="GPU time the roofline and e2e loops run at least (0: exactly --steps "
                          "iterations each, e.g. under a profiler)")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary workloads (configs 2, 4, 5 and the paged prefill) "
+                         "measured after the headline and reported in its line")
     ap.add_argument("--no-cascade", action="store_true",
                     help="run a shared-prefix workload through the plain decode call instead of "
                          "the shared-prefix (cascade) call")
