@@ -49,6 +49,8 @@
 // 2^8), so O is rarely rescaled; at the end each row is divided by its sum.
 #include <cuda.h>
 
+#include <cuda_fp16.h>
+
 #include "pkv_device.cuh"
 #include "tc_common.cuh"
 
@@ -161,18 +163,32 @@ struct PfWork {
     const float* v_scales;
 };
 
-// Four int8 values (one 32-bit word) times `scale`, as two bf16 pairs (RN): each byte goes to the
-// low byte of 2^23 + (x + 128) (the sign flipped by the XOR), so one subtraction gives x exactly.
-__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint64_t scale2, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint64_t bias2 = f32x2(8388736.0f, 8388736.0f);  // 2^23 + 128
-    float a, b, c, d;
-    f32x2_split(mul_f32x2(sub_f32x2(f32x2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
-                                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))), bias2), scale2), a, b);
-    f32x2_split(mul_f32x2(sub_f32x2(f32x2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
-                                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))), bias2), scale2), c, d);
-    lo = pack2_bf16(a, b);
-    hi = pack2_bf16(c, d);
+// INT8 cache: the products run on fp16 operands. Four int8 values (one 32-bit word, bytes b0..b3)
+// become two fp16 pairs exactly by the byte-permute / magic-number conversion (Kim et al. 2022):
+// the byte x + 128 (x XOR 0x80) in the low byte of the fp16 1024 is exactly 1152 + x, so
+// lo = (1152 + b0, 1152 + b2) is one LOP3 and hi = (1152 + b1, 1152 + b3) a shift and a LOP3. A
+// row's dims thus come in the order 4j, 4j + 2, 4j + 1, 4j + 3 within every group of four; Q is
+// written in the same order (so S is unchanged) and O's columns are put back in order when stored.
+constexpr float kPfI8Bias = 1152.0f;
+__device__ __forceinline__ uint32_t pf_i8_lo(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x64806480u; }
+__device__ __forceinline__ uint32_t pf_i8_hi(uint32_t w) { return ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u; }
+// the biased pair minus 1152 in each half: the codes themselves, exact in fp16
+__device__ __forceinline__ uint32_t pf_unbias(uint32_t h) {
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__float2half_rn(kPfI8Bias)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+// O columns 4j .. 4j + 3 hold dims 4j, 4j + 2, 4j + 1, 4j + 3: back in order
+__device__ __forceinline__ void pf_unpermute(float (&o)[32]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float t = o[4 * j + 1];
+        o[4 * j + 1] = o[4 * j + 2];
+        o[4 * j + 2] = t;
+    }
+}
+__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 template <bool kPrefix, bool kI8>
@@ -256,6 +272,7 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
     auto staged = [&](int g, int s) { return sbase + Gm::OffStaged + 8 * ridx(g, s); };
     auto scl = [&](int g, int s) { return sbase + Gm::OffScl + ridx(g, s) * 8 * kBlockSize * 4; };
     __shared__ int abort_flag;
+    __shared__ unsigned q_amax_bits;  // INT8: the CTA's largest |q| (a non-negative float's bits)
 
     // softmax thread (hf, r): row r, keys kPfKeysPer hf .. of each tile, output dims kPfDimsPer hf ..
     const int hf = (warp >> 2) & (kPfSplit - 1);
@@ -310,6 +327,7 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
         mbar_init(drain(0), 1);
         mbar_init(drain(1), 1);
         abort_flag = 0;
+        q_amax_bits = 0u;
         mbar_init_fence();
     }
     if (warp == kPfMmaWarp) {
@@ -327,11 +345,55 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
     // the S issuer waits for it (named barrier kPfQBar) and the producers start their copies at
     // once (measured: 7 % faster than a CTA-wide barrier). For an INT8 cache the CTA-wide barrier
     // stays: producers and converters started before Q was written made that kernel 7 % slower.
+    // INT8: q enters the fp16 products as q' = q * 2^e, e one power of two for the CTA's rows, so
+    // that the largest |q'| lies in [2^14, 2^15) (a bf16 value scaled by a power of two is exact in
+    // fp16 there, and nothing passes fp16's range); the scores' factor carries 2^-e. kcorr =
+    // 1152 * (sum of the row's q' as the product sees them) is what the biased K codes add to each
+    // of the row's scores.
+    float q_down = 1.f, kcorr = 0.f;
     if constexpr (kI8) {
-        if (warp < kPfSoftWarps) tmem_st_words(tmem + tl + kQCol + kPfDimsPer / 2 * hf, qw);
+        if (warp < kPfSoftWarps) {
+            float amax = 0.f;
+#pragma unroll
+            for (int c = 0; c < kPfDimsPer / 2; ++c)
+                amax = fmax3(amax, fabsf(__uint_as_float(qw[c] << 16)), fabsf(__uint_as_float(qw[c] & 0xffff0000u)));
+            atomicMax(&q_amax_bits, __float_as_uint(amax));
+        }
+        __syncthreads();
+        const float amax = __uint_as_float(q_amax_bits);
+        int e = 0;
+        if (amax > 0.f) {  // floor(log2(amax)) from the exponent field (-127 for a subnormal amax)
+            e = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xffu) - 127);
+            e = e < -126 ? -126 : (e > 126 ? 126 : e);  // 2^e and 2^-e stay normal floats
+        }
+        const float q_up = __uint_as_float((uint32_t)(127 + e) << 23);
+        q_down = __uint_as_float((uint32_t)(127 - e) << 23);
+        if (warp < kPfSoftWarps) {
+            float qsum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kPfDimsPer / 4; ++j) {  // dims 4j .. 4j + 3 of this thread's part
+                const uint32_t w0 = qw[2 * j], w1 = qw[2 * j + 1];
+                const uint32_t lo = pack2_f16(__uint_as_float(w0 << 16) * q_up, __uint_as_float(w1 << 16) * q_up);
+                const uint32_t hi = pack2_f16(__uint_as_float(w0 & 0xffff0000u) * q_up,
+                                              __uint_as_float(w1 & 0xffff0000u) * q_up);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+                qsum += (a.x + a.y) + (b.x + b.y);
+                qw[2 * j] = lo;
+                qw[2 * j + 1] = hi;
+            }
+            xsum[hf * kPfQ + r] = qsum;  // the row's other part is read after the barrier below
+            tmem_st_words(tmem + tl + kQCol + kPfDimsPer / 2 * hf, qw);
+        }
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (warp < kPfSoftWarps) {
+            float qs = 0.f;
+#pragma unroll
+            for (int q2 = 0; q2 < kPfSplit; ++q2) qs += xsum[q2 * kPfQ + r];
+            kcorr = kPfI8Bias * qs;
+        }
     } else if (warp < kPfSoftWarps) {
         tmem_st_words(tmem + tl + kQCol + kPfDimsPer / 2 * hf, qw);
         tc_fence_before();
@@ -366,6 +428,17 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             // bf16: the tensor copies complete full(g); INT8: the row copies complete staged(g)
             const uint32_t done = kI8 ? staged(g, st) : full(g, st);
             constexpr int kBytes = kI8 ? kPfBlockBytes / 2 + kBlockSize * 4 : kPfBlockBytes;
+            if constexpr (kI8) {
+                // V scales of blocks not copied: zero, so that a masked key's weight times its
+                // scale is 0 (a stale scale could be a NaN)
+                if (g == 1 && lane < 8 && id < 0) {
+                    float4* z = reinterpret_cast<float4*>(smem + Gm::OffScl + ridx(1, st) * 8 * kBlockSize * 4) +
+                                lane * (kBlockSize / 4);
+#pragma unroll
+                    for (int c = 0; c < kBlockSize / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                __syncwarp();
+            }
             if (lane == 0) {
                 if (valid == 0) mbar_arrive(done);
                 else mbar_arrive_expect_tx(done, __popc(valid) * kBytes);
@@ -408,7 +481,6 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             if (!got && lane_of() == 0) { atomicExch(&abort_flag, 1); flag(p.status, PKV_FLAG_TIMEOUT); }
             if (barrier_or(bar_id, kPfConvThreads, !got || aborted(&abort_flag))) break;
             uint4 in[2][8];
-            float sc[2];
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int key = c + 64 * kk, blk = key >> 4, kin = key & 15;
@@ -416,25 +488,29 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
                                                                    kPfI8Half + blk * (kPfBlockBytes / 2) + kin * 128);
 #pragma unroll
                 for (int v = 0; v < 8; ++v) in[kk][v] = row[(v + lane) & 7];  // rotated: no bank conflicts
-                sc[kk] = reinterpret_cast<const float*>(smem + Gm::OffScl)[(ridx(g, st) * 8 + blk) * kBlockSize + kin];
             }
             named_barrier_sync(bar_id, kPfConvThreads);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int key = c + 64 * kk, blk = key >> 4, kin = key & 15;
-                // K: the codes themselves (exact in bf16); the softmax multiplies each score by its
-                // key's scale in fp32. V: code * scale rounded to bf16.
-                const uint64_t s2 = g ? f32x2(sc[kk], sc[kk]) : f32x2(1.f, 1.f);
+                // K: the codes plus 1152 (the softmax subtracts kcorr from each score and applies
+                // the key's scale); V: the codes themselves (the key's scale goes onto its weight)
                 unsigned char* base = smem + (g ? Gm::OffV : kPfOffK) + st * kPfStage + blk * kPfBlockBytes +
                                       (kin >> 3) * 2048 + (kin & 7) * 128;
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     const int vv = (v + lane) & 7;  // dims 16 vv .. 16 vv + 15
                     uint32_t o[8];
-                    i8x4_to_bf16x4(in[kk][v].x, s2, o[0], o[1]);
-                    i8x4_to_bf16x4(in[kk][v].y, s2, o[2], o[3]);
-                    i8x4_to_bf16x4(in[kk][v].z, s2, o[4], o[5]);
-                    i8x4_to_bf16x4(in[kk][v].w, s2, o[6], o[7]);
+                    const uint32_t wv[4] = {in[kk][v].x, in[kk][v].y, in[kk][v].z, in[kk][v].w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        o[2 * x] = pf_i8_lo(wv[x]);
+                        o[2 * x + 1] = pf_i8_hi(wv[x]);
+                        if (g) {
+                            o[2 * x] = pf_unbias(o[2 * x]);
+                            o[2 * x + 1] = pf_unbias(o[2 * x + 1]);
+                        }
+                    }
                     const int half = vv >> 2, ch = (2 * vv) & 7;  // 16-byte chunks ch, ch + 1 of the half
                     unsigned char* hb = base + half * 1024;
                     *reinterpret_cast<uint4*>(hb + ((ch ^ (kin & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -448,8 +524,9 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
         // ---------------- MMA issuers: S (warp 8) and PV (warp 11) ----------------
         if (lane == 0) {
             const bool is_s = warp == kPfMmaWarp;
-            constexpr uint32_t kIdescS = idesc_bf16(kPfQ, kPfK, false);
-            constexpr uint32_t kIdescO = idesc_bf16(kPfQ, 128, true);
+            // fp16 operands for an INT8 cache, bf16 otherwise
+            constexpr uint32_t kIdescS = kI8 ? idesc_f16(kPfQ, kPfK, false) : idesc_bf16(kPfQ, kPfK, false);
+            constexpr uint32_t kIdescO = kI8 ? idesc_f16(kPfQ, 128, true) : idesc_bf16(kPfQ, 128, true);
             auto issue_s = [&](int t) {  // S(t) = Q . K(t)^T into S buffer t % SBufs
                 const uint32_t kbase = slot(0, t);
 #pragma unroll
@@ -718,7 +795,8 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
         // sign. |scale| is at least FLT_MIN so a masked score (-inf) never meets a zero factor: a
         // zero scale still gives weights of exactly 1 (every visible score times FLT_MIN is ~0).
         const bool neg = p.scale_log2 < 0.f;
-        const float csc = fmaxf(fabsf(p.scale_log2), 1.17549435e-38f);
+        // (INT8: times 2^-e, undoing q's prescale)
+        const float csc = fmaxf(fabsf(p.scale_log2) * q_down, 1.17549435e-38f);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // bit j of `present`: block 32 w + j of the current window is present (the producer's test)
@@ -766,17 +844,18 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             float s[kPfKeysPer];
             tmem_ld_words(s_col + 128 * su, s);  // (reading TMEM is harmless even when S(t) never came)
             if constexpr (kI8) {
-                // S holds q . codes: times each key's K scale (the staged scale row of the K slot,
-                // keys in tile order), then the slot may be refilled
+                // S holds q' . (codes + 1152): minus kcorr, times each key's K scale (the staged
+                // scale row of the K slot, keys in tile order), then the slot may be refilled
                 const float4* ks4 = reinterpret_cast<const float4*>(smem + Gm::OffScl) +
                                     ((t % Gm::SK) * 8 * kBlockSize + kPfKeysPer * hf) / 4;
+                const uint64_t nk2 = f32x2(-kcorr, -kcorr);
 #pragma unroll
                 for (int c = 0; c < kPfKeysPer / 4; ++c) {
                     const float4 k4 = ks4[c];
                     float a, b2;
-                    f32x2_split(mul_f32x2(f32x2(s[4 * c], s[4 * c + 1]), f32x2(k4.x, k4.y)), a, b2);
+                    f32x2_split(mul_f32x2(add_f32x2(f32x2(s[4 * c], s[4 * c + 1]), nk2), f32x2(k4.x, k4.y)), a, b2);
                     s[4 * c] = a; s[4 * c + 1] = b2;
-                    f32x2_split(mul_f32x2(f32x2(s[4 * c + 2], s[4 * c + 3]), f32x2(k4.z, k4.w)), a, b2);
+                    f32x2_split(mul_f32x2(add_f32x2(f32x2(s[4 * c + 2], s[4 * c + 3]), nk2), f32x2(k4.z, k4.w)), a, b2);
                     s[4 * c + 2] = a; s[4 * c + 3] = b2;
                 }
                 __syncwarp();
@@ -837,13 +916,29 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             uint32_t pw[kPfKeysPer / 2];
             const uint64_t cs2 = f32x2(csc, csc), nms2 = f32x2(-ms, -ms);
             uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+            // INT8: the weights enter the fp16 product times their key's V scale (the V slot's
+            // staged scale row; waited for on every tile, so the parity wait stays in step)
+            const float* vsc = nullptr;
+            if constexpr (kI8) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(full(1, t % Gm::SV), (t / Gm::SV) & 1))) {
+                    atomicExch(&abort_flag, 1);
+                    flag(p.status, PKV_FLAG_TIMEOUT);
+                }
+                vsc = reinterpret_cast<const float*>(smem + Gm::OffScl) +
+                      ridx(1, t % Gm::SV) * 8 * kBlockSize + kPfKeysPer * hf;
+            }
 #pragma unroll
             for (int c = 0; c < kPfKeysPer / 2; ++c) {
                 float y0, y1;
                 f32x2_split(fma_f32x2(f32x2(s[2 * c], s[2 * c + 1]), cs2, nms2), y0, y1);
                 const float a0 = ex2(y0), a1 = ex2(y1);
                 ls2[c & 1] = add_f32x2(ls2[c & 1], f32x2(a0, a1));
-                pw[c] = pack2_bf16(a0, a1);
+                if constexpr (kI8) {
+                    const float2 v2 = reinterpret_cast<const float2*>(vsc)[c];
+                    pw[c] = pack2_f16(a0 * v2.x, a1 * v2.y);
+                } else {
+                    pw[c] = pack2_bf16(a0, a1);
+                }
             }
             {
                 float e0, e1, o0, o1;
@@ -894,6 +989,7 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             for (int c0 = 0; c0 < kPfDimsPer; c0 += 32) {
                 float o[32];
                 tmem_ld32(o_col + c0, o);
+                if constexpr (kI8) pf_unpermute(o);
                 if (row_valid) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
@@ -912,6 +1008,7 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
             for (int c0 = 0; c0 < kPfDimsPer; c0 += 32) {
                 float o[32];
                 tmem_ld32(o_col + c0, o);
+                if constexpr (kI8) pf_unpermute(o);
                 if (row_valid) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
