@@ -123,3 +123,34 @@ def test_prefill_int8_argument_errors():
         P.paged_prefill_attention_int8(out, to_dev(w.q), to_dev(w.k_pool), to_dev(w.v_pool), None,
                                        to_dev(w.v_scales), to_dev(w.block_tables),
                                        to_dev(w.context_lens), to_dev(w.query_start), 3, w.scale)
+
+
+@pytest.mark.parametrize("mag,ndims,k_mult", [
+    (1e2, 4, 1.0), (1e3, 2, 1.0), (1e4, 1, 1.0),  # outlier dims, N(0, 1) keys
+    (1e6, 3, 1e-4),                               # |q| past fp16's range, logits of ordinary size
+    (1e-4, 128, 1e4),                             # |q| below fp16's normal range, same logits
+    (1e-6, 128, 1.0),                             # tiny queries: near-uniform weights
+])
+def test_prefill_int8_outlier_query_magnitudes(mag, ndims, k_mult):
+    """The INT8 prefill runs fp16 products with q scaled by one power of two per CTA: queries with a
+    few outlier dims (the magnitudes LLM activations reach), or whose magnitude falls outside fp16's
+    normal range while the keys (K scales times k_mult) keep the logits of ordinary size, must
+    neither overflow nor lose precision. The same INT8 bar as every other case."""
+    w = W.make_prefill(name="pfo", query_lens=[1, 40, 200], cached_lens=[0, 300, 100], Hq=16,
+                       Hkv=2, D=128, seed=int(np.log10(mag) * 10) + ndims, kv_dtype="i8")
+    rng = np.random.default_rng(ndims)
+    q = W.bf16_bits_to_f32(w.q).copy()
+    if ndims == w.D:
+        q *= np.float32(mag)
+    else:
+        for t in range(q.shape[0]):
+            for h in range(w.Hq):
+                dims = rng.choice(w.D, ndims, replace=False)
+                q[t, h, dims] = np.float32(mag) * np.sign(rng.standard_normal(ndims)).astype(np.float32)
+    w.q = W.f32_to_bf16_bits(q)
+    w.k_scales = (w.k_scales * np.float32(k_mult)).astype(np.float32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill_i8(w, st)
+    assert np.all(np.isfinite(got))
+    assert_close(got, reference(w), "i8", f"INT8 prefill |q| {mag} in {ndims} dims, keys x {k_mult}")
+    assert int(st.item()) == 0
