@@ -158,9 +158,11 @@ pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_p
  * rows, causal rule, arguments and errors as pkv_paged_prefill_attention, with
  *     K_t = k_pool[blk][g][off][:] * k_scales[blk][g][off],  V_t likewise with v_scales
  * (int8 pools [num_blocks][num_kv_heads][16][128], fp32 scales [num_blocks][num_kv_heads][16],
- * all 16-byte aligned; q and out bf16). Inside the kernel each staged int8 row is multiplied by
- * its token's scale and rounded to bf16 (one rounding, relative error <= 2^-9) before the tcgen05
- * products, which take both operands in one 16-bit type (q's bf16); accumulation fp32.
+ * all 16-byte aligned; q and out bf16). Inside the kernel the tcgen05 products run on fp16
+ * operands (they take both operands in one 16-bit type): the int8 codes exactly (K with an offset
+ * of 1152 removed from each score), q scaled by one power of two per 128 rows (exact for bf16
+ * values, within fp16's range), each key's K scale applied to its fp32 score and its V scale to
+ * its weight before the weight is rounded to fp16; accumulation fp32.
  */
 pkv_status pkv_paged_prefill_attention_int8(void* out, const void* q, const int8_t* k_pool,
                                             const int8_t* v_pool, const float* k_scales,

@@ -82,8 +82,8 @@ constexpr int kPfGroup = 32 * kPfSplit;             // threads of one barrier gr
 constexpr int kPfThreads = kPfSoftThreads + 128;
 // INT8 cache: the producers copy each block's int8 K (or V) rows (2 KB) into the second half of the
 // tile's slot and its 16 scales into a row of the scale area, completing on staged[ring slot]; four
-// converter warps (two per ring) widen them in place into the bf16 layout above and then complete
-// full[ring slot] for the MMA issuers, as the tensor copies do for a bf16 cache.
+// converter warps (two per ring) widen them in place into fp16 rows of the layout above and then
+// complete full[ring slot] for the MMA issuers, as the tensor copies do for a bf16 cache.
 constexpr int kPfConvWarp0 = kPfSoftWarps + 4;       // warps 12-13: K ring, 14-15: V ring
 constexpr int kPfConvThreads = 64;                   // per ring
 constexpr int kPfI8Half = kPfStage / 2;              // int8 rows of a tile start here in the slot
@@ -94,8 +94,9 @@ constexpr int kPfThreadsI8 = kPfThreads + 32 * 4;
 //    buffer (TMEM has room for one more 128-column buffer, not for both). K 3 slots, V 2: measured
 //    on GB300 (the 4 x 4096-token prefill) 1210-1220 TFLOP/s, against 1162 with V 3 slots and
 //    1137 with one S and two P buffers.
-//  - INT8: the converters bound the kernel and a PV waits for its V conversion, so the softmax
-//    keeps two P buffers (it need not wait for PV(t-1) before writing P(t)) and S one buffer.
+//  - INT8: a PV waits for its V conversion, so the softmax keeps two P buffers (it need not wait
+//    for PV(t-1) before writing P(t)) and S one buffer (two S and one P measured the same); the
+//    alternate-tile softmax needs ~160 registers, above the 128 of a 512-thread CTA.
 #ifndef PKV_PF_STAGES_K
 #define PKV_PF_STAGES_K 3
 #endif
@@ -466,11 +467,11 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
         }
     } else if (kI8 && warp >= kPfConvWarp0) {
         // ---------------- INT8: converters of ring g (warps 12-13: K, 14-15: V) ----------------
-        // Thread c widens keys c and c + 64 of each tile: the key's 128 int8 values (V: times the
-        // key's scale, rounded to bf16; K: the codes, exact) into the 128-byte-swizzled rows the MMA
-        // descriptors read. All of the
-        // ring's int8 rows are read into registers before any bf16 row is written, since the bf16
-        // tile fills the whole slot, over the int8 rows in its second half.
+        // Thread c widens keys c and c + 64 of each tile: the key's 128 int8 values into fp16
+        // (K: the codes plus 1152; V: the codes) in the 128-byte-swizzled rows the MMA
+        // descriptors read. All of the ring's int8 rows are read into registers before any fp16
+        // row is written, since the fp16 tile fills the whole slot, over the int8 rows in its
+        // second half.
         const int g = (warp - kPfConvWarp0) >> 1;
         const int c = tid - 32 * (kPfConvWarp0 + 2 * g);
         const int bar_id = 5 + g;  // named barrier of the ring's kPfConvThreads threads
