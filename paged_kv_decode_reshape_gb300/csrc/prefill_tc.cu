@@ -93,7 +93,8 @@ constexpr int kPfThreadsI8 = kPfThreads + 32 * 4;
 //  - bf16: two S buffers, so the S products run up to two tiles ahead of the softmax, and one P
 //    buffer (TMEM has room for one more 128-column buffer, not for both). K 3 slots, V 2: measured
 //    on GB300 (the 4 x 4096-token prefill) 1210-1220 TFLOP/s, against 1162 with V 3 slots and
-//    1137 with one S and two P buffers.
+//    1137 with one S and two P buffers (with the alternate-tile softmax: 1315-1320 against 1143;
+//    with one S buffer, S(t + 1) starts only after S(t) is read and then queues behind PV(t)).
 //  - INT8: a PV waits for its V conversion, so the softmax keeps two P buffers (it need not wait
 //    for PV(t-1) before writing P(t)) and S one buffer (two S and one P measured the same); the
 //    alternate-tile softmax needs ~160 registers, above the 128 of a 512-thread CTA.
