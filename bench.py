@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -297,6 +298,40 @@ def sample_bytes(w: W.DecodeWorkload, rows) -> int:
     return W.kv_bytes(sub)
 
 
+# Arm (implementer, part) codes of /proc/cpuinfo with a known core name
+ARM_CORES = {(0x41, 0xd4f): "Arm Neoverse-V2", (0x41, 0xd40): "Arm Neoverse-V1",
+             (0x41, 0xd0c): "Arm Neoverse-N1", (0x41, 0xd49): "Arm Neoverse-N2"}
+
+
+def parse_cpu_model(cpuinfo: str, machine: str) -> str:
+    """The CPU model from /proc/cpuinfo text: x86 kernels give a 'model name' line; Arm kernels
+    give implementer and part codes, named from ARM_CORES when known."""
+    impl = part = None
+    for ln in cpuinfo.splitlines():
+        key, _, val = ln.partition(":")
+        key, val = key.strip().lower(), val.strip()
+        if key == "model name" and val:
+            return val
+        try:
+            if key == "cpu implementer" and impl is None:
+                impl = int(val, 16)
+            elif key == "cpu part" and part is None:
+                part = int(val, 16)
+        except ValueError:
+            pass
+    if impl is not None and part is not None:
+        return ARM_CORES.get((impl, part), f"{machine} implementer 0x{impl:x} part 0x{part:x}")
+    return machine or "unknown"
+
+
+def host_cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            return parse_cpu_model(f.read(), platform.machine())
+    except OSError:
+        return platform.machine() or "unknown"
+
+
 def cpu_baseline(w: W.DecodeWorkload, cpu_budget_s: float = 20.0):
     """The oracle on a bounded sample: a prefix of the batch costing <= cpu_budget_s CPU
     seconds per step, repeated until about 10 CPU seconds have been spent."""
@@ -308,6 +343,7 @@ def cpu_baseline(w: W.DecodeWorkload, cpu_budget_s: float = 20.0):
         reps += 1
     gbs = sample_bytes(w, rows) * reps / secs / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_model": host_cpu_model(),
             "sample": f"{len(rows)} of {w.B} sequences of the {w.name} step (write + attention, "
                       f"all {w.Hq} heads) x {reps} repetitions, fp64 C oracle, {threads} threads, "
                       f"{secs:.2f} s wall"}
@@ -337,7 +373,7 @@ def run_reference(args):
             "config": {"workload": w.name, "description": W.CONFIGS[args.config]},
             "tokens_per_s": round(len(rows) * steps / secs, 2),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "cpu_model": host_cpu_model(), "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

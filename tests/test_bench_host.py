@@ -125,3 +125,14 @@ def test_reference_leg_runs(cfg, capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_cpu_model_parser():
+    x86 = "processor\t: 0\nvendor_id\t: GenuineIntel\nmodel name\t: Intel(R) Xeon(R) Platinum 8480+\n"
+    assert bench.parse_cpu_model(x86, "x86_64") == "Intel(R) Xeon(R) Platinum 8480+"
+    grace = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n"
+    assert bench.parse_cpu_model(grace, "aarch64") == "Arm Neoverse-V2"
+    other = "CPU implementer\t: 0x61\nCPU part\t: 0x022\n"
+    assert bench.parse_cpu_model(other, "aarch64") == "aarch64 implementer 0x61 part 0x22"
+    assert bench.parse_cpu_model("", "aarch64") == "aarch64"
+    assert isinstance(bench.host_cpu_model(), str) and bench.host_cpu_model()
