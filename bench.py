@@ -326,9 +326,9 @@ def parse_cpu_model(cpuinfo: str, machine: str) -> str:
 
 def host_cpu_model() -> str:
     try:
-        with open("/proc/cpuinfo") as f:
+        with open("/proc/cpuinfo", errors="replace") as f:
             return parse_cpu_model(f.read(), platform.machine())
-    except OSError:
+    except Exception:  # a descriptive field only: never fail the bench over it
         return platform.machine() or "unknown"
 
 
