@@ -17,6 +17,7 @@ of its own: weak scaling, no data-path collective); the barrier, the max over ra
 sum of bytes are the only communication.
 """
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -136,6 +137,27 @@ def profiled_traffic(workload: str):
         return int(entry["traffic_bytes_per_launch"])
     except (KeyError, TypeError, ValueError):
         return None
+
+
+@contextlib.contextmanager
+def nvtx_range(name: str):
+    """An NVTX range around a bench region (for ncu --nvtx or nsys); nothing if NVTX is not
+    available."""
+    pushed = False
+    try:
+        import torch
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:
+        pass
+    try:
+        yield
+    finally:
+        if pushed:
+            try:
+                torch.cuda.nvtx.range_pop()
+            except Exception:
+                pass
 
 
 def timed_loop(untimed, timed, min_ms: float, first: int, stream):
@@ -259,7 +281,9 @@ def cuda_launches_per_step(w: W.DecodeWorkload, chunk_used: int, cascade: bool =
 # the fp64 oracle on the host cores (cpu_baseline and --impl reference)
 # ------------------------------------------------------------------------------------------
 
-def oracle_step_seconds(w: W.DecodeWorkload, rows, threads: int) -> float:
+def oracle_step_seconds(w: W.DecodeWorkload, rows, threads: int, keep=None) -> float:
+    """Seconds of one oracle step (write + attention) over `rows`; with `keep` (a dict), also
+    keeps the rows and the fp64 output there."""
     import oracle
     kp, vp = w.k_pool, w.v_pool
     ks, vs = w.k_scales, w.v_scales
@@ -269,9 +293,24 @@ def oracle_step_seconds(w: W.DecodeWorkload, rows, threads: int) -> float:
                           None if w.k_new_scales is None else w.k_new_scales[rows],
                           None if w.v_new_scales is None else w.v_new_scales[rows],
                           ks, vs, inplace=True)
-    oracle.paged_decode_attention(w.q[rows], kp, vp, w.block_tables[rows], w.context_lens[rows],
-                                  w.scale, ks, vs, num_threads=threads)
-    return time.perf_counter() - t0
+    out = oracle.paged_decode_attention(w.q[rows], kp, vp, w.block_tables[rows], w.context_lens[rows],
+                                        w.scale, ks, vs, num_threads=threads)
+    dt = time.perf_counter() - t0
+    if keep is not None:
+        keep["rows"], keep["out"] = rows, out
+    return dt
+
+
+def accuracy_vs_oracle(gpu_out, ref, rows) -> dict:
+    """Max and mean |GPU - oracle| over the checked rows (the GPU output cast up to fp64)."""
+    got = np.asarray(gpu_out, dtype=np.float64)[np.asarray(rows)]
+    d = np.abs(got - ref)
+    finite = np.isfinite(d)
+    fin = lambda v: float(v) if np.isfinite(v) else None
+    return {"max_abs_err": fin(d[finite].max()) if finite.any() else None,
+            "mean_abs_err": fin(d[finite].mean()) if finite.any() else None,
+            "max_abs_ref": fin(np.abs(ref).max()), "nonfinite": int((~finite).sum()),
+            "rows_checked": int(len(rows)), "elements_checked": int(d.size)}
 
 
 def sample_rows(w: W.DecodeWorkload, cpu_budget_s: float):
@@ -332,14 +371,15 @@ def host_cpu_model() -> str:
         return platform.machine() or "unknown"
 
 
-def cpu_baseline(w: W.DecodeWorkload, cpu_budget_s: float = 20.0):
+def cpu_baseline(w: W.DecodeWorkload, cpu_budget_s: float = 20.0, keep=None):
     """The oracle on a bounded sample: a prefix of the batch costing <= cpu_budget_s CPU
-    seconds per step, repeated until about 10 CPU seconds have been spent."""
+    seconds per step, repeated until about 10 CPU seconds have been spent (`keep`: see
+    oracle_step_seconds)."""
     threads = os.cpu_count() or 1
     rows = sample_rows(w, cpu_budget_s)
     secs, reps = 0.0, 0
     while reps == 0 or (secs * threads < 10.0 and reps < 50):
-        secs += oracle_step_seconds(w, rows, threads)
+        secs += oracle_step_seconds(w, rows, threads, keep)
         reps += 1
     gbs = sample_bytes(w, rows) * reps / secs / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -519,20 +559,22 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for k in range(K):
-        flush_l2(k)                      # evict the previous step's lines (not timed)
-        ev[k][0].record(stream)
-        write()
-        attend()
-        ev[k][1].record(stream)
-    torch.cuda.synchronize()
+    with nvtx_range("timed steps (write + attention)"):
+        for k in range(K):
+            flush_l2(k)                      # evict the previous step's lines (not timed)
+            ev[k][0].record(stream)
+            write()
+            attend()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     wall_s = time.perf_counter() - t_wall
     step_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     # the dominant kernels alone (the attention call: split + merge), for the roofline: at least
     # MIN_LOOP_MS of GPU time whatever K is
-    attn_total_ms, KA = timed_loop(flush_l2, lambda k: attend(), args.min_loop_ms, K, stream)
+    with nvtx_range("attention calls (roofline loop)"):
+        attn_total_ms, KA = timed_loop(flush_l2, lambda k: attend(), args.min_loop_ms, K, stream)
 
     step_bytes = W.kv_bytes(w)
     total_bytes, max_ms = aggregate(step_bytes * K, step_ms)
@@ -553,7 +595,8 @@ def run_ours(args):
         write()
         attend()
         host_out.copy_(out, non_blocking=True)
-    e2e_ms, KE = timed_loop(flush_l2, e2e_step, args.min_loop_ms, K, stream)
+    with nvtx_range("e2e steps (host copies + write + attention)"):
+        e2e_ms, KE = timed_loop(flush_l2, e2e_step, args.min_loop_ms, K, stream)
     e2e_bytes, e2e_max = aggregate(step_bytes * KE, e2e_ms)
     e2e_value = e2e_bytes / (e2e_max / 1e3) / 1e9
     clk = clocks.stop()
@@ -579,7 +622,8 @@ def run_ours(args):
                    "shared_prefix_call": bool(cascade),
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write, then a "
                          f"{(L2_FLUSH_BYTES // 2) * 4 >> 20} MB read so no dirty line is left; untimed)",
-                   "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
+                   "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}",
+                   "seed": rank_seed(args.config, rank)},
         "tokens_per_s": round(tokens_per_s, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
@@ -602,7 +646,14 @@ def run_ours(args):
                          "(the timed steps, the roofline loop and the e2e loop)")
         line["clocks"] = clk
     if not args.no_cpu and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w)
+        # the last e2e step's output (the same inputs every step), against the oracle on the rows
+        # the baseline leg computes anyway
+        gpu_out = host_out.float().numpy()
+        kept = {}
+        line["cpu_baseline"] = cpu_baseline(w, keep=kept)
+        line["accuracy"] = {**accuracy_vs_oracle(gpu_out, kept["out"], kept["rows"]),
+                            "reference": "fp64 oracle on the cpu_baseline sample's rows",
+                            "output_dtype": str(out.dtype).replace("torch.", "")}
     if world == 1 and not args.no_secondary:
         # the other workloads, each as its own record (the headline keys above stay as they are):
         # the Llama-3-8B GQA batch, the INT8 batch, the shared-prefix batch, and the paged prefill

@@ -1,5 +1,7 @@
 """Host logic of bench.py without a GPU: the N-rank aggregation over gloo (world size 2), seeds,
-byte models, the clock-log parser and the staleness rule for profiled traffic."""
+byte models, the clock-log parser, the staleness rule for profiled traffic, the CPU model and the
+accuracy record."""
+import json
 import os
 import socket
 
@@ -136,3 +138,25 @@ def test_cpu_model_parser():
     assert bench.parse_cpu_model(other, "aarch64") == "aarch64 implementer 0x61 part 0x22"
     assert bench.parse_cpu_model("", "aarch64") == "aarch64"
     assert isinstance(bench.host_cpu_model(), str) and bench.host_cpu_model()
+
+
+def test_accuracy_record_against_the_oracle_rows():
+    ref = np.zeros((3, 2, 4))
+    ref[1] = 1.0
+    gpu = np.zeros((5, 2, 4), dtype=np.float32)
+    gpu[2] = 1.0 + 2 ** -8      # row 2 of the batch is the second checked row
+    gpu[0, 0, 0] = 0.5
+    acc = bench.accuracy_vs_oracle(gpu, ref, [0, 2, 4])
+    assert acc["max_abs_err"] == 0.5
+    assert abs(acc["mean_abs_err"] - (0.5 + 8 * 2 ** -8) / 24) < 1e-12
+    assert acc["max_abs_ref"] == 1.0 and acc["nonfinite"] == 0
+    assert acc["rows_checked"] == 3 and acc["elements_checked"] == 24
+    gpu[4, 1, 3] = np.nan
+    acc = bench.accuracy_vs_oracle(gpu, ref, [0, 2, 4])
+    assert acc["nonfinite"] == 1 and acc["max_abs_err"] == 0.5
+    json.dumps(acc, allow_nan=False)  # no NaN or inf reaches the JSON line
+
+
+def test_nvtx_range_never_fails():
+    with bench.nvtx_range("region"):
+        pass
