@@ -502,6 +502,17 @@ __global__ void PKV_MMA_BOUNDS mma_split_kernel(const SplitParams p,
                 // score multipliers: the K scale (INT8) or scale * log2(e) (bf16) per token row
                 float vs0 = 1.f, vs1 = 1.f, ks0 = score_mult, ks1 = score_mult;
                 if constexpr (kI8) {
+                    // A block that ends the context: the V scales of its slots past the context
+                    // may be any bits (NaN included), and those tokens' weights of 0 times NaN
+                    // would poison O, so they are zeroed here (their K scores are masked to -inf
+                    // below). The fence orders these writes before the stage's next bulk copy.
+                    if (nvalid < kBlockSize) {
+                        if (lane < kBlockSize - nvalid) {
+                            scl[st * 2 * kBlockSize + kBlockSize + nvalid + lane] = 0.f;
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        }
+                        __syncwarp();
+                    }
                     const float* sc = scl + st * 2 * kBlockSize;
                     ks0 = sc[r] * score_mult;
                     ks1 = sc[r + 8] * score_mult;

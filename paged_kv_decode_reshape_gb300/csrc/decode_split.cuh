@@ -278,7 +278,9 @@ __global__ void __launch_bounds__(128) split_kernel(const SplitParams p) {
                 float vf[8];
                 load8_f32<KV>(vt + (tok * D + slice * 8) * sizeof(KV), vf);
                 float vs = 1.f;
-                if constexpr (kI8) vs = reinterpret_cast<const float*>(kt + 2 * TILE + kBlockSize * 4)[tok];
+                // (a token past the context weighs 0; its scale may be any bits, NaN included, so
+                // it is not read into the product)
+                if constexpr (kI8) vs = valid[pp] ? reinterpret_cast<const float*>(kt + 2 * TILE + kBlockSize * 4)[tok] : 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) vf[e] = valid[pp] ? vf[e] : 0.f;  // rows past the context
 #pragma unroll

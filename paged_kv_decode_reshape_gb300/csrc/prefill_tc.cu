@@ -520,6 +520,15 @@ __global__ void __launch_bounds__(PfGeom<kI8>::Threads, 1) prefill_kernel(const 
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads them async
+            if (g == 1) {
+                // keys past the CTA's last visible key weigh 0, but their V scales may be any bits
+                // (NaN included) and 0 * NaN would poison O: zero them (the softmax reads the scale
+                // row only after full(1), which this thread completes below)
+                float* vsr = reinterpret_cast<float*>(smem + Gm::OffScl) + ridx(1, st) * 8 * kBlockSize;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    if (t * kPfK + c + 64 * kk >= n_tile_max) vsr[c + 64 * kk] = 0.f;
+            }
             mbar_arrive(full(g, st));
         }
     } else if (warp == kPfMmaWarp || warp == kPfMmaWarpPV) {

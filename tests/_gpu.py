@@ -99,3 +99,13 @@ def assert_close(got, ref, kind, what=""):
     assert m <= mx and a <= mean and r <= rel, (
         f"{what}: max-abs {m:.3g} (<= {mx}), mean-abs {a:.3g} (<= {mean}), rel-L2 {r:.3g} (<= {rel})")
     return m, a, r
+
+
+def dead_slots(block_tables, context_lens, NB, BS):
+    """[NB, BS] True where no sequence's context reaches (the first context_lens[b] positions of
+    table b are live; every other slot of every block is dead)."""
+    live = np.zeros((NB, BS), dtype=bool)
+    for b, n in enumerate(np.asarray(context_lens)):
+        for t0 in range(0, int(n), BS):
+            live[int(block_tables[b][t0 // BS]), :min(BS, int(n) - t0)] = True
+    return ~live

@@ -74,3 +74,14 @@ def test_bf16_rounding_is_nearest_even():
     back = W.bf16_bits_to_f32(bits)
     assert back[0] == 1.0 and back[1] == 1.0 and back[2] == 1.0 + 2**-6 and back[3] == -2.5
     assert abs(back[4] - 1e-3) <= 1e-3 * 2**-8
+
+
+def test_dead_slot_map_on_a_hand_made_table():
+    """The dead-slot rule the GPU sentinel tests fill with NaN: two sequences sharing block 0,
+    lengths 20 and 16."""
+    from _gpu import dead_slots
+    bt = np.array([[0, 2, -1], [0, -1, -1]], dtype=np.int32)
+    dead = dead_slots(bt, np.array([20, 16]), NB=4, BS=16)
+    assert not dead[0].any()                       # full, shared
+    assert not dead[2, :4].any() and dead[2, 4:].all()
+    assert dead[1].all() and dead[3].all()         # referenced by no table
