@@ -51,6 +51,12 @@
  * a context_len above max_blocks_per_seq * block_size) are never dereferenced: the kernels
  * skip them and, when `status` is non-NULL, OR a PKV_FLAG_* bit into that device int32.
  * The caller clears it; the library only sets bits.
+ *
+ * Pool contents: only the first context_lens[b] slots of each table are read into a result. The
+ * other slots of a sequence's last block, and blocks no table references, may hold any bits (stale
+ * tokens, NaN, never-written memory; INT8: any scales) without changing an output: K scores past
+ * the context are masked to -inf and their V rows (bf16 / fp32) or V scales (INT8) are zeroed or
+ * not read before a weight of 0 could meet them. Outputs are written in their own rows only.
  */
 #ifndef PKV_H
 #define PKV_H
