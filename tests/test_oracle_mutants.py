@@ -49,6 +49,21 @@ MUTANTS = [
     ("merge sum not weighted", [("L += l[base + j] * w;", "L += l[base + j];", 1)]),
     ("split ranges overlap by a token", [("int lo = j * per, hi = lo + per < n ? lo + per : n;",
                                           "int lo = j * per, hi = lo + per + 1 < n ? lo + per + 1 : n;", 1)]),
+    ("prefill query row from the sequence index", [("size_t r = (size_t)(query_start[b] + i) * Hq + h;",
+                                                   "size_t r = (size_t)(b + i) * Hq + h;", 1)]),
+    ("multi-token rows transposed", [("size_t r = (size_t)(b * L + l) * Hq + h;",
+                                      "size_t r = (size_t)(l * B + b) * Hq + h;", 1)]),
+    ("prefill skips the first key", [("rc = partial_q(&P, r * D, b, h, 0, n_i, &m, &lsum, acc, s, row);",
+                                      "rc = partial_q(&P, r * D, b, h, 1, n_i, &m, &lsum, acc, s, row);", 1)]),
+    ("prefill output not normalised",
+     [("rc = partial_q(&P, r * D, b, h, 0, n_i, &m, &lsum, acc, s, row);\n"
+       "                if (rc) break;\n"
+       "                double* o = out + r * D;\n"
+       "                for (int d = 0; d < D; ++d) o[d] = acc[d] / lsum;",
+       "rc = partial_q(&P, r * D, b, h, 0, n_i, &m, &lsum, acc, s, row);\n"
+       "                if (rc) break;\n"
+       "                double* o = out + r * D;\n"
+       "                for (int d = 0; d < D; ++d) o[d] = acc[d];", 1)]),
 ]
 
 
