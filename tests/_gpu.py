@@ -109,3 +109,20 @@ def dead_slots(block_tables, context_lens, NB, BS):
         for t0 in range(0, int(n), BS):
             live[int(block_tables[b][t0 // BS]), :min(BS, int(n) - t0)] = True
     return ~live
+
+
+def prefill_rows_by_decode(w, rows, num_threads=8, orc=None):
+    """Oracle rows of a paged prefill, each computed as the decode query it is by definition:
+    query row i of sequence b attends to the first context_lens[b] - (L_b - 1 - i) tokens of its
+    table. `rows` are flat query-token rows; returns fp64 [len(rows), Hq, D]. `orc`: the oracle
+    module to use (default: the oracle)."""
+    orc = oracle if orc is None else orc
+    rows = np.asarray(rows)
+    qs = np.asarray(w.query_start)
+    b = np.searchsorted(qs, rows, side="right") - 1
+    L = qs[b + 1] - qs[b]
+    i = rows - qs[b]
+    n = np.asarray(w.context_lens)[b] - (L - 1 - i)
+    return orc.paged_decode_attention(w.q[rows], w.k_pool, w.v_pool, np.asarray(w.block_tables)[b],
+                                         n.astype(np.int32), w.scale, w.k_scales, w.v_scales,
+                                         num_threads=num_threads)

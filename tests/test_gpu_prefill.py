@@ -6,7 +6,7 @@ import pytest
 import oracle
 import paged_kv_decode_reshape_gb300 as P
 import workloads as W
-from _gpu import assert_close, to_dev, to_f64
+from _gpu import assert_close, prefill_rows_by_decode, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -127,4 +127,28 @@ def test_prefill_reference_raised_on_alternate_tiles(growth):
     ref = oracle.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
                                          w.query_start, w.scale)
     assert_close(got, ref, "bf16", f"prefill rising keys x{growth}")
+    assert int(st.item()) == 0
+
+
+def full_size_rows(w, per_seq=(0, 1, 2, 127, 128, 129, 2047, 2048, 4094, 4095)):
+    """Rows of every sequence spread over the first, a middle and the last query tile (the tile
+    edges, where the causal limit and the tile split meet)."""
+    qs = np.asarray(w.query_start)
+    return np.concatenate([qs[b] + np.asarray([i for i in per_seq if i < qs[b + 1] - qs[b]])
+                           for b in range(len(qs) - 1)])
+
+
+def test_prefill_full_size_sampled_rows():
+    """The bench's prefill workload at full size (4 sequences x 4096 new tokens after 2048 cached,
+    Llama-3-8B heads) through the same call the bench times, every head of sampled rows of every
+    sequence against the oracle (each row as the decode query it is)."""
+    import os
+    w = W.make_prefill(name="prefill_llama3_8b", query_lens=[4096] * 4, cached_lens=[2048] * 4,
+                       Hq=32, Hkv=8, D=128, seed=7)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill(w, st)
+    rows = full_size_rows(w)
+    ref = prefill_rows_by_decode(w, rows, num_threads=os.cpu_count() or 8)
+    assert_close(got[rows], ref, "bf16", f"full-size prefill, {rows.size} rows x 32 heads")
+    assert np.all(np.isfinite(got))
     assert int(st.item()) == 0

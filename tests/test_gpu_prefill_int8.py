@@ -9,7 +9,7 @@ import pytest
 import oracle
 import paged_kv_decode_reshape_gb300 as P
 import workloads as W
-from _gpu import assert_close, to_dev, to_f64
+from _gpu import assert_close, prefill_rows_by_decode, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -153,4 +153,22 @@ def test_prefill_int8_outlier_query_magnitudes(mag, ndims, k_mult):
     got = run_prefill_i8(w, st)
     assert np.all(np.isfinite(got))
     assert_close(got, reference(w), "i8", f"INT8 prefill |q| {mag} in {ndims} dims, keys x {k_mult}")
+    assert int(st.item()) == 0
+
+
+def test_prefill_int8_full_size_sampled_rows():
+    """The bench's INT8 prefill workload at full size (4 x 4096 new tokens after 2048 cached,
+    Llama-3-8B heads) through the call the bench times, every head of sampled rows of every
+    sequence (first, middle and last query tiles and their edges) against the oracle."""
+    import os
+    w = W.make_prefill(name="prefill_llama3_8b_int8", query_lens=[4096] * 4, cached_lens=[2048] * 4,
+                       Hq=32, Hkv=8, D=128, seed=7, kv_dtype="i8")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_prefill_i8(w, st)
+    qs = np.asarray(w.query_start)
+    rows = np.concatenate([qs[b] + np.asarray([0, 1, 2, 127, 128, 129, 2047, 2048, 4094, 4095])
+                           for b in range(w.B)])
+    ref = prefill_rows_by_decode(w, rows, num_threads=os.cpu_count() or 8)
+    assert_close(got[rows], ref, "i8", f"full-size INT8 prefill, {rows.size} rows x 32 heads")
+    assert np.all(np.isfinite(got))
     assert int(st.item()) == 0

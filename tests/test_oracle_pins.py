@@ -504,3 +504,17 @@ def test_prefill_int8_matches_library_causal_attention(orc):
             torch.from_numpy(V).repeat_interleave(2, 0), is_causal=True, scale=w.scale)
         np.testing.assert_allclose(out[w.query_start[b]:w.query_start[b + 1]],
                                    ref.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "i8"])
+def test_prefill_rows_are_decode_queries_at_their_causal_limits(orc, kv):
+    """Each prefill row is, by definition, one decode query: row i of a sequence with L new tokens
+    attends to the first context_len - (L - 1 - i) tokens of its table. The prefill equals the
+    decode oracle run row by row with those limits, bit for bit (this is also how the full-size GPU
+    tests get their sampled rows)."""
+    from _gpu import prefill_rows_by_decode
+    w = W.make_prefill(name="p", query_lens=[37, 1, 20, 5], cached_lens=[5, 0, 30, 16], Hq=4, Hkv=2,
+                       D=64, seed=21, kv_dtype=kv)
+    full = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                       w.query_start, w.scale, w.k_scales, w.v_scales)
+    assert np.array_equal(full, prefill_rows_by_decode(w, np.arange(w.q.shape[0]), orc=orc))
