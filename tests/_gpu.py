@@ -126,3 +126,26 @@ def prefill_rows_by_decode(w, rows, num_threads=8, orc=None):
     return orc.paged_decode_attention(w.q[rows], w.k_pool, w.v_pool, np.asarray(w.block_tables)[b],
                                          n.astype(np.int32), w.scale, w.k_scales, w.v_scales,
                                          num_threads=num_threads)
+
+
+def poisoned(w):
+    """A copy of workload w with NaN in every dead slot (dead_slots): bf16 / fp32 K and V rows, or
+    for an INT8 cache the K and V scales."""
+    NB, Hkv, BS, D = w.k_pool.shape
+    dead = dead_slots(w.block_tables, w.context_lens, NB, BS)
+    rep = {}
+    if w.kv_dtype == "i8":
+        m = np.broadcast_to(dead[:, None, :], w.k_scales.shape)
+        for name in ("k_scales", "v_scales"):
+            a = getattr(w, name).copy()
+            a[m] = np.nan
+            rep[name] = a
+    else:
+        m = np.broadcast_to(dead[:, None, :, None], w.k_pool.shape)
+        nan = np.uint16(0x7FC0) if w.k_pool.dtype == np.uint16 else np.float32(np.nan)
+        for name in ("k_pool", "v_pool"):
+            a = getattr(w, name).copy()
+            a[m] = nan
+            rep[name] = a
+    assert dead.any(), "the workload leaves no slot dead"
+    return type(w)(**{**w.__dict__, **rep})

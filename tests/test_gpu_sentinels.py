@@ -15,41 +15,18 @@ import pytest
 import oracle
 import paged_kv_decode_reshape_gb300 as P
 import workloads as W
-from _gpu import DevWorkload, assert_close, dead_slots, oracle_step, to_dev, to_f64
+from _gpu import DevWorkload, assert_close, oracle_step, poisoned, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 GUARD = 3                # guard rows before and after the output
-BF16_NAN = 0x7FC0
 
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib(pkv):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-
-
-def poisoned(w):
-    """A copy of workload w with NaN in every dead slot (see the module docstring)."""
-    NB, Hkv, BS, D = w.k_pool.shape
-    dead = dead_slots(w.block_tables, w.context_lens, NB, BS)
-    rep = {}
-    if w.kv_dtype == "i8":
-        m = np.broadcast_to(dead[:, None, :], w.k_scales.shape)
-        for name in ("k_scales", "v_scales"):
-            a = getattr(w, name).copy()
-            a[m] = np.nan
-            rep[name] = a
-    else:
-        m = np.broadcast_to(dead[:, None, :, None], w.k_pool.shape)
-        nan = np.uint16(BF16_NAN) if w.k_pool.dtype == np.uint16 else np.float32(np.nan)
-        for name in ("k_pool", "v_pool"):
-            a = getattr(w, name).copy()
-            a[m] = nan
-            rep[name] = a
-    assert dead.any(), "the workload leaves no slot dead"
-    return type(w)(**{**w.__dict__, **rep})
 
 
 def guarded(shape, dtype):

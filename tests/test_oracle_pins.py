@@ -518,3 +518,36 @@ def test_prefill_rows_are_decode_queries_at_their_causal_limits(orc, kv):
     full = orc.paged_prefill_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
                                        w.query_start, w.scale, w.k_scales, w.v_scales)
     assert np.array_equal(full, prefill_rows_by_decode(w, np.arange(w.q.shape[0]), orc=orc))
+
+
+@pytest.mark.parametrize("kv", ["f32", "bf16", "i8"])
+def test_oracle_reads_no_slot_past_a_context(orc, kv):
+    """The oracle reads only the first context_len positions of each table: NaN in every other slot
+    and in every unreferenced block (rows, or INT8 scales) leaves its decode, multi-token and
+    prefill answers bit-identical and finite. The GPU sentinel tests compare against exactly this."""
+    from _gpu import poisoned
+    q_dtype = "f32" if kv == "f32" else "bf16"
+    w = W.make_decode(name="d", B=4, Hq=8, Hkv=2, D=64, context_lens=[5, 33, 250, 17], kv_dtype=kv,
+                      q_dtype=q_dtype, seed=90)
+    pw = poisoned(w)
+    a = orc.paged_decode_attention(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale,
+                                   w.k_scales, w.v_scales)
+    b = orc.paged_decode_attention(pw.q, pw.k_pool, pw.v_pool, pw.block_tables, pw.context_lens,
+                                   pw.scale, pw.k_scales, pw.v_scales)
+    assert np.all(np.isfinite(a)) and np.array_equal(a, b)
+    m = W.make_multi_token(w, 3, seed=91)
+    pm = poisoned(m)
+    a = orc.paged_decode_attention_multi(m.q, m.k_pool, m.v_pool, m.block_tables, m.context_lens,
+                                         m.scale, m.k_scales, m.v_scales)
+    b = orc.paged_decode_attention_multi(pm.q, pm.k_pool, pm.v_pool, pm.block_tables, pm.context_lens,
+                                         pm.scale, pm.k_scales, pm.v_scales)
+    assert np.all(np.isfinite(a)) and np.array_equal(a, b)
+    if kv != "f32":
+        p = W.make_prefill(name="p", query_lens=[20, 1, 7], cached_lens=[13, 40, 0], Hq=4, Hkv=2, D=64,
+                           seed=92, kv_dtype=kv)
+        pp = poisoned(p)
+        a = orc.paged_prefill_attention(p.q, p.k_pool, p.v_pool, p.block_tables, p.context_lens,
+                                        p.query_start, p.scale, p.k_scales, p.v_scales)
+        b = orc.paged_prefill_attention(pp.q, pp.k_pool, pp.v_pool, pp.block_tables, pp.context_lens,
+                                        pp.query_start, pp.scale, pp.k_scales, pp.v_scales)
+        assert np.all(np.isfinite(a)) and np.array_equal(a, b)
