@@ -360,3 +360,51 @@ def test_oracle_prefix_hits_count_their_references():
     assert t1[0] not in ob.free and t1[1] not in ob.free and len(ob.free) == 16 - 3
     ob.free_seq(1)
     assert len(ob.free) == 16 and all(u == 0 for u in ob.users)
+
+
+@pytest.mark.parametrize("prefix_cache", [True, False])
+def test_decode_loop_preempting_from_the_tail_matches_oracle(pkv, prefix_cache):
+    """Decode scheduling on a small pool ("AMD ATOM inference engine", section 5: can_append before
+    each decode step, preemption when the KV blocks run out): every running sequence appends one
+    token per step; when the pool cannot take a sequence's token, the most recently admitted
+    running sequence (the tail of the running queue) is preempted -- its blocks freed -- until it
+    can, or until the sequence itself is the one preempted. The native manager and the oracle
+    agree on every decision and on every slot, table and free count; preempted sequences are
+    admitted again (recomputed from their tokens) when the whole prompt fits."""
+    rng = np.random.default_rng(11)
+    NB = 14
+    bm, ob = P.BlockManager(NB, 16, prefix_cache), O.BlockManager(NB, 16, prefix_cache)
+    tokens = {sid: list(rng.integers(0, 1000, int(rng.integers(5, 40)))) for sid in range(8)}
+    waiting, running, preemptions, next_id, ids = list(range(8)), [], 0, 100, {}
+    for step in range(80):
+        # admit waiting sequences (first come, first served) while their tokens fit
+        while waiting and ob.can_allocate(len(tokens[waiting[0]])):
+            s = waiting.pop(0)
+            assert bm.can_allocate(len(tokens[s]))
+            ids[s], next_id = next_id, next_id + 1   # a re-admitted sequence gets a fresh id
+            assert bm.allocate(ids[s], tokens[s]) == ob.allocate(ids[s], tokens[s])
+            running.append(s)
+        if waiting:
+            assert not bm.can_allocate(len(tokens[waiting[0]]))
+        for s in list(running):
+            if s not in running:
+                continue
+            while not ob.can_append(ids[s], 1):
+                assert not bm.can_append(ids[s], 1)
+                victim = running.pop()                # the tail of the running queue
+                bm.free(ids[victim])
+                ob.free_seq(ids[victim])
+                waiting.insert(0, victim)             # back to the head of the waiting queue
+                preemptions += 1
+                if victim == s:
+                    break
+            if s not in running:
+                continue
+            assert bm.can_append(ids[s], 1)
+            t = [int(rng.integers(0, 1000))]
+            slots, copies = bm.append_cow(ids[s], t)
+            oslots, ocopies = ob.append(ids[s], t)
+            assert np.array_equal(slots, oslots) and copies == ocopies
+            tokens[s] += t
+        _compare(bm, ob, [ids[s] for s in running])
+    assert preemptions > 0 and running   # the pool did run out, and decoding went on
