@@ -1,5 +1,7 @@
 """Helpers for the GPU parity tests: move a seeded workload to the device, run one decode step
-through the C ABI binding, and compute the oracle's answer for the same inputs."""
+through the C ABI binding, and compute the oracle's answer for the same inputs (also for sampled
+rows of a prefill, each as the decode query it is); the dead-slot map of a batch's tables and a
+copy of a workload with NaN in those slots."""
 import numpy as np
 
 import oracle
